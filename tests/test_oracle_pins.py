@@ -1,0 +1,376 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each test ties one part of the oracle to something fixed independently: a value printed in
+QUADS (arXiv 2607.15810) §2.2 (the E2M1 grid, E4M3 with maximum 448), a hand-worked example,
+a library routine (torch's float8_e4m3fn and bfloat16 casts, torch fp32 matmul), a closed form
+or invariant of the method (odd symmetry, power-of-two scale invariance, Eq. (22)), or brute
+force on small inputs.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from nvfp4_w4a4_quantized_quantize_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _grid():
+    with open(os.path.join(GOLDEN, "e2m1_grid.txt")) as f:
+        line = [l for l in f if not l.startswith("#")][0]
+    return [float(v) for v in line.split()]
+
+
+def _f32_bits(a):
+    return np.asarray(a, np.float32).view(np.uint32)
+
+
+# ------------------------------------------------------------------------------ formats
+def test_e2m1_decode_matches_printed_grid():
+    grid = _grid()
+    assert [oracle.e2m1_value(c) for c in range(8)] == grid
+    assert [oracle.e2m1_value(8 | c) for c in range(8)] == [-g for g in grid]
+    assert math.copysign(1.0, oracle.e2m1_value(8)) == -1.0
+
+
+def test_e4m3_decode_matches_paper_and_torch():
+    spec = dict(l.split() for l in open(os.path.join(GOLDEN, "e4m3_format.txt")) if not l.startswith("#"))
+    vals = np.array([oracle.e4m3_value(b) for b in range(256)])
+    finite = vals[np.isfinite(vals)]
+    assert finite.max() == float(spec["max"])
+    assert np.isnan(vals[0x7F]) and np.isnan(vals[0xFF])
+    assert np.count_nonzero(np.isfinite(vals[:128])) == 127
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ok = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(vals), ok)
+    assert np.array_equal(vals[ok], ref[ok])
+
+
+def test_e4m3_encode_against_torch_cast():
+    rng = np.random.default_rng(5)
+    # every fp32 value that is an E4M3 midpoint or neighbour, plus random values over [0, 448]
+    pos = np.array([oracle.e4m3_value(b) for b in range(0x7F)])
+    mids = (pos[:-1] + pos[1:]) / 2
+    t = np.concatenate([pos, mids, np.nextafter(mids, 0), np.nextafter(mids, 1000),
+                        rng.uniform(0, 448, 20000), 2.0 ** rng.uniform(-14, 8.8, 20000)])
+    t = t.astype(np.float32)
+    t = t[t <= 448]
+    got = oracle.e4m3_encode(t)
+    ref = torch.from_numpy(t).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, ref)
+    # saturation (reading R3): above 448 -> 448
+    big = np.array([448.0, 449.0, 464.0, 480.0, 1e6, 3e38], np.float32)
+    assert np.all(oracle.e4m3_encode(big) == 0x7E)
+
+
+def test_e2m1_encode_is_nearest_with_even_ties_exhaustive():
+    grid = np.array(_grid())
+    allbits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    v = wl.bf16_bits_to_f32(allbits)
+    v = v[np.isfinite(v)]
+    for scale in [1.0, 0.5, 2.0, 0.125, 3.0, 6.2222223, 1.7, 0.01]:
+        with np.errstate(over="ignore"):
+            y = (v * np.float32(scale)).astype(np.float32)
+        y = y[np.isfinite(y)]
+        c = oracle.e2m1_encode(y)
+        a = np.abs(y.astype(np.float64))
+        d = np.abs(a[:, None] - grid[None, :])
+        best = d.min(axis=1)
+        mag = c & 7
+        assert np.all(d[np.arange(a.size), mag] == best), "not a nearest grid value"
+        tie = (d == best[:, None]).sum(axis=1) > 1
+        assert np.all(mag[tie] % 2 == 0), "tie not resolved to the even magnitude index"
+        assert np.array_equal((c >> 3).astype(bool), np.signbit(y)), "sign bit not kept"
+
+
+def test_e2m1_tie_examples():
+    cases = [(0.25, 0), (0.75, 2), (1.25, 2), (1.75, 4), (2.5, 4), (3.5, 6), (5.0, 6), (7.0, 7),
+             (1e9, 7), (-0.25, 8), (-5.0, 14), (0.0, 0), (-0.0, 8), (0.2499, 0), (0.2501, 1)]
+    got = oracle.e2m1_encode(np.array([v for v, _ in cases], np.float32))
+    assert [int(g) for g in got] == [c for _, c in cases]
+
+
+def test_bf16_round_against_torch():
+    rng = np.random.default_rng(1)
+    f = np.concatenate([rng.standard_normal(50000) * 10.0 ** rng.uniform(-30, 30, 50000),
+                        [0.0, -0.0, 1.0, 1.00390625, 1.005859375, 65504.0, 3e38]]).astype(np.float32)
+    got = oracle.bf16_round(f)
+    ref = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+# ------------------------------------------------------------------------------ quantizer
+def test_hand_worked_block_example():
+    ex = json.load(open(os.path.join(GOLDEN, "nvfp4_block_example.json")))
+    x = wl.to_bf16_bits(np.array(ex["x"], np.float64))[None, :]
+    assert np.array_equal(wl.bf16_bits_to_f32(x)[0], np.array(ex["x"], np.float32))
+    ts = oracle.tensor_scale(x)
+    assert ts.amax == ex["amax"] and ts.s_enc == ex["s_enc"]
+    codes, scales = oracle.quantize(x, ts)
+    assert [f"0x{b:02x}" for b in scales[0]] == ex["block_scale_bytes"]
+    unpacked = np.stack([codes[0] & 15, codes[0] >> 4], axis=1).ravel()
+    expect = np.array([int(c, 16) for blk in ex["codes"] for c in blk])
+    assert np.array_equal(unpacked, expect)
+
+
+def _rand_x(M, K, seed, outliers=3):
+    x, _ = wl.activations(M, K, seed, "normal", 1.0, outliers, 16.0)
+    return x
+
+
+def test_round_trip_of_grid_values():
+    grid = _grid()
+    for j in [-8, -3, 0, 2, 5]:
+        vals = np.array([g * 2.0 ** j for g in grid] + [-g * 2.0 ** j for g in grid])
+        x = wl.to_bf16_bits(vals)[None, :]
+        ts = oracle.tensor_scale(x)
+        codes, scales = oracle.quantize(x, ts)
+        dq = oracle.dequantize(codes, scales, ts.s_dec)[0]
+        assert np.allclose(dq, vals, rtol=1e-6, atol=0)
+        unpacked = np.stack([codes[0] & 15, codes[0] >> 4], axis=1).ravel()
+        assert list(unpacked[:8]) == list(range(8))
+        assert list(unpacked[8:]) == [8 | c for c in range(8)]
+
+
+def test_saturation_and_scale_representability():
+    x = _rand_x(64, 512, 3)
+    ts = oracle.tensor_scale(x)
+    codes, scales = oracle.quantize(x, ts)
+    sv = np.array([oracle.e4m3_value(b) for b in range(256)])
+    assert np.all(scales <= 0x7E), "every block scale is a finite non-negative E4M3 <= 448"
+    dq = oracle.dequantize(codes, scales, ts.s_dec)
+    d_b = (sv[scales].astype(np.float32) * np.float32(ts.s_dec)).astype(np.float32)
+    assert np.all(np.abs(dq) <= 6.0 * np.repeat(d_b, 16, axis=1) * (1 + 1e-7))
+    # the tensor amax maps to the top of the E4M3 x E2M1 range
+    i, j = np.unravel_index(np.argmax(np.abs(wl.bf16_bits_to_f32(x))), x.shape)
+    assert scales[i, j // 16] in (0x7E, 0x7D)
+
+
+def test_power_of_two_scale_invariance():
+    x = _rand_x(32, 256, 4)
+    xf = wl.bf16_bits_to_f32(x)
+    ts = oracle.tensor_scale(x)
+    c0, s0 = oracle.quantize(x, ts)
+    for j in [-6, -1, 1, 7]:
+        x2 = wl.to_bf16_bits(xf.astype(np.float64) * 2.0 ** j)
+        ts2 = oracle.tensor_scale(x2)
+        c2, s2 = oracle.quantize(x2, ts2)
+        assert np.array_equal(c0, c2) and np.array_equal(s0, s2)
+        assert ts2.s_dec == np.float32(ts.s_dec * 2.0 ** j)
+
+
+def test_odd_symmetry():
+    x = _rand_x(32, 256, 5)
+    xn = x ^ np.uint16(0x8000)
+    ts = oracle.tensor_scale(x)
+    c, s = oracle.quantize(x, ts)
+    cn, sn = oracle.quantize(xn, oracle.tensor_scale(xn))
+    assert np.array_equal(s, sn)
+    assert np.array_equal(cn, c ^ np.uint8(0x88))
+
+
+def test_block_encoding_is_nearest_for_the_block_scale():
+    """Brute force: given each block's scale, every code is the nearest grid value of x * e_b,
+    and the block scale is the E4M3 rounding of fl(amax_b / 6) * S_enc."""
+    x = _rand_x(16, 128, 6)
+    xf = wl.bf16_bits_to_f32(x)
+    ts = oracle.tensor_scale(x)
+    codes, scales = oracle.quantize(x, ts)
+    grid = np.array(_grid())
+    sv = np.array([oracle.e4m3_value(b) for b in range(256)])
+    for i in range(16):
+        for b in range(8):
+            blk = xf[i, b * 16:(b + 1) * 16]
+            t = np.float32(np.float32(np.abs(blk).max() / np.float32(6)) * np.float32(ts.s_enc))
+            assert scales[i, b] == np.argmin(np.where(np.arange(256) <= 0x7E, np.abs(sv - float(t)), np.inf))
+            e_b = np.float32(np.float32(ts.s_enc) / np.float32(sv[scales[i, b]]))
+            y = (blk * e_b).astype(np.float32).astype(np.float64)
+            cc = np.stack([codes[i] & 15, codes[i] >> 4], axis=1).ravel()[b * 16:(b + 1) * 16]
+            got = np.array([oracle.e2m1_value(c) for c in cc])
+            assert np.all(np.abs(np.abs(y) - np.abs(got)) <= np.min(np.abs(np.abs(y)[:, None] - grid[None, :]), axis=1))
+
+
+def test_tensor_scale_edge_cases():
+    z = np.zeros((4, 32), np.uint16)
+    ts = oracle.tensor_scale(z)
+    assert ts.s_enc == 1.0 and ts.s_dec == 1.0
+    c, s = oracle.quantize(z, ts)
+    assert not c.any() and not s.any()
+    one = wl.to_bf16_bits(np.full((1, 16), 6.0))
+    ts = oracle.tensor_scale(one)
+    assert ts.s_enc == 448.0 and ts.shift_e == 4
+
+
+# ------------------------------------------------------------------------------ RAC
+def test_scores_rank_like_l2_norm():
+    """Eq. (23): the integer score ranks channels as the L2 norm of the residual does."""
+    for seed in range(3):
+        x = _rand_x(96, 256, 10 + seed, outliers=5)
+        ts = oracle.tensor_scale(x)
+        s = oracle.scores(x, ts)
+        r = oracle.residual(x, ts).astype(np.float64)
+        l2sq = (r * r).sum(axis=0)
+        eps = 96 * float(ts.amax) ** 2 * 2.0 ** -40
+        exact = l2sq * 2.0 ** (44 - 2 * ts.shift_e)
+        assert np.all(np.abs(s.astype(np.float64) - exact) <= 96 + 1e-6 * exact)
+        o_int = np.lexsort((np.arange(256), -s.astype(np.float64)))
+        for a, b in zip(o_int[:-1], o_int[1:]):
+            assert l2sq[a] >= l2sq[b] - eps
+
+
+def test_residual_definition_sign():
+    x = _rand_x(8, 64, 20)
+    ts = oracle.tensor_scale(x)
+    r = oracle.residual(x, ts)
+    codes, scales = oracle.quantize(x, ts)
+    dq = oracle.dequantize(codes, scales, ts.s_dec)
+    assert np.array_equal(r, (wl.bf16_bits_to_f32(x) - dq).astype(np.float32))
+
+
+def test_topk_against_brute_force_sort():
+    rng = np.random.default_rng(7)
+    for n, k in [(64, 16), (256, 64), (4096, 64), (300, 300)]:
+        s = rng.integers(0, 50, n).astype(np.uint64) * np.uint64(1 << 40)  # many ties
+        idx = oracle.topk(s, k)
+        order = sorted(range(n), key=lambda j: (-int(s[j]), j))[:k]
+        assert list(idx) == sorted(order)
+
+
+def _reconstruct(x, q: "oracle.RacQuant"):
+    dq = oracle.dequantize(q.codes, q.scales, q.ts.s_dec).astype(np.float64)
+    if q.idx.size:
+        dt = oracle.dequantize(q.tail_codes, q.tail_scales, q.ts.s_dec).astype(np.float64)
+        dq[:, q.idx] += dt
+    return dq
+
+
+def test_rac_reduces_activation_error_eq22_and_monotone_in_k():
+    x = _rand_x(64, 512, 30, outliers=8)
+    xf = wl.bf16_bits_to_f32(x).astype(np.float64)
+    errs = []
+    for k in [0, 16, 64, 256, 512]:
+        q = oracle.rac_quantize(x, k)
+        errs.append(np.linalg.norm(_reconstruct(x, q) - xf))
+        if k:
+            assert q.tail_codes.any()
+            # selected channels are the k largest scores
+            assert set(q.idx) == set(np.lexsort((np.arange(512), -q.scores.astype(np.float64)))[:k])
+    assert errs[1] < errs[0], "Eq. (22): compensation must shrink the activation error"
+    assert all(a > b for a, b in zip(errs[:-1], errs[1:])), errs
+
+
+def test_rac_tail_equals_quantized_residual_on_selected_channels():
+    x = _rand_x(16, 256, 31)
+    q = oracle.rac_quantize(x, 32)
+    r = oracle.residual(x, q.ts)
+    rs = r[:, q.idx]
+    dt = oracle.dequantize(q.tail_codes, q.tail_scales, q.ts.s_dec)
+    # second-pass error never exceeds the residual it compensates (norm over each row)
+    assert np.all(np.linalg.norm(rs - dt, axis=1) <= np.linalg.norm(rs, axis=1) + 1e-12)
+    # odd symmetry: Q(-R) is the sign-flipped Q(R), so adding DQ(Q(R)) is Eq. (21)'s subtraction
+    for i in range(16):
+        c, sb = oracle.quantize_block16(-rs[i, :16], q.ts.s_enc)
+        c2, sb2 = oracle.quantize_block16(rs[i, :16], q.ts.s_enc)
+        assert sb == sb2 and np.array_equal(c, c2 ^ 8)
+
+
+def test_k_equal_K_selects_every_channel():
+    x = _rand_x(8, 64, 32)
+    q = oracle.rac_quantize(x, 64)
+    assert list(q.idx) == list(range(64))
+
+
+def test_weight_tail_requantizes_dequantized_weights():
+    w = wl.weights((32, 128), 0.02, 33)
+    wts = oracle.tensor_scale(w)
+    wc, ws = oracle.quantize(w, wts)
+    idx = np.arange(0, 128, 4, dtype=np.int32)[:32]
+    tc, tsc = oracle.weight_tail(wc, ws, wts, idx)
+    wdq = oracle.dequantize(wc, ws, wts.s_dec)[:, idx]
+    tdq = oracle.dequantize(tc, tsc, wts.s_dec)
+    assert np.max(np.abs(tdq - wdq)) <= np.max(np.abs(wdq)) / 4  # within half a grid step of 6 -> 4
+    # selecting a whole original block that keeps its amax reproduces it exactly
+    idx2 = np.arange(16, 48, dtype=np.int32)
+    tc2, tsc2 = oracle.weight_tail(wc, ws, wts, idx2)
+    assert np.array_equal(oracle.dequantize(tc2, tsc2, wts.s_dec), oracle.dequantize(wc, ws, wts.s_dec)[:, 16:48])
+
+
+# ------------------------------------------------------------------------------ GEMM
+def test_gemm_exact_form_matches_fp64_and_torch():
+    x = _rand_x(24, 160, 40)
+    w = wl.weights((40, 160), 0.02, 41)
+    tx, tw = oracle.tensor_scale(x), oracle.tensor_scale(w)
+    ac, as_ = oracle.quantize(x, tx)
+    bc, bs = oracle.quantize(w, tw)
+    y = oracle.gemm(ac, as_, bc, bs, tx.s_dec, tw.s_dec)
+    mi, ni = np.meshgrid(np.arange(24), np.arange(40), indexing="ij")
+    y64 = oracle.gemm_pairs_fp64(ac, as_, bc, bs, tx.s_dec, tw.s_dec, mi.ravel(), ni.ravel()).reshape(24, 40)
+    assert np.allclose(y, y64, rtol=1e-12, atol=1e-300)
+    a = torch.from_numpy(oracle.dequantize(ac, as_, tx.s_dec))
+    b = torch.from_numpy(oracle.dequantize(bc, bs, tw.s_dec))
+    yt = (a @ b.T).numpy().astype(np.float64)
+    assert np.allclose(y, yt, rtol=1e-4, atol=1e-5 * np.abs(y).max())
+
+
+def test_gemm_tiny_brute_force():
+    """M = 2, N = 3, K = 32: every term written out from the decoded codes and scales."""
+    x = _rand_x(2, 32, 42, outliers=1)
+    w = wl.weights((3, 32), 0.02, 43)
+    tx, tw = oracle.tensor_scale(x), oracle.tensor_scale(w)
+    ac, as_ = oracle.quantize(x, tx)
+    bc, bs = oracle.quantize(w, tw)
+    y = oracle.gemm(ac, as_, bc, bs, tx.s_dec, tw.s_dec)
+    from fractions import Fraction as F
+    for m in range(2):
+        for n in range(3):
+            tot = F(0)
+            for c in range(32):
+                ca = (ac[m, c // 2] >> (4 * (c % 2))) & 15
+                cb = (bc[n, c // 2] >> (4 * (c % 2))) & 15
+                tot += (F(oracle.e2m1_value(ca)) * F(oracle.e4m3_value(as_[m, c // 16]))
+                        * F(oracle.e2m1_value(cb)) * F(oracle.e4m3_value(bs[n, c // 16])))
+            ref = float(tot * F(float(tx.s_dec)) * F(float(tw.s_dec)))
+            assert y[m, n] == pytest.approx(ref, rel=1e-15, abs=1e-300)
+
+
+def test_gemm_transposed_operands_differ():
+    """A plain check that the oracle does not silently symmetrise the operands."""
+    x = _rand_x(16, 64, 44)
+    tx = oracle.tensor_scale(x)
+    ac, as_ = oracle.quantize(x, tx)
+    y = oracle.gemm(ac, as_, ac[:8], as_[:8], tx.s_dec, tx.s_dec)
+    assert y.shape == (16, 8)
+    assert np.allclose(y[:8, :8], y[:8, :8].T)   # X X^T is symmetric...
+    assert not np.allclose(y[8:, :], 0)
+
+
+# ------------------------------------------------------------------------------ MoE plumbing
+def test_dispatch_is_stable_counting_sort():
+    ids, _ = wl.routing_zipf(257, 16, 4, 1.1, 9)
+    grp_off, row_src = oracle.moe_dispatch(ids, 16)
+    flat = ids.ravel()
+    order = np.argsort(flat, kind="stable")
+    assert np.array_equal(row_src, order.astype(np.int32))
+    assert np.array_equal(grp_off, np.concatenate([[0], np.cumsum(np.bincount(flat, minlength=16))]))
+
+
+def test_swiglu_and_combine_against_torch():
+    g = np.linspace(-8, 8, 101)
+    u = np.linspace(2, -3, 101)
+    ref = (torch.nn.functional.silu(torch.from_numpy(g)) * torch.from_numpy(u)).numpy()
+    assert np.allclose(oracle.swiglu(g, u), ref, rtol=1e-14, atol=1e-300)
+    rng = np.random.default_rng(3)
+    y = wl.to_bf16_bits(rng.standard_normal((40, 24)))
+    pos = rng.permutation(40).astype(np.int64)
+    out = oracle.moe_combine(y, pos, 4)
+    yt = torch.from_numpy(wl.bf16_bits_to_f32(y))[torch.from_numpy(pos)].view(10, 4, 24)
+    acc = yt[:, 0].clone()
+    for s in range(1, 4):
+        acc = acc + yt[:, s]
+    ref = acc.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(out, ref)
