@@ -25,9 +25,12 @@
  *   R5 Block scale: sb = e4m3(fl(fl(amax_b / 6) * S_enc)); element code
  *      q = e2m1(fl(x * fl(S_enc / sb))); sb == 0 gives code 0 (0x8 for a negative sign bit).
  *   R6 Dequantization: fl(V[q] * fl(sb * S_dec)).
- *   R7 Residual r = fl(x - DQ(Q(x))) (= -dX_q of Eq. (20)); channel score is the exact integer
- *      sum over rows of trunc(r^2 * 2^(44 - 2E)), E = ilogb(amax) + 2, which ranks channels as
- *      the L2 norm of Eq. (23) does except between scores closer than M * amax^2 * 2^-40.
+ *   R7 Residual r = fl(x - DQ(Q(x))) (= -dX_q of Eq. (20)).  The channel score of Eq. (23) is
+ *      the exact integer sum over rows of q^2 with q = rint(|r| * 2^(20 - E)) (nearest integer,
+ *      ties to even), E = ilogb(amax) + 2.  Since |r| < 2^(E-1), q < 2^19 and the uint64 sum is
+ *      exact and independent of summation order for up to 2^19 rows.  It ranks channels as the
+ *      L2 norm does except between channels whose sums of r^2 differ by less than about
+ *      M * amax^2 * 2^-17.
  *   R8 Top-k of Eq. (24) with an absolute channel count k; ties broken to the lower channel
  *      index; the selected indices are emitted in ascending order.
  *   R9 Second pass: the residual on the selected channels, gathered in ascending index order,
@@ -272,9 +275,8 @@ void oracle_scores(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
     for (int64_t i = 0; i < rows; ++i) {
         oracle_residual(x + i * ldx, 1, cols, ldx, ts, r, cols);
         for (int64_t j = 0; j < cols; ++j) {
-            double sq = (double)r[j] * (double)r[j];
-            double scaled = ldexp(sq, 44 - 2 * ts->shift_e);
-            scores[j] += (uint64_t)trunc(scaled);
+            double q = rint(ldexp(fabs((double)r[j]), 20 - ts->shift_e));
+            scores[j] += (uint64_t)q * (uint64_t)q;
         }
     }
     free(r);

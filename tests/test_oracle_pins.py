@@ -215,9 +215,12 @@ def test_scores_rank_like_l2_norm():
         s = oracle.scores(x, ts)
         r = oracle.residual(x, ts).astype(np.float64)
         l2sq = (r * r).sum(axis=0)
-        eps = 96 * float(ts.amax) ** 2 * 2.0 ** -40
-        exact = l2sq * 2.0 ** (44 - 2 * ts.shift_e)
-        assert np.all(np.abs(s.astype(np.float64) - exact) <= 96 + 1e-6 * exact)
+        # |q - |r| 2^(20-E)| <= 1/2 per element bounds the gap to the scaled L2 norm
+        scale = 2.0 ** (20 - ts.shift_e)
+        exact = l2sq * scale * scale
+        bound = (np.abs(r).sum(axis=0) * scale + 0.25 * 96)
+        assert np.all(np.abs(s.astype(np.float64) - exact) <= bound + 1e-9 * exact)
+        eps = 2 * bound.max() / scale ** 2
         o_int = np.lexsort((np.arange(256), -s.astype(np.float64)))
         for a, b in zip(o_int[:-1], o_int[1:]):
             assert l2sq[a] >= l2sq[b] - eps
