@@ -1,0 +1,451 @@
+#!/usr/bin/env python
+"""Benchmark of the rollout-side NVFP4 W4A4 + RAC hot path on GB300.
+
+One step = one forward pass of the routed SwiGLU MoE expert layer with W4A4 + RAC in both
+expert GEMMs (dispatch, activation quantization + channel selection + residual tail, gather,
+gate/up grouped GEMM with SwiGLU, per-expert quantization + selection of h, down grouped GEMM
+with routing weights, combine) over one synthetic batch: T = 16384 tokens, hidden 2048,
+128 experts, top-8 with Zipf(1.1)-skewed routing, intermediate 768, k = 32 per GEMM.
+
+The JSON line reports whole-job tokens/s (inputs resident in HBM, device-timed), an end-to-end
+figure through the same public API with host buffers, the roofline of the dominant kernel
+(the gate/up grouped GEMM), the activation quantizer + RAC bandwidth on the 8192 x 4096
+activation workload, and the CPU oracle timed on a bounded sample on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+L2_FLUSH_BYTES = 512 << 20           # > 2x the 129 MB L2
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense ratio (NVFP4 / BF16) on GB300
+METRIC = "W4A4+RAC grouped-GEMM TFLOPS & tokens/s; act-quant+RAC HBM GB/s (1×GB300)"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling (every 200 ms) over the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- our arm
+class LaunchCounter:
+    """Kernels each C-ABI call launches (counted by the binding calls below)."""
+    PER_CALL = {"moe_dispatch": 4, "nvfp4_quantize": 2, "rac_select_quantize": 2, "nvfp4_gather_rows": 1,
+                "rac_weight_tail": 1, "w4a4_rac_grouped_gemm": 1, "moe_combine": 1}
+
+
+def _bf16(t_bits, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(t_bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    from nvfp4_w4a4_quantized_quantize_gb300 import _lib as L
+    from nvfp4_w4a4_quantized_quantize_gb300 import workloads as wl
+    from nvfp4_w4a4_quantized_quantize_gb300.layers import MoERacLayer
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    cfg = wl.CFG_MOE_PREFILL
+    # every rank processes its own independent batch (weak scaling, no data-path collective)
+    cfg_r = wl.MoELayer(cfg.name, cfg.T, cfg.H, cfg.E, cfg.topk, cfg.I, cfg.k, cfg.seed + 1000 * rank,
+                        cfg.routing, cfg.zipf_s, cfg.n_outliers, cfg.outlier_gain, cfg.w_std)
+    x_bits, ids, tw, _ = cfg_r.make_tokens()
+    w13_bits, w2_bits = wl.MoELayer(**{**cfg.__dict__}).make_weights()
+    E, H, I, T, topk, k = cfg.E, cfg.H, cfg.I, cfg.T, cfg.topk, cfg.k
+    w13 = _bf16(w13_bits.reshape(E * 2 * I, H), dev).view(E, 2 * I, H)
+    w2 = _bf16(w2_bits.reshape(E * H, I), dev).view(E, H, I)
+    layer = MoERacLayer(w13, w2, k, topk, T)
+    del w13, w2
+    x = _bf16(x_bits, dev)
+    ids_d = torch.from_numpy(ids).to(dev)
+    tw_d = torch.from_numpy(tw).to(dev)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    probes = {}
+
+    def step(events=None):
+        layer.forward(x, ids_d, tw_d, out, events=events)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st, where = L.device_status()
+    if st != 0:
+        raise RuntimeError(f"device wait ran out ({where}) during warm-up")
+
+    # ---- device-timed steps (inputs resident), L2 flushed before every step (untimed)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_lists = [dict() for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step(ev_lists[i])
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    barrier(world)
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = max_over_ranks(sum(step_ms), world)
+    ms_per_step = total_ms / args.steps
+    launches_per_step = layer.kernel_launches_per_step()
+
+    # per-kernel durations of the two grouped GEMMs inside the timed steps
+    def avg(name):
+        v = [ev[name][0].elapsed_time(ev[name][1]) for ev in ev_lists if name in ev]
+        return sum(v) / len(v) if v else None
+
+    t_gu, t_dn = avg("gemm_gate_up"), avg("gemm_down")
+    t_q1 = avg("quant_rac_tokens")
+    rows_total = T * topk
+    flop_gu = 2.0 * rows_total * (2 * I) * (H + k)
+    flop_dn = 2.0 * rows_total * H * (I + k)
+    peaks, src = _peaks()
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    ach_gu = flop_gu / (t_gu * 1e-3) / 1e12
+    tokens_per_s = T * world / (ms_per_step * 1e-3)
+
+    # ---- end-to-end through the same API with host buffers (H2D inputs, D2H output each step)
+    x_h = torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).view(torch.bfloat16).pin_memory()
+    ids_h = torch.from_numpy(ids).pin_memory()
+    tw_h = torch.from_numpy(tw).pin_memory()
+    out_h = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    h2d = x_h.numel() * 2 + ids_h.numel() * 4 + tw_h.numel() * 4
+    d2h = out_h.numel() * 2
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        x.copy_(x_h, non_blocking=True)
+        ids_d.copy_(ids_h, non_blocking=True)
+        tw_d.copy_(tw_h, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        e.record(stream)
+        e.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(s.elapsed_time(e))
+    e2e_tot = max_over_ranks(sum(e2e_ms), world)
+    e2e_tps = T * world / (e2e_tot / len(e2e_ms) * 1e-3)
+    st, where = L.device_status()
+    if st != 0:
+        raise RuntimeError(f"device wait ran out ({where}) in the timed region")
+
+    # ---- activation quantizer + RAC on the 8192 x 4096 Student-t workload (HBM-bound)
+    act = act_quant_bench(args, L, wl, dev, flush, peaks) if rank == 0 else None
+
+    result = {
+        "metric": METRIC,
+        "value": round(tokens_per_s, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "nvfp4(e2m1+ue4m3) x nvfp4 -> fp32 acc, bf16 io",
+        "data": "synthetic (seeded; MoE routing Zipf(1.1), 1% outlier channels x20, N(0,0.02) weights)",
+        "config": {"workload": cfg.name, "tokens": T, "hidden": H, "experts": E, "topk": topk,
+                   "intermediate": I, "rac_k": k, "parallelism": f"dp{world} (independent batches)",
+                   "l2": "flushed (512 MiB write) before every timed step"},
+        "gemm_tflops": round((flop_gu + flop_dn) / (ms_per_step * 1e-3) / 1e12, 2),
+        "kernel_ms": {"gemm_gate_up": t_gu, "gemm_down": t_dn, "quant_rac_tokens": t_q1},
+        "roofline": {"kernel": "gemm_kernel (gate/up, SwiGLU epilogue)", "bound": "tensor",
+                     "achieved": round(ach_gu, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(ach_gu / fp4_peak, 4), "traffic": None,
+                     "peak_source": f"{src} bf16 burst {peaks['bf16_tflops']} x nominal NVFP4/BF16 ratio 6"},
+        "e2e": {"value": round(e2e_tps, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+    if act:
+        result["act_quant_rac"] = act
+    return result, (x_bits, ids, tw, w13_bits, w2_bits, cfg)
+
+
+def act_quant_bench(args, L, wl, dev, flush, peaks):
+    import torch
+    cfg = wl.CFG_ACT
+    x_bits, _, _ = cfg.make()
+    M, K, k = cfg.M, cfg.K, cfg.k
+    x = _bf16(x_bits, dev)
+    ld = (K + k) // 2
+    sfc = L.sf_cols(K + k)
+    codes = torch.empty(M, ld, dtype=torch.uint8, device=dev)
+    sf = torch.empty(L.sf_bytes(M, sfc), dtype=torch.uint8, device=dev)
+    ts = torch.empty(1, 4, dtype=torch.float32, device=dev)
+    scores = torch.empty(K, dtype=torch.int64, device=dev)
+    idx = torch.empty(k, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        L.nvfp4_quantize(x, codes, sf, sfc, ts, scores=scores)
+        if ev is not None:
+            ev[1].record(stream)
+        L.rac_select_quantize(x, ts, scores, k, codes, sf, sfc, idx)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    evs = []
+    for _ in range(args.steps):
+        flush.zero_()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        step(ev)
+        evs.append(ev)
+    torch.cuda.synchronize()
+    t_all = sum(e[0].elapsed_time(e[2]) for e in evs) / len(evs)
+    t_q = sum(e[0].elapsed_time(e[1]) for e in evs) / len(evs)
+    t_r = sum(e[1].elapsed_time(e[2]) for e in evs) / len(evs)
+    algo = M * K * (2 + 0.5 + 1 / 16) + M * k * (2 + 0.5 + 1 / 16) + k * 4
+    q_bytes = M * K * (2 + 0.5 + 1 / 16)
+    hbm = peaks["hbm_gbs"]
+    return {"workload": cfg.name, "algorithmic_bytes": int(algo), "ms": round(t_all, 4),
+            "gbs": round(algo / (t_all * 1e-3) / 1e9, 1), "frac_of_measured_hbm": round(algo / (t_all * 1e-3) / 1e9 / hbm, 4),
+            "nvfp4_quantize_ms": round(t_q, 4), "nvfp4_quantize_gbs": round(q_bytes / (t_q * 1e-3) / 1e9, 1),
+            "rac_select_quantize_ms": round(t_r, 4)}
+
+
+# ----------------------------------------------------------------------------- oracle (CPU)
+def oracle_moe_sample(tokens, x_bits, ids, tw, w_q13, w_q2, cfg):
+    """The oracle's MoE layer on a sample of tokens, in the paper's order of steps; weights are
+    already quantized (quantization of the experts' weights happens once, outside the timing)."""
+    import oracle
+    k, I, H, topk = cfg.k, cfg.I, cfg.H, cfg.topk
+    xs = x_bits[tokens]
+    q1 = oracle.rac_quantize(xs, k)
+    a1c = np.concatenate([q1.codes, q1.tail_codes], 1)
+    a1s = np.concatenate([q1.scales, q1.tail_scales], 1)
+    h_rows, h_exp, h_w, h_pos = [], [], [], []
+    for ti in range(len(tokens)):
+        for s in range(topk):
+            e = int(ids[tokens[ti], s])
+            wc, ws, wts = w_q13[e]
+            tc, tsc = oracle.weight_tail(wc, ws, wts, q1.idx)
+            gu = oracle.gemm(a1c[ti:ti + 1], a1s[ti:ti + 1], np.concatenate([wc, tc], 1), np.concatenate([ws, tsc], 1),
+                             q1.ts.s_dec, wts.s_dec)[0]
+            h = oracle.swiglu(gu[:I], gu[I:])
+            h_rows.append(oracle.bf16_round(h.astype(np.float32)))
+            h_exp.append(e)
+            h_w.append(tw[tokens[ti], s])
+            h_pos.append(ti * topk + s)
+    h_rows = np.stack(h_rows)
+    h_exp = np.array(h_exp)
+    y = np.zeros((len(h_rows), H), np.uint16)
+    for e in np.unique(h_exp):
+        sel = np.nonzero(h_exp == e)[0]
+        hq = oracle.rac_quantize(h_rows[sel], k)
+        wc, ws, wts = w_q2[e]
+        tc, tsc = oracle.weight_tail(wc, ws, wts, hq.idx)
+        ye = oracle.gemm(np.concatenate([hq.codes, hq.tail_codes], 1), np.concatenate([hq.scales, hq.tail_scales], 1),
+                         np.concatenate([wc, tc], 1), np.concatenate([ws, tsc], 1), hq.ts.s_dec, wts.s_dec)
+        ye = ye * np.array(h_w)[sel][:, None]
+        y[sel] = oracle.bf16_round(ye.astype(np.float32))
+    pos = np.zeros(len(tokens) * topk, np.int64)
+    pos[np.array(h_pos)] = np.arange(len(h_pos))
+    return oracle.moe_combine(y, pos, topk)
+
+
+def oracle_setup(tokens, ids, w13_bits, w2_bits):
+    import oracle
+    experts = sorted({int(e) for t in tokens for e in ids[t]})
+    w_q13, w_q2 = {}, {}
+    for e in experts:
+        t13 = oracle.tensor_scale(w13_bits[e])
+        c, s = oracle.quantize(w13_bits[e], t13)
+        w_q13[e] = (c, s, t13)
+        t2 = oracle.tensor_scale(w2_bits[e])
+        c, s = oracle.quantize(w2_bits[e], t2)
+        w_q2[e] = (c, s, t2)
+    return w_q13, w_q2
+
+
+def cpu_baseline(inputs, n_tokens=6):
+    x_bits, ids, tw, w13_bits, w2_bits, cfg = inputs
+    tokens = np.arange(n_tokens)
+    w_q13, w_q2 = oracle_setup(tokens, ids, w13_bits, w2_bits)
+    t0 = time.perf_counter()
+    oracle_moe_sample(tokens, x_bits, ids, tw, w_q13, w_q2, cfg)
+    dt = time.perf_counter() - t0
+    return {"value": round(n_tokens / dt, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_tokens} tokens ({n_tokens * cfg.topk} routed rows) of the {cfg.name} batch, "
+                      f"full layer (quantize, select k={cfg.k}, tails, both GEMMs, SwiGLU, combine); "
+                      f"expert weights pre-quantized outside the timing; {dt:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    """The oracle, as it stands, on the host cores: each step one bounded sample of the batch."""
+    from nvfp4_w4a4_quantized_quantize_gb300 import workloads as wl
+    if rank != 0:
+        return None
+    cfg = wl.CFG_MOE_PREFILL
+    x_bits, ids, tw, _ = cfg.make_tokens()
+    w13_bits, w2_bits = cfg.make_weights()
+    per_step = 2
+    tokens = np.arange(per_step)
+    w_q13, w_q2 = oracle_setup(tokens, ids, w13_bits, w2_bits)
+    for _ in range(args.warmup):
+        oracle_moe_sample(tokens, x_bits, ids, tw, w_q13, w_q2, cfg)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_moe_sample(tokens, x_bits, ids, tw, w_q13, w_q2, cfg)
+    dt = time.perf_counter() - t0
+    v = per_step * args.steps / dt
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32 encode / exact int64 GEMM",
+        "data": "synthetic (seeded)",
+        "config": {"workload": cfg.name, "tokens": cfg.T, "hidden": cfg.H, "experts": cfg.E, "topk": cfg.topk,
+                   "intermediate": cfg.I, "rac_k": cfg.k, "parallelism": "1 host core"},
+        "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} tokens ({per_step * cfg.topk} routed rows) of the batch per step"},
+        "e2e": {"value": round(v, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    res, inputs = run_ours(args, world, rank, local)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(inputs)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

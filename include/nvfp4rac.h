@@ -1,0 +1,254 @@
+/*
+ * nvfp4rac.h -- C ABI of the GB300 (sm_103a) library for the rollout-side NVFP4 W4A4 linear
+ * layer with Residual Activation Compensation (RAC).
+ *
+ * The method is that of "QUADS: Stabilizing NVFP4 Reinforcement Learning for MoE via
+ * QUantization-error Alignment across Dual Sides" (arXiv 2607.15810), cited below as QUADS:
+ *   - online activation quantization to NVFP4 (§2.2 "FP4", §3.1 Eq. (9));
+ *   - residual R = X - DQ(Q(X)), channel score and top-k selection, second-pass quantization
+ *     of the residual on the selected channels (§3.3 Eq. (20)-(24));
+ *   - the native block-scaled W4A4 GEMM that carries the correction as extra K-columns
+ *     (§3.3 "Targeted residual compensation"), grouped over routed MoE experts;
+ *   - the trainer-side weight QDQ whose codes and scales equal the rollout quantizer's
+ *     (§3.2 Eq. (12), (15)-(16)).
+ *
+ * Conventions shared by every call
+ *   Memory     All pointers are caller-owned DEVICE memory unless a parameter says otherwise.
+ *              The library never allocates device memory and keeps no pointer after a call.
+ *   Streams    Every call is asynchronous on the given cudaStream_t (passed as void*; NULL is
+ *              the legacy default stream).  Scalars stay on the device.
+ *   Errors     Every call returns an nvq_status.  Argument and shape checks run on the host
+ *              before anything is launched; on failure nothing is launched and
+ *              nvq_last_error() (thread-local) describes the problem.  Device-side waits are
+ *              bounded: a wait that runs out records NVQ_ERR_TIMEOUT in a device status word
+ *              that nvq_device_status() reads (the kernel then returns without hanging).
+ *   Inputs     bf16 inputs must be finite; non-finite inputs give unspecified codes.
+ *
+ * Data formats
+ *   Codes      NVFP4 (E2M1) codes, two per byte, element 2i in the LOW nibble; row-major with a
+ *              leading dimension in bytes (multiple of 16).  Code = sign<<3 | magnitude index
+ *              into {0, 0.5, 1, 1.5, 2, 3, 4, 6}; a negative value that rounds to 0 keeps its
+ *              sign (0x8).
+ *   Scales     One UE4M3 byte per 16 consecutive elements of a row, stored in the MMA-ready
+ *              blocked layout: with sf_cols scale columns (a multiple of 4) and rows padded
+ *              to a multiple of 128, the byte of (row r, scale column c) is at
+ *                ((r / 128) * (sf_cols / 4) + c / 4) * 512 + (r % 32) * 16 + ((r / 32) % 4) * 4 + c % 4
+ *              (nvq_sf_offset).  A buffer for R rows holds nvq_sf_bytes(R, sf_cols) bytes.
+ *   RAC tail   The k compensation columns of an operand live in columns [K, K + k) of the same
+ *              code and scale buffers, so a GEMM sees K_tot = K + k columns.  Scale columns from
+ *              (K + k) / 16 up to sf_cols are written as zero by rac_select_quantize (and by
+ *              nvfp4_quantize when k is 0), so sf_cols = nvq_sf_cols(K + k).
+ *   Tensor scale  nvq_tensor_scale per tensor (or per row group): amax, S_enc = 2688 / amax,
+ *              S_dec = 1 / S_enc (both fp32; amax 0 gives 1 and 1) and the score exponent
+ *              E = ilogb(amax) + 2.
+ *   Row groups Grouped calls take grp_off (int64 [G + 1]) and grp_rows (int64 [G]) in device
+ *              memory: group g owns rows [grp_off[g], grp_off[g] + grp_rows[g]) and
+ *              grp_rows[g] <= grp_off[g + 1] - grp_off[g].  grp_rows NULL means
+ *              grp_rows[g] = grp_off[g + 1] - grp_off[g].  grp_off NULL with G > 1 means
+ *              G equal groups of rows / G rows; G = 1 with grp_off NULL is one dense tensor.
+ *              For the GEMM every grp_off[g] must be a multiple of 128 (moe_dispatch writes
+ *              such offsets).
+ */
+#ifndef NVFP4RAC_H
+#define NVFP4RAC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nvq_status {
+    NVQ_OK = 0,
+    NVQ_ERR_ARG = 1,     /* null pointer or invalid enumerator */
+    NVQ_ERR_SHAPE = 2,   /* unsupported or inconsistent sizes */
+    NVQ_ERR_ALIGN = 3,   /* pointer or leading dimension not aligned as required */
+    NVQ_ERR_CUDA = 4,    /* a CUDA runtime or driver call failed */
+    NVQ_ERR_TIMEOUT = 5  /* a bounded device-side wait ran out (reported by nvq_device_status) */
+} nvq_status;
+
+typedef struct nvq_tensor_scale {
+    float amax;      /* max |x| over the tensor or group */
+    float s_enc;     /* fl(2688 / amax), 1 when amax is 0 */
+    float s_dec;     /* fl(1 / s_enc) */
+    int32_t shift_e; /* ilogb(amax) + 2, 0 when amax is 0 */
+} nvq_tensor_scale;
+
+enum nvq_epilogue {
+    NVQ_EPI_STORE = 0,      /* out[r, n] = bf16(alpha_g * acc[r, n]),                 out is [rows][N]   */
+    NVQ_EPI_SWIGLU = 1,     /* out[r, j] = bf16(silu(g) * u), g = alpha*acc[r, j],
+                               u = alpha*acc[r, N/2 + j], silu(g) = g / (1 + exp(-g)), out is [rows][N/2] */
+    NVQ_EPI_ROW_SCALE = 2,  /* out[r, n] = bf16(alpha_g * acc[r, n] * row_w[r]),      out is [rows][N]   */
+    NVQ_EPI_STORE_F32 = 3   /* out[r, n] = fl(alpha_g * acc[r, n]) as fp32,            out is [rows][N]   */
+};
+
+enum nvq_dtype { NVQ_BF16 = 0, NVQ_F32 = 1 };
+
+/* Message describing the last failure on the calling thread ("" after a success). */
+const char* nvq_last_error(void);
+
+/* Reads and clears the device status word of the current device (synchronises the stream).
+ * *status receives NVQ_OK or NVQ_ERR_TIMEOUT; *where an identifier of the wait that ran out. */
+nvq_status nvq_device_status(void* stream, int32_t* status, int32_t* where);
+
+/* Sets the bound of every device-side wait, in GPU clock cycles (default 2^32, about 2 s).
+ * Applies to launches made after the call on the current device. */
+nvq_status nvq_set_wait_limit(uint64_t cycles);
+
+/* Scale-layout helpers (host functions, no device access). */
+int64_t nvq_sf_cols(int64_t ktot);                      /* roundup(ktot / 16, 4) */
+int64_t nvq_sf_bytes(int64_t rows, int64_t sf_cols);    /* roundup(rows, 128) * sf_cols */
+int64_t nvq_sf_offset(int64_t row, int64_t col, int64_t sf_cols);
+
+/*
+ * nvfp4_quantize -- Q_A of QUADS Eq. (9) / Q_W of Eq. (7): NVFP4 quantization of a bf16 matrix
+ * (§2.2 "FP4": E2M1 codes, one E4M3 scale per 16 elements along K, one FP32 tensor scale),
+ * plus the per-channel residual scores of Eq. (23) when scores is not NULL.
+ *
+ *   x         bf16 [rows][ldx], ldx >= K, ldx % 8 == 0, x 16-byte aligned.
+ *   rows, K   1 <= rows <= 2^24 (at most 2^19 rows per group when scores is not NULL),
+ *             16 <= K <= 8192, K % 16 == 0.
+ *   grp_off, grp_rows, groups   row groups (see header); each group gets its own tensor scale
+ *             and its own scores; rows outside every group are not read or written.
+ *   codes     [rows][ld_codes] bytes, columns [0, K) written; ld_codes % 16 == 0, >= K / 2.
+ *   sf        blocked scales with sf_cols columns (sf_cols % 4 == 0, >= K / 16); columns
+ *             [0, K / 16) written; if zero_pad is non-zero, columns [K / 16, sf_cols) are
+ *             zeroed as well (use it when no RAC tail follows).
+ *   tscale    [groups] out.
+ *   scores    NULL, or uint64 [groups][K] out: score_j = sum over the group's rows of
+ *             rint(|r_j| * 2^(20 - E))^2, r = x - DQ(Q(x)) in fp32 (exact, order independent).
+ * Ownership: all buffers caller-owned; nothing retained.  Errors: NVQ_ERR_ARG / SHAPE / ALIGN
+ * before launch, NVQ_ERR_CUDA if a launch fails.
+ */
+nvq_status nvfp4_quantize(const void* x, int64_t rows, int64_t K, int64_t ldx,
+                          const int64_t* grp_off, const int64_t* grp_rows, int32_t groups,
+                          uint8_t* codes, int64_t ld_codes, uint8_t* sf, int64_t sf_cols,
+                          int32_t zero_pad, nvq_tensor_scale* tscale, uint64_t* scores,
+                          void* stream);
+
+/*
+ * rac_select_quantize -- channel selection of QUADS Eq. (24) and the second-pass quantization
+ * of Eq. (21): per group, S = the k channels with the largest score (ties to the lower channel
+ * index), written ascending to idx; then the residual R[:, S] = X[:, S] - DQ(Q(X))[:, S], with
+ * blocks of 16 consecutive selected channels and the group's own S_enc, is quantized into
+ * columns [K, K + k) of codes and scale columns [K / 16, (K + k) / 16) of sf; scale columns
+ * [(K + k) / 16, sf_cols) are zeroed.
+ *
+ *   x, rows, K, ldx, grp_*, groups   as for nvfp4_quantize (the same call's inputs).
+ *   tscale    [groups] from nvfp4_quantize.   scores  uint64 [groups][K] from nvfp4_quantize.
+ *   k         0 <= k <= K, k % 16 == 0, k <= 512.  k = 0 only zeroes the scale padding.
+ *   codes, sf the buffers nvfp4_quantize wrote; ld_codes >= (K + k) / 2; sf_cols >= (K + k) / 16.
+ *   idx       int32 [groups][k] out (may be NULL when k == 0).
+ */
+nvq_status rac_select_quantize(const void* x, int64_t rows, int64_t K, int64_t ldx,
+                               const int64_t* grp_off, const int64_t* grp_rows, int32_t groups,
+                               const nvq_tensor_scale* tscale, const uint64_t* scores, int32_t k,
+                               uint8_t* codes, int64_t ld_codes, uint8_t* sf, int64_t sf_cols,
+                               int32_t* idx, void* stream);
+
+/*
+ * weight_qdq -- the trainer-side QDQ_W of QUADS Eq. (12): for each of G weight tensors
+ * W_g = w[g] ([N][K] bf16, tensor g at w + g * N * ldw elements) the same quantizer as
+ * nvfp4_quantize with one tensor scale per tensor, so that its codes and scales are the
+ * rollout weight codes bit for bit (Eq. (15)-(16)).  Optionally writes W-hat = DQ(Q(W)).
+ *
+ *   codes     [G * N][ld_codes], sf blocked scales of G * N rows with sf_cols columns
+ *             (rows of tensor g start at row g * N; N % 128 == 0).
+ *   tscale    [G] out.
+ *   w_hat     NULL, or [G * N][K] of w_hat_dtype (NVQ_BF16: nearest-even bf16 of the fp32
+ *             dequantized value; NVQ_F32: the fp32 value fl(V * fl(sb * S_dec))).
+ */
+nvq_status weight_qdq(const void* w, int32_t groups, int64_t N, int64_t K, int64_t ldw,
+                      uint8_t* codes, int64_t ld_codes, uint8_t* sf, int64_t sf_cols,
+                      nvq_tensor_scale* tscale, void* w_hat, int32_t w_hat_dtype, void* stream);
+
+/*
+ * w4a4_rac_grouped_gemm -- the native block-scaled W4A4 GEMM of QUADS §3.3 with the RAC
+ * correction as K-columns [K, K + k), over row groups (routed MoE experts) that each have
+ * their own weight matrix:  Y_g = alpha_g * [A_g | R_g] [W_g | W'_g]^T,
+ * alpha_g = S_dec(A_g) * S_dec(W_g), FP32 accumulation on tcgen05 tensor cores.
+ *
+ * When idx is not NULL the call first builds each group's weight tail W'_g into columns
+ * [K, K + k) of b_codes / b_sf (as rac_weight_tail does); with idx NULL and k > 0 the tail
+ * columns are used as they are (built earlier by rac_weight_tail).
+ *
+ *   groups, grp_off, grp_rows   A row groups (grp_off[g] % 128 == 0); groups = 1 with
+ *             grp_off NULL is a dense GEMM over all `rows`.
+ *   rows      number of rows of A and out (buffer extent); rows <= 2^24.
+ *   a_codes, lda, a_sf, a_sf_cols    A = quantized activations + RAC tail (nvfp4_quantize +
+ *             rac_select_quantize).  a_tscale  [groups] if a_scale_per_group else [1].
+ *   b_codes, ldb, b_sf, b_sf_cols    W_g = rows [g * N, (g + 1) * N) (weight_qdq output);
+ *             tail columns rewritten by this call.  b_tscale  [groups].
+ *   N, K, k   N % 256 == 0 (NVQ_EPI_SWIGLU: N / 2 % 128 == 0); K % 64 == 0; k as above.
+ *   idx       NULL, or int32 [groups][k] if idx_per_group else [k] (rac_select_quantize output).
+ *   epilogue  enum nvq_epilogue.   row_w  fp32 [rows] for NVQ_EPI_ROW_SCALE, else NULL.
+ *   out, ldo  bf16 (fp32 for NVQ_EPI_STORE_F32) [rows][ldo], ldo in elements, ldo % 8 == 0;
+ *             rows outside every group are not written.
+ */
+nvq_status w4a4_rac_grouped_gemm(int32_t groups, const int64_t* grp_off, const int64_t* grp_rows,
+                                 int64_t rows, const uint8_t* a_codes, int64_t lda,
+                                 const uint8_t* a_sf, int64_t a_sf_cols,
+                                 const nvq_tensor_scale* a_tscale, int32_t a_scale_per_group,
+                                 uint8_t* b_codes, int64_t ldb, uint8_t* b_sf, int64_t b_sf_cols,
+                                 const nvq_tensor_scale* b_tscale, int64_t N, int64_t K, int32_t k,
+                                 const int32_t* idx, int32_t idx_per_group, int32_t epilogue,
+                                 const float* row_w, void* out, int64_t ldo, void* stream);
+
+/*
+ * rac_weight_tail -- the weight columns that multiply the RAC correction (QUADS §3.3, Eq. (21):
+ * the correction term is a product with the same layer's weights on the selected channels).
+ * Reading of the paper: W'_g = Q(DQ(W_g)[:, S_g]), i.e. the dequantized stored NVFP4 weights on
+ * the selected channels, gathered in ascending channel order and re-quantized (blocks of 16
+ * gathered channels) with the weight tensor's own S_enc, written into columns [K, K + k) of
+ * b_codes and scale columns [K / 16, (K + k) / 16) of b_sf; scale columns beyond are zeroed.
+ *   b_codes, ldb, b_sf, b_sf_cols, b_tscale   weight_qdq output for groups x N rows.
+ *   idx       int32 [groups][k] if idx_per_group else [k].  1 <= k <= min(K, 512), k % 16 == 0.
+ */
+nvq_status rac_weight_tail(int32_t groups, int64_t N, int64_t K, int32_t k, const int32_t* idx,
+                           int32_t idx_per_group, uint8_t* b_codes, int64_t ldb, uint8_t* b_sf,
+                           int64_t b_sf_cols, const nvq_tensor_scale* b_tscale, void* stream);
+
+/*
+ * moe_dispatch -- routing plumbing of the MoE expert layer (not described by the paper):
+ * a stable counting sort of the tokens * topk (token, slot) pairs by expert.
+ *
+ *   topk_ids  int32 [tokens][topk] expert ids in [0, groups).   topk_w  fp32 [tokens][topk] or NULL.
+ *   grp_off   int64 [groups + 1] out: group g starts at row grp_off[g] (multiple of 128);
+ *             grp_rows int64 [groups] out: number of routed rows of group g.
+ *   row_src   int32 [capacity] out: routed row -> token * topk + slot (-1 on padding rows);
+ *             inside a group rows are in ascending (token, slot) order.
+ *   row_of    int64 [tokens * topk] out: routed row of each (token, slot).
+ *   row_w     fp32 [capacity] out (NULL allowed): topk_w of the routed row, 0 on padding.
+ *   capacity  >= moe_capacity(tokens, topk, groups).
+ *   workspace device bytes >= moe_dispatch_workspace_size(tokens, topk, groups).
+ */
+int64_t moe_capacity(int64_t tokens, int32_t topk, int32_t groups);
+size_t moe_dispatch_workspace_size(int64_t tokens, int32_t topk, int32_t groups);
+nvq_status moe_dispatch(const int32_t* topk_ids, const float* topk_w, int64_t tokens, int32_t topk,
+                        int32_t groups, int64_t* grp_off, int64_t* grp_rows, int32_t* row_src,
+                        int64_t* row_of, float* row_w, int64_t capacity, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/*
+ * nvfp4_gather_rows -- copies quantized rows (codes and blocked scales of K_tot columns) into
+ * the routed layout: out row r = source row row_src[r] / topk, padding rows (row_src < 0) get
+ * zero codes and zero scales.  out_sf uses the same sf_cols as sf.
+ */
+nvq_status nvfp4_gather_rows(const uint8_t* codes, int64_t ld_codes, const uint8_t* sf,
+                             int64_t sf_cols, int64_t src_rows, const int32_t* row_src,
+                             int32_t topk, int64_t capacity, int64_t ktot, uint8_t* out_codes,
+                             int64_t ld_out, uint8_t* out_sf, void* stream);
+
+/*
+ * moe_combine -- out[t, :] = bf16( sum over slots s = 0..topk-1, in slot order, in fp32, of
+ * y[row_of[t * topk + s], :] ).  y bf16 [capacity][ldy]; out bf16 [tokens][ldo].
+ */
+nvq_status moe_combine(const void* y, int64_t ldy, const int64_t* row_of, int64_t tokens,
+                       int32_t topk, int64_t hidden, void* out, int64_t ldo, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4RAC_H */

@@ -1,0 +1,280 @@
+// moe.cu -- routing plumbing around the grouped W4A4 GEMM of the MoE expert layer.
+//
+// The paper runs its RAC linear layers inside the experts of an MoE model (QUADS §3.3, the
+// "W13" activation site; §4.1 MoE 25B-A2.8B) but does not describe dispatch or combine; these
+// are the plain steps of a top-k routed layer:
+//   dispatch   stable counting sort of the (token, slot) pairs by expert; every expert's rows
+//              start on a multiple of 128 so that a 128-row GEMM tile never spans two experts
+//              and the blocked scale layout stays tile-aligned;
+//   gather     copies each routed row's quantized codes and scales from its token row;
+//   combine    sums each token's topk expert outputs in slot order (fp32) and rounds to bf16.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace nvq {
+
+// Pairs are cut into units of 256 consecutive (token, slot) pairs; one warp owns a unit.
+static constexpr int kUnit = 256;
+static constexpr int kWarpsPerCta = 8;
+
+// Per-unit histogram of experts: counts[unit][G].
+__global__ void dispatch_hist_kernel(const int32_t* __restrict__ ids, int64_t n, int G, int32_t* __restrict__ counts)
+{
+    extern __shared__ int32_t hist[];  // [kWarpsPerCta][G]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int32_t* h = hist + warp * G;
+    for (int e = lane; e < G; e += 32) h[e] = 0;
+    __syncwarp();
+    const int64_t unit = (int64_t)blockIdx.x * kWarpsPerCta + warp;
+    const int64_t p0 = unit * kUnit;
+    if (p0 >= n) return;
+    const int64_t p1 = min(p0 + kUnit, n);
+    for (int64_t p = p0 + lane; p < p1; p += 32) atomicAdd(&h[ids[p]], 1);
+    __syncwarp();
+    for (int e = lane; e < G; e += 32) counts[unit * G + e] = h[e];
+}
+
+// CTA per expert: exclusive scan of its count over units; grp_rows[e] = total.
+__global__ void __launch_bounds__(1024) dispatch_scan_kernel(int32_t* __restrict__ counts, int units, int G,
+                                                             int64_t* __restrict__ grp_rows)
+{
+    __shared__ int warp_sums[32];
+    const int e = blockIdx.x;
+    const int per = (units + blockDim.x - 1) / blockDim.x;
+    const int u0 = threadIdx.x * per, u1 = min(units, u0 + per);
+    int local = 0;
+    for (int u = u0; u < u1; ++u) local += counts[(int64_t)u * G + e];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int s = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        warp_sums[lane] = s;
+    }
+    __syncthreads();
+    int run = (warp ? warp_sums[warp - 1] : 0) + x - local;
+    for (int u = u0; u < u1; ++u) {
+        int v = counts[(int64_t)u * G + e];
+        counts[(int64_t)u * G + e] = run;
+        run += v;
+    }
+    if (threadIdx.x == blockDim.x - 1) grp_rows[e] = run;
+}
+
+// One CTA: 128-padded group offsets and the padding rows.
+__global__ void dispatch_offsets_kernel(int G, const int64_t* __restrict__ grp_rows, int64_t* __restrict__ grp_off,
+                                        int32_t* __restrict__ row_src, float* __restrict__ row_w, int64_t capacity)
+{
+    __shared__ int64_t off[1025];
+    if (threadIdx.x == 0) {
+        int64_t s = 0;
+        for (int i = 0; i < G; ++i) {
+            off[i] = s;
+            s += (grp_rows[i] + 127) / 128 * 128;
+        }
+        off[G] = s;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e <= G; e += blockDim.x) grp_off[e] = off[e];
+    for (int e = threadIdx.x; e < G; e += blockDim.x) {
+        const int64_t end = off[e] + grp_rows[e];
+        for (int64_t r = end; r < off[e + 1]; ++r) {
+            row_src[r] = -1;
+            if (row_w) row_w[r] = 0.0f;
+        }
+    }
+    for (int64_t r = off[G] + threadIdx.x; r < capacity; r += blockDim.x) {
+        row_src[r] = -1;
+        if (row_w) row_w[r] = 0.0f;
+    }
+}
+
+// Warp per unit keeps the (token, slot) order inside every expert.
+__global__ void dispatch_scatter_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w, int64_t n, int G,
+                                        const int32_t* __restrict__ counts, const int64_t* __restrict__ grp_off,
+                                        int32_t* __restrict__ row_src, int64_t* __restrict__ row_of,
+                                        float* __restrict__ row_w)
+{
+    extern __shared__ int64_t base_all[];  // [kWarpsPerCta][G]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int64_t* base = base_all + warp * G;
+    const int64_t unit = (int64_t)blockIdx.x * kWarpsPerCta + warp;
+    const int64_t p0 = unit * kUnit;
+    if (p0 >= n) return;
+    for (int e = lane; e < G; e += 32) base[e] = grp_off[e] + counts[unit * G + e];
+    __syncwarp();
+    const int64_t p1 = min(p0 + kUnit, n);
+    for (int64_t pb = p0; pb < p1; pb += 32) {
+        const int64_t p = pb + lane;
+        const bool valid = p < p1;
+        const unsigned act = __ballot_sync(0xffffffffu, valid);
+        int e = 0, rank = 0;
+        unsigned peers = 0;
+        int64_t pos = 0;
+        if (valid) {
+            e = ids[p];
+            peers = __match_any_sync(act, e);
+            rank = __popc(peers & ((1u << lane) - 1u));
+            pos = base[e] + rank;
+            row_src[pos] = (int32_t)p;
+            row_of[p] = pos;
+            if (row_w) row_w[pos] = w ? w[p] : 1.0f;
+        }
+        __syncwarp();
+        if (valid && rank == 0) base[e] += __popc(peers);
+        __syncwarp();
+    }
+}
+
+// Warp per routed row: codes as 16-byte vectors, scales as the 4-byte words of the blocked layout.
+__global__ void gather_rows_kernel(const uint8_t* __restrict__ codes, int64_t ld_codes, const uint8_t* __restrict__ sf,
+                                   int64_t sf_cols, const int32_t* __restrict__ row_src, int topk, int64_t capacity,
+                                   int64_t ktot, uint8_t* __restrict__ out_codes, int64_t ld_out, uint8_t* __restrict__ out_sf)
+{
+    const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= capacity) return;
+    const int32_t s = row_src[r];
+    const int64_t src = s >= 0 ? s / topk : -1;
+    const int64_t nvec = ktot / 32;  // 16-byte vectors of codes
+    uint4* dst = reinterpret_cast<uint4*>(out_codes + r * ld_out);
+    if (src >= 0) {
+        const uint4* srcp = reinterpret_cast<const uint4*>(codes + src * ld_codes);
+        for (int64_t v = lane; v < nvec; v += 32) dst[v] = __ldg(srcp + v);
+        if (lane == 0 && (ktot % 32) != 0) {
+            const uint2* s2 = reinterpret_cast<const uint2*>(codes + src * ld_codes) + nvec * 2;
+            reinterpret_cast<uint2*>(out_codes + r * ld_out)[nvec * 2] = *s2;
+        }
+    } else {
+        for (int64_t v = lane; v < nvec; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+        if (lane == 0 && (ktot % 32) != 0) reinterpret_cast<uint2*>(out_codes + r * ld_out)[nvec * 2] = make_uint2(0, 0);
+    }
+    for (int64_t c4 = lane; c4 < sf_cols / 4; c4 += 32) {
+        uint32_t v = 0;
+        if (src >= 0) v = *reinterpret_cast<const uint32_t*>(sf + sf_offset(src, c4 * 4, sf_cols));
+        *reinterpret_cast<uint32_t*>(out_sf + sf_offset(r, c4 * 4, sf_cols)) = v;
+    }
+}
+
+// CTA per token; each thread sums 8 columns over the slots in slot order.
+__global__ void combine_kernel(const __nv_bfloat16* __restrict__ y, int64_t ldy, const int64_t* __restrict__ row_of,
+                               int topk, int64_t hidden, __nv_bfloat16* __restrict__ out, int64_t ldo)
+{
+    const int64_t t = blockIdx.x;
+    for (int64_t c = (int64_t)threadIdx.x * 8; c < hidden; c += (int64_t)blockDim.x * 8) {
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (int s = 0; s < topk; ++s) {
+            const int64_t r = row_of[t * topk + s];
+            uint4 w = __ldg(reinterpret_cast<const uint4*>(y + r * ldy + c));
+            acc[0] = __fadd_rn(acc[0], bf16lo(w.x)); acc[1] = __fadd_rn(acc[1], bf16hi(w.x));
+            acc[2] = __fadd_rn(acc[2], bf16lo(w.y)); acc[3] = __fadd_rn(acc[3], bf16hi(w.y));
+            acc[4] = __fadd_rn(acc[4], bf16lo(w.z)); acc[5] = __fadd_rn(acc[5], bf16hi(w.z));
+            acc[6] = __fadd_rn(acc[6], bf16lo(w.w)); acc[7] = __fadd_rn(acc[7], bf16hi(w.w));
+        }
+        uint32_t pk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+            pk[i] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(out + t * ldo + c) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+}
+
+}  // namespace nvq
+
+using namespace nvq;
+
+extern "C" int64_t moe_capacity(int64_t tokens, int32_t topk, int32_t groups)
+{
+    return (tokens * topk + 127) / 128 * 128 + (int64_t)groups * 128;
+}
+
+extern "C" size_t moe_dispatch_workspace_size(int64_t tokens, int32_t topk, int32_t groups)
+{
+    const int64_t units = (tokens * topk + kUnit - 1) / kUnit;
+    return (size_t)(units * groups * sizeof(int32_t));
+}
+
+extern "C" nvq_status moe_dispatch(const int32_t* topk_ids, const float* topk_w, int64_t tokens, int32_t topk,
+                                   int32_t groups, int64_t* grp_off, int64_t* grp_rows, int32_t* row_src,
+                                   int64_t* row_of, float* row_w, int64_t capacity, void* workspace,
+                                   size_t workspace_bytes, void* stream)
+{
+    NVQ_CHECK_ARG(topk_ids && grp_off && grp_rows && row_src && row_of && workspace, NVQ_ERR_ARG,
+                  "moe_dispatch: null pointer argument");
+    NVQ_CHECK_ARG(tokens >= 1 && topk >= 1 && topk <= 64 && tokens * topk <= (1ll << 26), NVQ_ERR_SHAPE,
+                  "moe_dispatch: tokens*topk outside [1, 2^26] or topk outside [1, 64]");
+    NVQ_CHECK_ARG(groups >= 1 && groups <= 1024, NVQ_ERR_SHAPE, "moe_dispatch: groups outside [1, 1024]");
+    NVQ_CHECK_ARG(capacity >= moe_capacity(tokens, topk, groups), NVQ_ERR_SHAPE,
+                  "moe_dispatch: capacity %lld < moe_capacity() = %lld", (long long)capacity,
+                  (long long)moe_capacity(tokens, topk, groups));
+    NVQ_CHECK_ARG(workspace_bytes >= moe_dispatch_workspace_size(tokens, topk, groups), NVQ_ERR_SHAPE,
+                  "moe_dispatch: workspace too small");
+    set_error("");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t n = tokens * topk;
+    const int units = (int)((n + kUnit - 1) / kUnit);
+    const int ctas = (units + kWarpsPerCta - 1) / kWarpsPerCta;
+    int32_t* counts = static_cast<int32_t*>(workspace);
+    dispatch_hist_kernel<<<ctas, 32 * kWarpsPerCta, kWarpsPerCta * groups * sizeof(int32_t), st>>>(topk_ids, n, groups, counts);
+    NVQ_LAUNCH_CHECK("dispatch_hist_kernel");
+    dispatch_scan_kernel<<<groups, units >= 1024 ? 1024 : ((units + 31) / 32) * 32, 0, st>>>(counts, units, groups, grp_rows);
+    NVQ_LAUNCH_CHECK("dispatch_scan_kernel");
+    dispatch_offsets_kernel<<<1, 1024, 0, st>>>(groups, grp_rows, grp_off, row_src, row_w, capacity);
+    NVQ_LAUNCH_CHECK("dispatch_offsets_kernel");
+    dispatch_scatter_kernel<<<ctas, 32 * kWarpsPerCta, kWarpsPerCta * groups * sizeof(int64_t), st>>>(
+        topk_ids, topk_w, n, groups, counts, grp_off, row_src, row_of, row_w);
+    NVQ_LAUNCH_CHECK("dispatch_scatter_kernel");
+    return NVQ_OK;
+}
+
+extern "C" nvq_status nvfp4_gather_rows(const uint8_t* codes, int64_t ld_codes, const uint8_t* sf, int64_t sf_cols,
+                                        int64_t src_rows, const int32_t* row_src, int32_t topk, int64_t capacity,
+                                        int64_t ktot, uint8_t* out_codes, int64_t ld_out, uint8_t* out_sf, void* stream)
+{
+    NVQ_CHECK_ARG(codes && sf && row_src && out_codes && out_sf, NVQ_ERR_ARG, "nvfp4_gather_rows: null pointer argument");
+    NVQ_CHECK_ARG(ktot >= 16 && ktot % 16 == 0 && sf_cols >= ktot / 16 && sf_cols % 4 == 0, NVQ_ERR_SHAPE,
+                  "nvfp4_gather_rows: bad ktot / sf_cols");
+    NVQ_CHECK_ARG(capacity >= 1 && capacity % 128 == 0 && src_rows >= 1 && topk >= 1, NVQ_ERR_SHAPE,
+                  "nvfp4_gather_rows: capacity must be a positive multiple of 128");
+    NVQ_CHECK_ARG(ld_codes % 16 == 0 && ld_out % 16 == 0 && ld_codes >= ktot / 2 && ld_out >= ktot / 2 &&
+                      aligned(codes, 16) && aligned(out_codes, 16) && aligned(sf, 4) && aligned(out_sf, 4),
+                  NVQ_ERR_ALIGN, "nvfp4_gather_rows: codes need 16-byte aligned rows");
+    set_error("");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    gather_rows_kernel<<<(unsigned)((capacity + 7) / 8), 256, 0, st>>>(codes, ld_codes, sf, sf_cols, row_src, topk,
+                                                                      capacity, ktot, out_codes, ld_out, out_sf);
+    NVQ_LAUNCH_CHECK("gather_rows_kernel");
+    return NVQ_OK;
+}
+
+extern "C" nvq_status moe_combine(const void* y, int64_t ldy, const int64_t* row_of, int64_t tokens, int32_t topk,
+                                  int64_t hidden, void* out, int64_t ldo, void* stream)
+{
+    NVQ_CHECK_ARG(y && row_of && out, NVQ_ERR_ARG, "moe_combine: null pointer argument");
+    NVQ_CHECK_ARG(tokens >= 1 && tokens <= (1ll << 31) - 1 && topk >= 1 && hidden >= 8 && hidden % 8 == 0, NVQ_ERR_SHAPE,
+                  "moe_combine: hidden must be a positive multiple of 8");
+    NVQ_CHECK_ARG(ldy % 8 == 0 && ldo % 8 == 0 && ldy >= hidden && ldo >= hidden && aligned(y, 16) && aligned(out, 16),
+                  NVQ_ERR_ALIGN, "moe_combine: rows must be 16-byte aligned");
+    set_error("");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    combine_kernel<<<(unsigned)tokens, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(y), ldy, row_of, topk, hidden,
+                                                     static_cast<__nv_bfloat16*>(out), ldo);
+    NVQ_LAUNCH_CHECK("combine_kernel");
+    return NVQ_OK;
+}

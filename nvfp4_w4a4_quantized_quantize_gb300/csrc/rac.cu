@@ -1,0 +1,289 @@
+// rac.cu -- Residual Activation Compensation (QUADS §3.3).
+//
+//   topk_kernel        S = TopK of the channel scores (Eq. (24)), one CTA per group: an
+//                      MSB-first radix select over the uint64 scores in shared memory finds the
+//                      k-th largest score, ties at the threshold go to the lower channel index,
+//                      and a block scan emits the selected channels in ascending order.
+//   act_tail_kernel    second pass of Eq. (21): the residual X - DQ(Q(X)) on the selected
+//                      channels (recomputed from x and the stored block scale, bit-identical to
+//                      the first pass) is quantized, 16 selected channels per block, into the
+//                      tail columns [K, K + k) of the activation operand.
+//   weight_tail_kernel the weight columns that multiply the correction: dequantized stored
+//                      weights on the selected channels, re-quantized with the weight's S_enc,
+//                      into the tail columns of the weight operand.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace nvq {
+
+static constexpr int kTopkThreads = 1024;
+
+// Exclusive scan of one int per thread over the block; returns the block total in *total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int s = (lane < (int)(blockDim.x >> 5)) ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        warp_sums[lane] = s;  // inclusive
+    }
+    __syncthreads();
+    int base = (warp == 0) ? 0 : warp_sums[warp - 1];
+    *total = warp_sums[(blockDim.x >> 5) - 1];
+    __syncthreads();
+    return base + x - v;
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const unsigned long long* __restrict__ scores, int K, int k,
+                                                             int32_t* __restrict__ idx)
+{
+    extern __shared__ unsigned long long s[];  // [K]
+    __shared__ unsigned int hist[256];
+    __shared__ int warp_sums[32];
+    __shared__ unsigned long long s_prefix, s_or;
+    __shared__ int s_remaining, s_digit, s_above;
+    const int g = blockIdx.x;
+    const unsigned long long* src = scores + (int64_t)g * K;
+    int32_t* out = idx + (int64_t)g * k;
+    const int tid = threadIdx.x;
+
+    unsigned long long orv = 0;
+    for (int j = tid; j < K; j += kTopkThreads) {
+        unsigned long long v = src[j];
+        s[j] = v;
+        orv |= v;
+    }
+    if (tid == 0) { s_or = 0; s_prefix = 0; s_remaining = k; }
+    __syncthreads();
+    for (int o = 16; o > 0; o >>= 1) orv |= __shfl_xor_sync(0xffffffffu, orv, o);
+    if ((tid & 31) == 0 && orv) atomicOr(&s_or, orv);
+    __syncthreads();
+    const int top_bit = s_or ? 63 - __clzll(s_or) : 0;
+    unsigned long long mask = 0;
+    for (int shift = (top_bit / 8) * 8; shift >= 0; shift -= 8) {
+        for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
+        __syncthreads();
+        const unsigned long long prefix = s_prefix;
+        for (int j = tid; j < K; j += kTopkThreads) {
+            unsigned long long v = s[j];
+            if ((v & mask) == prefix) atomicAdd(&hist[(v >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (tid < 32) {
+            // lane l owns digits 255-8l .. 248-8l (descending)
+            int cnt[8], tot = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) { cnt[i] = (int)hist[255 - 8 * tid - i]; tot += cnt[i]; }
+            int incl = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o) incl += y;
+            }
+            int above = incl - tot;
+            const int rem = s_remaining;
+            if (above < rem && rem <= incl) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (above < rem && rem <= above + cnt[i]) {
+                        s_digit = 255 - 8 * tid - i;
+                        s_above = above;
+                    }
+                    above += cnt[i];
+                }
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            s_prefix = prefix | ((unsigned long long)s_digit << shift);
+            s_remaining -= s_above;
+        }
+        mask |= 255ull << shift;
+        __syncthreads();
+    }
+    // s_prefix is now the k-th largest score T; s_remaining of the channels equal to T are taken.
+    const unsigned long long T = s_prefix;
+    const int take_eq = s_remaining;
+    // Each thread owns a contiguous run of channels so that scans follow channel order.
+    const int per = (K + kTopkThreads - 1) / kTopkThreads;
+    const int j0 = tid * per, j1 = min(K, j0 + per);
+    int n_eq = 0;
+    for (int j = j0; j < j1; ++j) n_eq += (s[j] == T);
+    int total;
+    int eq_rank = block_exclusive_scan(n_eq, warp_sums, &total);
+    int n_sel = 0;
+    {
+        int r = eq_rank;
+        for (int j = j0; j < j1; ++j) {
+            unsigned long long v = s[j];
+            bool sel = v > T || (v == T && r < take_eq);
+            r += (v == T);
+            n_sel += sel;
+        }
+    }
+    int pos = block_exclusive_scan(n_sel, warp_sums, &total);
+    {
+        int r = eq_rank;
+        for (int j = j0; j < j1; ++j) {
+            unsigned long long v = s[j];
+            bool sel = v > T || (v == T && r < take_eq);
+            r += (v == T);
+            if (sel) out[pos++] = j;
+        }
+    }
+}
+
+// ------------------------------------------------------------------------ activation tail
+// One warp per row; lane b handles tail block b (16 selected channels).
+__global__ void __launch_bounds__(256) act_tail_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, int K, int k,
+                                                        Groups gr, const nvq_tensor_scale* __restrict__ ts,
+                                                        const int32_t* __restrict__ idx, uint8_t* __restrict__ codes,
+                                                        int64_t ld_codes, uint8_t* __restrict__ sf, int64_t sf_cols)
+{
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= gr.total_rows) return;
+    const int g = group_of_row(gr, row);
+    int64_t gb, ge;
+    group_range(gr, g, gb, ge);
+    if (row < gb || row >= ge) return;
+    const float s_enc = ts[g].s_enc, s_dec = ts[g].s_dec;
+    const int32_t* sel = idx + (int64_t)g * k;
+    const int nbt = k / 16;
+    const __nv_bfloat16* xr = x + row * ldx;
+    for (int b = lane; b < nbt; b += 32) {
+        float rv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int j = sel[b * 16 + i];
+            const float xv = __bfloat162float(xr[j]);
+            const uint32_t sb = sf[sf_offset(row, j >> 4, sf_cols)];
+            const float sbv = e4m3_value(sb);
+            uint32_t code;
+            if (sb == 0) {
+                code = (__float_as_uint(xv) >> 28) & 0x8u;
+            } else {
+                const float e_b = __fdiv_rn(s_enc, sbv);
+                code = e2m1x2(__fmul_rn(xv, e_b), 0.0f) & 0xfu;
+            }
+            rv[i] = residual(xv, code, __fmul_rn(sbv, s_dec));
+        }
+        BlockOut o = quantize16(rv, s_enc, s_dec);
+        *reinterpret_cast<uint2*>(codes + row * ld_codes + (K + 16 * b) / 2) = make_uint2(o.code_lo, o.code_hi);
+        sf[sf_offset(row, K / 16 + b, sf_cols)] = (uint8_t)o.sb;
+    }
+    for (int64_t c = (K + k) / 16 + lane; c < sf_cols; c += 32) sf[sf_offset(row, c, sf_cols)] = 0;
+}
+
+// ------------------------------------------------------------------------ weight tail
+// Thread per (weight row, tail block).  Weight rows of group g are [g * N, (g + 1) * N).
+__global__ void __launch_bounds__(256) weight_tail_kernel(uint8_t* __restrict__ codes, int64_t ld_codes,
+                                                           uint8_t* __restrict__ sf, int64_t sf_cols, int64_t N, int K,
+                                                           int k, int G, const nvq_tensor_scale* __restrict__ ts,
+                                                           const int32_t* __restrict__ idx, int idx_per_group)
+{
+    const int nbt = k / 16;
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t total = (int64_t)G * N * nbt;
+    if (t >= total) return;
+    const int b = (int)(t % nbt);
+    const int64_t row = t / nbt;
+    const int g = (int)(row / N);
+    const float s_enc = ts[g].s_enc, s_dec = ts[g].s_dec;
+    const int32_t* sel = idx + (idx_per_group ? (int64_t)g * k : 0);
+    const uint8_t* cr = codes + row * ld_codes;
+    float wv[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int j = sel[b * 16 + i];
+        const uint32_t c = (cr[j >> 1] >> ((j & 1) * 4)) & 0xfu;
+        const uint32_t sb = sf[sf_offset(row, j >> 4, sf_cols)];
+        wv[i] = __fmul_rn(e2m1_value(c), __fmul_rn(e4m3_value(sb), s_dec));
+    }
+    BlockOut o = quantize16(wv, s_enc, s_dec);
+    *reinterpret_cast<uint2*>(codes + row * ld_codes + (K + 16 * b) / 2) = make_uint2(o.code_lo, o.code_hi);
+    sf[sf_offset(row, K / 16 + b, sf_cols)] = (uint8_t)o.sb;
+    if (b == 0)
+        for (int64_t c = (K + k) / 16; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
+}
+
+nvq_status weight_tail_impl(uint8_t* codes, int64_t ld_codes, uint8_t* sf, int64_t sf_cols, int64_t N, int K, int k,
+                            int G, const nvq_tensor_scale* ts, const int32_t* idx, int idx_per_group, cudaStream_t st)
+{
+    if (k == 0) return NVQ_OK;
+    const int64_t total = (int64_t)G * N * (k / 16);
+    const int threads = 256;
+    weight_tail_kernel<<<(unsigned)((total + threads - 1) / threads), threads, 0, st>>>(
+        codes, ld_codes, sf, sf_cols, N, K, k, G, ts, idx, idx_per_group);
+    NVQ_LAUNCH_CHECK("weight_tail_kernel");
+    return NVQ_OK;
+}
+
+}  // namespace nvq
+
+using namespace nvq;
+
+extern "C" nvq_status rac_select_quantize(const void* x, int64_t rows, int64_t K, int64_t ldx, const int64_t* grp_off,
+                                          const int64_t* grp_rows, int32_t groups, const nvq_tensor_scale* tscale,
+                                          const uint64_t* scores, int32_t k, uint8_t* codes, int64_t ld_codes,
+                                          uint8_t* sf, int64_t sf_cols, int32_t* idx, void* stream)
+{
+    NVQ_CHECK_ARG(x && codes && sf && tscale, NVQ_ERR_ARG, "rac_select_quantize: null pointer argument");
+    NVQ_CHECK_ARG(k == 0 || (scores && idx), NVQ_ERR_ARG, "rac_select_quantize: scores and idx are required when k > 0");
+    NVQ_CHECK_ARG(rows >= 1 && rows <= (1ll << 24), NVQ_ERR_SHAPE, "rac_select_quantize: rows outside [1, 2^24]");
+    NVQ_CHECK_ARG(K >= 16 && K <= 8192 && K % 16 == 0, NVQ_ERR_SHAPE, "rac_select_quantize: K must be a multiple of 16 in [16, 8192]");
+    NVQ_CHECK_ARG(k >= 0 && k <= K && k % 16 == 0 && k <= 512, NVQ_ERR_SHAPE,
+                  "rac_select_quantize: k=%d must be a multiple of 16 in [0, min(K, 512)]", k);
+    NVQ_CHECK_ARG(groups >= 1 && groups <= 4096, NVQ_ERR_SHAPE, "rac_select_quantize: groups outside [1, 4096]");
+    NVQ_CHECK_ARG(grp_off || groups == 1 || rows % groups == 0, NVQ_ERR_SHAPE, "rac_select_quantize: rows not divisible by groups");
+    NVQ_CHECK_ARG(ldx >= K && ldx % 8 == 0, NVQ_ERR_ALIGN, "rac_select_quantize: ldx must be >= K and a multiple of 8");
+    NVQ_CHECK_ARG(ld_codes >= (K + k) / 2 && ld_codes % 16 == 0, NVQ_ERR_ALIGN, "rac_select_quantize: ld_codes must be >= (K+k)/2 and a multiple of 16");
+    NVQ_CHECK_ARG(sf_cols >= (K + k) / 16 && sf_cols % 4 == 0, NVQ_ERR_SHAPE, "rac_select_quantize: sf_cols must be >= (K+k)/16 and a multiple of 4");
+    NVQ_CHECK_ARG(aligned(codes, 16), NVQ_ERR_ALIGN, "rac_select_quantize: codes must be 16-byte aligned");
+    set_error("");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Groups gr{grp_off, grp_rows, groups, rows};
+    if (k > 0) {
+        size_t smem = sizeof(unsigned long long) * (size_t)K;
+        if (smem > 32 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(topk_kernel)");
+        }
+        topk_kernel<<<groups, kTopkThreads, smem, st>>>(reinterpret_cast<const unsigned long long*>(scores), (int)K, k, idx);
+        NVQ_LAUNCH_CHECK("topk_kernel");
+    }
+    act_tail_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), ldx, (int)K, k, gr,
+                                                                tscale, idx, codes, ld_codes, sf, sf_cols);
+    NVQ_LAUNCH_CHECK("act_tail_kernel");
+    return NVQ_OK;
+}
+
+extern "C" nvq_status rac_weight_tail(int32_t groups, int64_t N, int64_t K, int32_t k, const int32_t* idx,
+                                      int32_t idx_per_group, uint8_t* b_codes, int64_t ldb, uint8_t* b_sf,
+                                      int64_t b_sf_cols, const nvq_tensor_scale* b_tscale, void* stream)
+{
+    NVQ_CHECK_ARG(idx && b_codes && b_sf && b_tscale, NVQ_ERR_ARG, "rac_weight_tail: null pointer argument");
+    NVQ_CHECK_ARG(groups >= 1 && groups <= 4096 && N >= 1 && (int64_t)groups * N <= (1ll << 24), NVQ_ERR_SHAPE,
+                  "rac_weight_tail: groups*N outside [1, 2^24]");
+    NVQ_CHECK_ARG(K >= 16 && K <= 8192 && K % 16 == 0, NVQ_ERR_SHAPE, "rac_weight_tail: K must be a multiple of 16 in [16, 8192]");
+    NVQ_CHECK_ARG(k >= 16 && k <= K && k % 16 == 0 && k <= 512, NVQ_ERR_SHAPE, "rac_weight_tail: bad k=%d", k);
+    NVQ_CHECK_ARG(ldb % 16 == 0 && ldb >= (K + k) / 2 && aligned(b_codes, 16), NVQ_ERR_ALIGN,
+                  "rac_weight_tail: ldb must be a multiple of 16 covering (K+k)/2 bytes");
+    NVQ_CHECK_ARG(b_sf_cols % 4 == 0 && b_sf_cols >= (K + k) / 16, NVQ_ERR_SHAPE, "rac_weight_tail: b_sf_cols too small");
+    set_error("");
+    return weight_tail_impl(b_codes, ldb, b_sf, b_sf_cols, N, (int)K, k, groups, b_tscale, idx, idx_per_group,
+                            static_cast<cudaStream_t>(stream));
+}

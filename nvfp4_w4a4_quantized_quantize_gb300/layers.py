@@ -1,0 +1,178 @@
+"""The rollout-side RAC linear layer and MoE expert layer, composed from the C-ABI calls.
+
+Every arithmetic step runs in libnvfp4rac.so; this module only allocates buffers once (torch
+device memory) and issues the calls on one stream, so a forward pass makes no allocation and
+can be captured in a CUDA graph.
+
+QUADS (arXiv 2607.15810) §3.3: activations are quantized online (Eq. (9)), the k channels with
+the largest residual norm are selected per forward pass (Eq. (23)-(24)), their residual is
+quantized a second time and carried as extra K-columns of the same W4A4 GEMM (Eq. (21)).
+§3.2: weights are quantized once by the same quantizer the trainer's QDQ uses (Eq. (12)).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _lib as L
+
+
+def _round_up(x: int, m: int) -> int:
+    return (x + m - 1) // m * m
+
+
+@dataclass
+class Operand:
+    """An NVFP4 GEMM operand: codes [rows, ld] (two per byte), blocked UE4M3 scales, tensor scales."""
+    codes: torch.Tensor
+    sf: torch.Tensor
+    sf_cols: int
+    tscale: torch.Tensor  # float32 [G, 4]: amax, s_enc, s_dec, shift_e (int32 bits)
+    rows: int
+    K: int
+    k: int
+
+    @staticmethod
+    def empty(rows: int, K: int, k_max: int, groups: int = 1, device="cuda") -> "Operand":
+        ktot = K + k_max
+        ld = _round_up(max(ktot // 2, 16), 16)
+        cols = L.sf_cols(ktot)
+        codes = torch.zeros(rows, ld, dtype=torch.uint8, device=device)
+        sf = torch.zeros(L.sf_bytes(rows, cols), dtype=torch.uint8, device=device)
+        ts = torch.zeros(groups, 4, dtype=torch.float32, device=device)
+        return Operand(codes, sf, cols, ts, rows, K, k_max)
+
+
+def quantize_weights(w: torch.Tensor, k_max: int, w_hat: Optional[torch.Tensor] = None,
+                     w_hat_dtype: int = L.NVQ_BF16) -> Operand:
+    """W [G, N, K] (or [N, K]) bf16 -> NVFP4 operand with room for a k_max-column RAC tail."""
+    w3 = w if w.dim() == 3 else w.unsqueeze(0)
+    G, N, K = w3.shape
+    op = Operand.empty(G * N, K, k_max, G, device=w.device)
+    L.weight_qdq(w3, G, N, K, op.codes, op.sf, op.sf_cols, op.tscale, w_hat=w_hat, w_hat_dtype=w_hat_dtype)
+    return op
+
+
+class RacLinear:
+    """Dense rollout linear layer Y = X W^T with NVFP4 W4A4 + RAC (k compensated channels)."""
+
+    def __init__(self, w: torch.Tensor, k: int, max_rows: int):
+        self.N, self.K = w.shape
+        self.k = k
+        self.w = quantize_weights(w, k)
+        self.a = Operand.empty(max_rows, self.K, k, 1, device=w.device)
+        self.scores = torch.zeros(self.K, dtype=torch.int64, device=w.device)
+        self.idx = torch.zeros(max(k, 1), dtype=torch.int32, device=w.device)
+
+    def forward(self, x: torch.Tensor, out: torch.Tensor, k: Optional[int] = None, stream=None):
+        k = self.k if k is None else k
+        M = x.shape[0]
+        L.nvfp4_quantize(x, self.a.codes, self.a.sf, self.a.sf_cols, self.a.tscale,
+                         scores=self.scores if k else None, zero_pad=(k == 0), stream=stream)
+        if k:
+            L.rac_select_quantize(x, self.a.tscale, self.scores, k, self.a.codes, self.a.sf, self.a.sf_cols,
+                                  self.idx, stream=stream)
+        L.w4a4_rac_grouped_gemm(self.a.codes, self.a.sf, self.a.sf_cols, self.a.tscale, self.w.codes, self.w.sf,
+                                self.w.sf_cols, self.w.tscale, self.N, self.K, k, self.idx if k else None, out,
+                                rows=M, stream=stream)
+        return out
+
+
+class MoERacLayer:
+    """Routed SwiGLU expert layer with NVFP4 W4A4 + RAC in both expert GEMMs.
+
+    gate/up:  A = Q(X) per token with one channel set S over all tokens (the W13 site of QUADS
+              §3.3), gathered into the routed layout; fused gate/up weights W13 [E, 2I, H];
+              SwiGLU in the GEMM epilogue -> h [routed rows, I] bf16.
+    down:     h quantized with one tensor scale and one channel set per expert; W2 [E, H, I];
+              the routing weight is applied in the GEMM epilogue -> y; combine sums the topk
+              rows of every token.
+    """
+
+    def __init__(self, w13: torch.Tensor, w2: torch.Tensor, k: int, topk: int, max_tokens: int):
+        dev = w13.device
+        self.E, twoI, self.H = w13.shape
+        self.I = twoI // 2
+        self.k, self.topk, self.T = k, topk, max_tokens
+        self.w13 = quantize_weights(w13, k)
+        self.w2 = quantize_weights(w2, k)
+        cap = L.moe_capacity(max_tokens, topk, self.E)
+        self.cap = cap
+        E = self.E
+        self.grp_off = torch.zeros(E + 1, dtype=torch.int64, device=dev)
+        self.grp_rows = torch.zeros(E, dtype=torch.int64, device=dev)
+        self.row_src = torch.zeros(cap, dtype=torch.int32, device=dev)
+        self.row_of = torch.zeros(max_tokens * topk, dtype=torch.int64, device=dev)
+        self.row_w = torch.zeros(cap, dtype=torch.float32, device=dev)
+        self.ws = torch.zeros(L.moe_dispatch_workspace_size(max_tokens, topk, E), dtype=torch.uint8, device=dev)
+        self.a_tok = Operand.empty(max_tokens, self.H, k, 1, device=dev)
+        self.scores1 = torch.zeros(self.H, dtype=torch.int64, device=dev)
+        self.idx1 = torch.zeros(max(k, 1), dtype=torch.int32, device=dev)
+        self.a_routed = Operand.empty(cap, self.H, k, 1, device=dev)
+        self.h = torch.zeros(cap, self.I, dtype=torch.bfloat16, device=dev)
+        self.a2 = Operand.empty(cap, self.I, k, E, device=dev)
+        self.scores2 = torch.zeros(E, self.I, dtype=torch.int64, device=dev)
+        self.idx2 = torch.zeros(E, max(k, 1), dtype=torch.int32, device=dev)
+        self.y = torch.zeros(cap, self.H, dtype=torch.bfloat16, device=dev)
+
+    def kernel_launches_per_step(self) -> int:
+        """Kernels one forward() launches (dispatch 4; per GEMM side: quantize 2, selection and
+        residual tail 2, weight tail 1, GEMM 1; gather 1; combine 1)."""
+        side = 2 + (3 if self.k else 0) + 1
+        return 4 + 1 + 2 * side + 1
+
+    def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, out: torch.Tensor,
+                stream=None, events: Optional[dict] = None):
+        """events: optional dict that receives (start, end) CUDA events around the stages
+        'quant_rac_tokens', 'gemm_gate_up' and 'gemm_down' (for per-kernel timing)."""
+        T = x.shape[0]
+        k, E, H, I = self.k, self.E, self.H, self.I
+        st = torch.cuda.current_stream() if stream is None else stream
+
+        def mark(name, pos):
+            if events is not None:
+                ev = events.setdefault(name, (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+                ev[pos].record(st)
+
+        L.moe_dispatch(topk_ids, topk_w, E, self.grp_off, self.grp_rows, self.row_src, self.row_of, self.row_w,
+                       self.ws, stream=stream)
+        # gate/up input: per-token quantization, one tensor scale, one channel set
+        mark("quant_rac_tokens", 0)
+        L.nvfp4_quantize(x, self.a_tok.codes, self.a_tok.sf, self.a_tok.sf_cols, self.a_tok.tscale,
+                         scores=self.scores1 if k else None, zero_pad=(k == 0), stream=stream)
+        if k:
+            L.rac_select_quantize(x, self.a_tok.tscale, self.scores1, k, self.a_tok.codes, self.a_tok.sf,
+                                  self.a_tok.sf_cols, self.idx1, stream=stream)
+        mark("quant_rac_tokens", 1)
+        L.nvfp4_gather_rows(self.a_tok.codes, self.a_tok.sf, self.a_tok.sf_cols, T, self.row_src, self.topk, H + k,
+                            self.a_routed.codes, self.a_routed.sf, stream=stream)
+        if k:
+            L.rac_weight_tail(E, 2 * I, H, k, self.idx1, self.w13.codes, self.w13.sf, self.w13.sf_cols,
+                              self.w13.tscale, stream=stream)
+        mark("gemm_gate_up", 0)
+        L.w4a4_rac_grouped_gemm(self.a_routed.codes, self.a_routed.sf, self.a_routed.sf_cols, self.a_tok.tscale,
+                                self.w13.codes, self.w13.sf, self.w13.sf_cols, self.w13.tscale, 2 * I, H, k,
+                                None, self.h, groups=E, grp_off=self.grp_off, grp_rows=self.grp_rows,
+                                rows=self.cap, epilogue=L.NVQ_EPI_SWIGLU, stream=stream)
+        mark("gemm_gate_up", 1)
+        # down input: per-expert tensor scale and channel set
+        L.nvfp4_quantize(self.h, self.a2.codes, self.a2.sf, self.a2.sf_cols, self.a2.tscale,
+                         scores=self.scores2 if k else None, grp_off=self.grp_off, grp_rows=self.grp_rows,
+                         groups=E, zero_pad=(k == 0), stream=stream)
+        if k:
+            L.rac_select_quantize(self.h, self.a2.tscale, self.scores2, k, self.a2.codes, self.a2.sf,
+                                  self.a2.sf_cols, self.idx2, grp_off=self.grp_off, grp_rows=self.grp_rows,
+                                  groups=E, stream=stream)
+            L.rac_weight_tail(E, H, I, k, self.idx2, self.w2.codes, self.w2.sf, self.w2.sf_cols, self.w2.tscale,
+                              idx_per_group=True, stream=stream)
+        mark("gemm_down", 0)
+        L.w4a4_rac_grouped_gemm(self.a2.codes, self.a2.sf, self.a2.sf_cols, self.a2.tscale, self.w2.codes,
+                                self.w2.sf, self.w2.sf_cols, self.w2.tscale, H, I, k, None,
+                                self.y, groups=E, grp_off=self.grp_off, grp_rows=self.grp_rows, rows=self.cap,
+                                a_scale_per_group=True, idx_per_group=True, epilogue=L.NVQ_EPI_ROW_SCALE,
+                                row_w=self.row_w, stream=stream)
+        mark("gemm_down", 1)
+        L.moe_combine(self.y, self.row_of, T, self.topk, H, out, stream=stream)
+        return out

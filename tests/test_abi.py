@@ -1,0 +1,51 @@
+"""The C-ABI library loads and exports every function include/nvfp4rac.h declares; host-only
+helpers behave as documented.  No compute call is made (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "nvfp4rac.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z][a-z0-9_]*)\s*\(", src)) - {"sizeof", "if", "return"})
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ["nvfp4_quantize", "rac_select_quantize", "w4a4_rac_grouped_gemm", "weight_qdq"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    from nvfp4_w4a4_quantized_quantize_gb300 import _lib
+    lib = ctypes.CDLL(_lib.LIB_PATH)
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(_declared()) == set(_lib.EXPORTED)
+
+
+def test_layout_helpers():
+    from nvfp4_w4a4_quantized_quantize_gb300 import _lib as L
+    from tests.nvfp4_testutil import sf_index
+    assert L.sf_cols(256) == 16 and L.sf_cols(272) == 20 and L.sf_cols(16) == 4
+    assert L.sf_bytes(1, 4) == 512 and L.sf_bytes(129, 8) == 256 * 8
+    idx = sf_index(300, 20, 20)
+    for r in [0, 1, 31, 32, 127, 128, 299]:
+        for c in [0, 3, 4, 19]:
+            assert L.sf_offset(r, c, 20) == idx[r, c]
+    assert len(set(idx.ravel().tolist())) == idx.size   # a permutation
+    assert L.moe_capacity(16384, 8, 128) >= 16384 * 8 + 128 * 127
+
+
+def test_product_path_has_no_oracle_import():
+    pkg = os.path.join(ROOT, "nvfp4_w4a4_quantized_quantize_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                txt = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in txt and "from oracle" not in txt and "nvfp4_oracle" not in txt, f

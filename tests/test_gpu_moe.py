@@ -1,0 +1,149 @@
+"""Stage-wise GPU parity of the MoE expert layer with W4A4 + RAC in both expert GEMMs.
+
+Each stage is compared with the oracle fed by the GPU's own (already checked) upstream output:
+dispatch, token quantization and selection, gather (bit-exact); gate/up GEMM with SwiGLU
+(2e-3 rule); per-expert quantization and selection of h (bit-exact); down GEMM with the routing
+weight (2e-3 rule); combine (bit-exact)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from nvfp4_w4a4_quantized_quantize_gb300 import workloads as wl
+from tests.nvfp4_testutil import GEMM_RTOL, bf16_bits, bf16_tensor, gemm_error, tscale_fields, unswizzle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from nvfp4_w4a4_quantized_quantize_gb300 import _lib
+    _lib.set_wait_limit(1 << 31)
+    return _lib
+
+
+def _operand_rows(op, rows, ktot):
+    codes = op.codes.cpu().numpy()[rows, :ktot // 2]
+    sfl = unswizzle(op.sf, int(rows.max()) + 1, ktot // 16, op.sf_cols)[rows]
+    return codes, sfl
+
+
+def _check_layer(L, T, H, E, topk, I, k, routing, seed, sample_rows=None):
+    from nvfp4_w4a4_quantized_quantize_gb300.layers import MoERacLayer
+    cfg = wl.MoELayer("t", T=T, H=H, E=E, topk=topk, I=I, k=k, seed=seed, routing=routing, n_outliers=max(1, H // 100))
+    x_bits, ids, tw, _ = cfg.make_tokens()
+    w13_bits, w2_bits = cfg.make_weights()
+    dev = "cuda"
+    w13 = bf16_tensor(w13_bits.reshape(E * 2 * I, H)).view(E, 2 * I, H)
+    w2 = bf16_tensor(w2_bits.reshape(E * H, I)).view(E, H, I)
+    layer = MoERacLayer(w13, w2, k, topk, T)
+    x = bf16_tensor(x_bits)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    layer.forward(x, torch.from_numpy(ids).to(dev), torch.from_numpy(tw).to(dev), out)
+    torch.cuda.synchronize()
+    assert L.device_status() == (0, 0)
+
+    # 1. dispatch
+    grp_off = layer.grp_off.cpu().numpy()
+    grp_rows = layer.grp_rows.cpu().numpy()
+    row_src = layer.row_src.cpu().numpy()
+    row_of = layer.row_of.cpu().numpy()
+    row_w = layer.row_w.cpu().numpy()
+    o_off, o_src = oracle.moe_dispatch(ids, E)
+    assert np.array_equal(grp_rows, np.diff(o_off))
+    assert np.all(grp_off[:-1] % 128 == 0)
+    for g in range(E):
+        seg = row_src[grp_off[g]:grp_off[g] + grp_rows[g]]
+        assert np.array_equal(seg, o_src[o_off[g]:o_off[g + 1]])
+        assert np.all(row_src[grp_off[g] + grp_rows[g]:grp_off[g + 1]] == -1)
+    assert np.array_equal(row_src[row_of], np.arange(T * topk))
+    assert np.array_equal(row_w[row_of], tw.ravel())
+
+    # 2. token quantization + selection (one tensor scale and one channel set for all tokens)
+    q1 = oracle.rac_quantize(x_bits, k)
+    assert np.array_equal(layer.idx1.cpu().numpy()[:k], q1.idx)
+    a1c, a1s = _operand_rows(layer.a_tok, np.arange(T), H + k)
+    assert np.array_equal(a1c, np.concatenate([q1.codes, q1.tail_codes], 1))
+    assert np.array_equal(a1s, np.concatenate([q1.scales, q1.tail_scales], 1))
+
+    # 3. gather into the routed layout
+    routed = np.nonzero(row_src >= 0)[0]
+    if sample_rows is not None and routed.size > sample_rows:
+        routed = np.sort(np.random.default_rng(seed).choice(routed, sample_rows, replace=False))
+    arc, ars = _operand_rows(layer.a_routed, routed, H + k)
+    tok = row_src[routed] // topk
+    assert np.array_equal(arc, a1c[tok]) and np.array_equal(ars, a1s[tok])
+
+    # weights as the GEMM saw them (tails rebuilt inside the calls): check them against the oracle
+    _, _, w13_sdec, _ = tscale_fields(layer.w13.tscale)
+    _, _, w2_sdec, _ = tscale_fields(layer.w2.tscale)
+    h_gpu = bf16_bits(layer.h)
+    worst_h = 0.0
+    groups_of_rows = np.searchsorted(grp_off, routed, side="right") - 1
+    for g in np.unique(groups_of_rows):
+        rows_g = routed[groups_of_rows == g]
+        wg = w13_bits[g]
+        wts = oracle.tensor_scale(wg)
+        assert np.float32(wts.s_dec) == w13_sdec[g]
+        wc, ws = oracle.quantize(wg, wts)
+        tc, tsc = oracle.weight_tail(wc, ws, wts, q1.idx)
+        bc, bs = _operand_rows(layer.w13, np.arange(g * 2 * I, (g + 1) * 2 * I), H + k)
+        assert np.array_equal(bc, np.concatenate([wc, tc], 1)) and np.array_equal(bs, np.concatenate([ws, tsc], 1))
+        ac, as_ = _operand_rows(layer.a_routed, rows_g, H + k)
+        ref = oracle.gemm(ac, as_, bc, bs, q1.ts.s_dec, wts.s_dec)
+        href = oracle.swiglu(ref[:, :I], ref[:, I:]).reshape(len(rows_g), I)
+        worst_h = max(worst_h, gemm_error(wl.bf16_bits_to_f32(h_gpu[rows_g]), href))
+    assert worst_h <= GEMM_RTOL, worst_h
+
+    # 4./5. per-expert quantization of the GPU's h, selection, down GEMM with routing weights
+    a2_amax, _, a2_sdec, _ = tscale_fields(layer.a2.tscale)
+    idx2 = layer.idx2.cpu().numpy()
+    y_gpu = bf16_bits(layer.y)
+    worst_y = 0.0
+    for g in range(E):
+        c = int(grp_rows[g])
+        if c == 0:
+            continue
+        rows_g = np.arange(grp_off[g], grp_off[g] + c)
+        hq = oracle.rac_quantize(h_gpu[rows_g], k)
+        assert np.float32(hq.ts.amax) == a2_amax[g] and np.float32(hq.ts.s_dec) == a2_sdec[g]
+        assert np.array_equal(idx2[g, :k], hq.idx)
+        ac, as_ = _operand_rows(layer.a2, rows_g, I + k)
+        assert np.array_equal(ac, np.concatenate([hq.codes, hq.tail_codes], 1))
+        assert np.array_equal(as_, np.concatenate([hq.scales, hq.tail_scales], 1))
+        if sample_rows is not None and c > 64:
+            pick = np.sort(np.random.default_rng(g).choice(c, 64, replace=False))
+        else:
+            pick = np.arange(c)
+        wg = w2_bits[g]
+        wts = oracle.tensor_scale(wg)
+        wc, ws = oracle.quantize(wg, wts)
+        tc, tsc = oracle.weight_tail(wc, ws, wts, hq.idx)
+        bc, bs = _operand_rows(layer.w2, np.arange(g * H, (g + 1) * H), I + k)
+        assert np.array_equal(bc, np.concatenate([wc, tc], 1)) and np.array_equal(bs, np.concatenate([ws, tsc], 1))
+        ref = oracle.gemm(ac[pick], as_[pick], bc, bs, hq.ts.s_dec, wts.s_dec)
+        ref = ref * row_w[rows_g[pick]][:, None].astype(np.float64)
+        worst_y = max(worst_y, gemm_error(wl.bf16_bits_to_f32(y_gpu[rows_g[pick]]), ref))
+    assert worst_y <= GEMM_RTOL, worst_y
+
+    # 6. combine of the GPU's y, bit-exact
+    out_bits = bf16_bits(out)
+    tsel = np.arange(T) if sample_rows is None else np.sort(np.random.default_rng(1).choice(T, min(T, 512), replace=False))
+    pos = row_of.reshape(T, topk)[tsel].ravel()
+    ref_out = oracle.moe_combine(y_gpu, pos, topk)
+    assert np.array_equal(out_bits[tsel], ref_out)
+    return worst_h, worst_y
+
+
+def test_moe_layer_small_zipf(L):
+    _check_layer(L, T=300, H=256, E=8, topk=2, I=128, k=16, routing="zipf", seed=21)
+
+
+def test_moe_layer_small_uniform_topk8(L):
+    _check_layer(L, T=200, H=512, E=16, topk=8, I=256, k=32, routing="uniform", seed=22)
+
+
+def test_moe_layer_without_rac(L):
+    _check_layer(L, T=130, H=256, E=4, topk=2, I=128, k=0, routing="uniform", seed=23)
