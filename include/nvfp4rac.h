@@ -96,6 +96,13 @@ nvq_status nvq_device_status(void* stream, int32_t* status, int32_t* where);
  * Applies to launches made after the call on the current device. */
 nvq_status nvq_set_wait_limit(uint64_t cycles);
 
+/* Measured NVFP4 tensor-core rate of the current GPU (a roofline reference; not part of the
+ * paper's method): back-to-back tcgen05 M128 N256 K64 mxf4nvf4 MMAs with FP32 accumulation in
+ * TMEM on every SM, no memory traffic, mmas_per_sm per SM (16 .. 2^20).  with_cp != 0 adds the
+ * three scale-factor copies into TMEM that the GEMM issues per MMA.  Synchronous on `stream`;
+ * *tflops receives the achieved TFLOP/s. */
+nvq_status nvq_fp4_mma_rate(int32_t mmas_per_sm, int32_t with_cp, float* tflops, void* stream);
+
 /* Scale-layout helpers (host functions, no device access). */
 int64_t nvq_sf_cols(int64_t ktot);                      /* roundup(ktot / 16, 4) */
 int64_t nvq_sf_bytes(int64_t rows, int64_t sf_cols);    /* roundup(rows, 128) * sf_cols */
@@ -177,7 +184,8 @@ nvq_status weight_qdq(const void* w, int32_t groups, int64_t N, int64_t K, int64
  *             grp_off NULL is a dense GEMM over all `rows`.
  *   rows      number of rows of A and out (buffer extent); rows <= 2^24.
  *   a_codes, lda, a_sf, a_sf_cols    A = quantized activations + RAC tail (nvfp4_quantize +
- *             rac_select_quantize).  a_tscale  [groups] if a_scale_per_group else [1].
+ *             rac_select_quantize; for routed MoE rows, nvfp4_gather_rows output), [rows] rows.
+ *             a_tscale  [groups] if a_scale_per_group else [1].
  *   b_codes, ldb, b_sf, b_sf_cols    W_g = rows [g * N, (g + 1) * N) (weight_qdq output);
  *             tail columns rewritten by this call.  b_tscale  [groups].
  *   N, K, k   N % 256 == 0 (NVQ_EPI_SWIGLU: N / 2 % 128 == 0); K % 64 == 0; k as above.
@@ -233,7 +241,8 @@ nvq_status moe_dispatch(const int32_t* topk_ids, const float* topk_w, int64_t to
 /*
  * nvfp4_gather_rows -- copies quantized rows (codes and blocked scales of K_tot columns) into
  * the routed layout: out row r = source row row_src[r] / topk, padding rows (row_src < 0) get
- * zero codes and zero scales.  out_sf uses the same sf_cols as sf.
+ * zero codes and zero scales.  out_sf uses the same sf_cols as sf.  With out_codes NULL only
+ * the scales are copied.
  */
 nvq_status nvfp4_gather_rows(const uint8_t* codes, int64_t ld_codes, const uint8_t* sf,
                              int64_t sf_cols, int64_t src_rows, const int32_t* row_src,

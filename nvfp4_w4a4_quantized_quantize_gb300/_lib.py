@@ -19,6 +19,7 @@ _SIGS = {
     "nvq_last_error": ([], C.c_char_p),
     "nvq_device_status": ([_P, _P, _P], C.c_int),
     "nvq_set_wait_limit": ([_U64], C.c_int),
+    "nvq_fp4_mma_rate": ([_I32, _I32, _P, _P], C.c_int),
     "nvq_sf_cols": ([_I64], _I64),
     "nvq_sf_bytes": ([_I64, _I64], _I64),
     "nvq_sf_offset": ([_I64, _I64, _I64], _I64),
@@ -113,6 +114,13 @@ def device_status(stream=None):
     return st.value, wh.value
 
 
+def fp4_mma_rate(mmas_per_sm: int = 65536, with_cp: bool = False, stream=None) -> float:
+    """Measured TFLOP/s of back-to-back NVFP4 MMAs on every SM (no memory traffic)."""
+    v = C.c_float(0.0)
+    _check("nvq_fp4_mma_rate", LIB.nvq_fp4_mma_rate(mmas_per_sm, int(bool(with_cp)), C.byref(v), _stream(stream)))
+    return float(v.value)
+
+
 # --------------------------------------------------------------------------- the C ABI calls
 def nvfp4_quantize(x, codes, sf, sf_cols_, tscale, scores=None, grp_off=None, grp_rows=None, groups=1,
                    zero_pad=False, rows=None, K=None, stream=None):
@@ -165,7 +173,7 @@ def moe_dispatch(topk_ids, topk_w, groups, grp_off, grp_rows, row_src, row_of, r
 def nvfp4_gather_rows(codes, sf, sf_cols_, src_rows, row_src, topk, ktot, out_codes, out_sf, stream=None):
     _check("nvfp4_gather_rows", LIB.nvfp4_gather_rows(
         _ptr(codes), codes.stride(0), _ptr(sf), sf_cols_, src_rows, _ptr(row_src), topk, row_src.numel(), ktot,
-        _ptr(out_codes), out_codes.stride(0), _ptr(out_sf), _stream(stream)))
+        _ptr(out_codes), out_codes.stride(0) if out_codes is not None else 0, _ptr(out_sf), _stream(stream)))
 
 
 def moe_combine(y, row_of, tokens, topk, hidden, out, stream=None):

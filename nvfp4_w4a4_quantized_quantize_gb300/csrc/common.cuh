@@ -117,18 +117,15 @@ __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w <
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // Two fp32 -> two E2M1 codes in one byte (lo -> low nibble), round to nearest even, saturate.
-// The sign of each code is taken from the sign bit of its input so that values rounding to
-// zero keep their sign whatever the conversion instruction does with them.
+// The conversion keeps the sign of inputs that round to zero (-0 and small negatives give
+// 0x8), which is the sign convention of the codes; the GB300 tests check every bf16 input.
 __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi)
 {
-    uint16_t r;
-    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
-        : "=h"(r)
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r)
         : "f"(hi), "f"(lo));
-    uint32_t c = (uint32_t)r & 0x77u;
-    c |= (__float_as_uint(lo) >> 28) & 0x8u;
-    c |= (__float_as_uint(hi) >> 24) & 0x80u;
-    return c;
+    return r;
 }
 
 // fp32 (>= 0) -> E4M3 byte, round to nearest even, saturating at 448.
@@ -159,6 +156,15 @@ __device__ __forceinline__ float e2m1_value(uint32_t c)
     uint32_t lb = __byte_perm(lo_lo, lo_hi, m);
     uint32_t bits = ((hb & 0xffu) << 24) | ((lb & 0xffu) << 16) | ((c & 8u) << 28);
     return __uint_as_float(bits);
+}
+
+// Two E2M1 codes (one byte, element 0 in the low nibble) -> two fp32 values (exact).
+__device__ __forceinline__ float2 e2m1x2_value(uint32_t byte)
+{
+    uint32_t h;
+    uint16_t in = (uint16_t)(byte & 0xffu);
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h) : "h"(in));
+    return __half22float2(*reinterpret_cast<__half2*>(&h));
 }
 
 // Quantization of one 16-element block held as 8 bf16x2 words.  Returns the scale byte,

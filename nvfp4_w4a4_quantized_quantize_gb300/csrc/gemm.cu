@@ -32,7 +32,8 @@ constexpr int kSFABytes = kBM * kBK / 16;  // 2048: 4 atoms of 512 B
 constexpr int kSFBBytes = kBN * kBK / 16;  // 4096: 2 row blocks x 4 atoms
 constexpr int kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;  // 55296 (54 x 1024)
 constexpr int kSmemBytes = kStages * kStageBytes + 1024;
-constexpr int kThreads = 192;
+constexpr int kThreads = 352;  // warp 0 TMA, warp 1 MMA, warp 2 scale copies, warps 3-10 epilogue
+constexpr int kEpiThreads = 256;
 constexpr int kMaxGroups = 512;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;                  // 256 fp32 columns
@@ -93,14 +94,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 // Bounded wait; returns false (after recording the timeout) if the limit ran out or another
 // role of the CTA already gave up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const GemmArgs& a, volatile int* abort_flag,
-                                          int where)
+                                          int where, bool draining = false)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
+        if (!draining && *abort_flag) return false;
         if ((unsigned long long)(clock64() - t0) > a.wait_limit) {
             report_timeout(a.status, where);
             *abort_flag = 1;
@@ -179,6 +180,35 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v)
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 64 consecutive accumulator columns of this thread's TMEM lane (one load, then the wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v)
+{
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,"
+        "%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
 __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v)
 {
     uint32_t pk[16];
@@ -195,65 +225,107 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v
 // ------------------------------------------------------------------ tile scheduling
 struct Tile {
     int g;
-    int64_t row0;   // first A row of the tile
+    int row0;       // first A row of the tile (rows < 2^24)
     int rows;       // valid rows in the tile (<= 128)
     int nt;         // N tile
 };
 
-__device__ __forceinline__ Tile tile_of(int64_t t, int total_mtiles, const int* mt_pre, const GemmArgs& a)
+// Per-group tables in shared memory, filled once per CTA: first row, row count and the prefix
+// of 128-row tiles.  Tiles run N-fastest inside each 128-row block so that the CTAs working at
+// the same time share one A tile (read from HBM once) and one group's weights (kept in L2).
+struct GroupTab {
+    int start[kMaxGroups];
+    int rows[kMaxGroups];
+    int mt_pre[kMaxGroups + 1];
+};
+
+__device__ __forceinline__ Tile tile_of(int64_t t, int n_tiles, const GroupTab& tab, int G)
 {
     Tile T;
-    T.nt = (int)(t / total_mtiles);
-    const int gm = (int)(t % total_mtiles);
-    int lo = 0, hi = a.gr.G - 1;
+    T.nt = (int)(t % n_tiles);
+    const int gm = (int)(t / n_tiles);
+    int lo = 0, hi = G - 1;
     while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (mt_pre[mid] <= gm) lo = mid; else hi = mid - 1;
+        const int mid = (lo + hi + 1) >> 1;
+        if (tab.mt_pre[mid] <= gm) lo = mid; else hi = mid - 1;
     }
     T.g = lo;
-    int64_t gb, ge;
-    group_range(a.gr, lo, gb, ge);
-    const int mt = gm - mt_pre[lo];
-    T.row0 = gb + (int64_t)mt * kBM;
-    const int64_t left = ge - T.row0;
-    T.rows = (int)(left < kBM ? left : kBM);
+    const int mt = gm - tab.mt_pre[lo];
+    T.row0 = tab.start[lo] + mt * kBM;
+    const int left = tab.rows[lo] - mt * kBM;
+    T.rows = left < kBM ? left : kBM;
     return T;
 }
 
 // ------------------------------------------------------------------ the kernel
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                                 uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                            const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], acc_full, acc_empty, drain_bar;
+    __shared__ __align__(8) uint64_t full_bar[kStages], sf_bar[kStages], empty_bar[kStages], acc_full, acc_empty, drain_bar, drain_sf;
     __shared__ uint32_t tmem_base_slot;
-    __shared__ int mt_pre[kMaxGroups + 1];
+    __shared__ GroupTab tab;
     __shared__ int abort_flag;
 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = a.gr.G;
 
-    // group m-tile prefix
+    // per-group tables: rows and starts in parallel, the tile prefix by warp 0
+    for (int g = threadIdx.x; g < G; g += kThreads) {
+        int64_t gb, ge;
+        group_range(a.gr, g, gb, ge);
+        tab.start[g] = (int)gb;
+        tab.rows[g] = ge > gb ? (int)(ge - gb) : 0;
+    }
     if (threadIdx.x == 0) {
-        int s = 0;
-        for (int g = 0; g < a.gr.G; ++g) {
-            mt_pre[g] = s;
-            int64_t gb, ge;
-            group_range(a.gr, g, gb, ge);
-            const int64_t n = ge > gb ? ge - gb : 0;
-            s += (int)((n + kBM - 1) / kBM);
-        }
-        mt_pre[a.gr.G] = s;
         abort_flag = 0;
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&full_bar[i], 1);
+            mbar_init(&sf_bar[i], 1);
             mbar_init(&empty_bar[i], 1);
         }
         mbar_init(&acc_full, 1);
-        mbar_init(&acc_empty, 128);
+        mbar_init(&acc_empty, kEpiThreads);
         mbar_init(&drain_bar, 1);
+        mbar_init(&drain_sf, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+    if (warp == 0) {
+        constexpr int kPer = kMaxGroups / 32;
+        int cnt[kPer], sum = 0;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int g = lane * kPer + i;
+            cnt[i] = g < G ? (tab.rows[g] + kBM - 1) / kBM : 0;
+            sum += cnt[i];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int run = incl - sum;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int g = lane * kPer + i;
+            if (g <= G) tab.mt_pre[g] = run;
+            run += cnt[i];
+        }
+        if (lane == 31 && G == kMaxGroups) tab.mt_pre[G] = run;
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_slot)),
@@ -264,27 +336,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_slot;
-    const int total_mtiles = mt_pre[a.gr.G];
+    const int total_mtiles = tab.mt_pre[G];
     const int n_tiles = (int)(a.N / kBN);
     const int64_t total_tiles = (int64_t)total_mtiles * n_tiles;
     const int num_kt = (a.ktot + kBK - 1) / kBK;
     volatile int* abrt = &abort_flag;
 
     if (warp == 0) {
-        // ---------------- TMA producer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            for (int64_t t = blockIdx.x; t < total_tiles && !*abrt; t += gridDim.x) {
-                const Tile T = tile_of(t, total_mtiles, mt_pre, a);
-                int64_t brow0, brow1;
-                if (a.epilogue == NVQ_EPI_SWIGLU) {
-                    brow0 = (int64_t)T.g * a.N + (int64_t)T.nt * (kBN / 2);
-                    brow1 = brow0 + a.N / 2;
-                } else {
-                    brow0 = (int64_t)T.g * a.N + (int64_t)T.nt * kBN;
-                    brow1 = brow0 + kBN / 2;
-                }
+        // ---------------- producer: A and B code tiles by TMA (weights L2 evict-last: every
+        // 128-row block of the group re-reads them), scale atoms by bulk copies.
+        uint64_t pol_keep;
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
+        int stage = 0;
+        uint32_t phase = 0, issued = 0;
+        for (int64_t t = blockIdx.x; t < total_tiles && !*abrt; t += gridDim.x) {
+            const Tile T = tile_of(t, n_tiles, tab, G);
+            int64_t brow0, brow1;
+            if (a.epilogue == NVQ_EPI_SWIGLU) {
+                brow0 = (int64_t)T.g * a.N + (int64_t)T.nt * (kBN / 2);
+                brow1 = brow0 + a.N / 2;
+            } else {
+                brow0 = (int64_t)T.g * a.N + (int64_t)T.nt * kBN;
+                brow1 = brow0 + kBN / 2;
+            }
+            if (lane == 0) {
                 for (int kt = 0; kt < num_kt; ++kt) {
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1, a, abrt, 1)) break;
                     const int kleft = a.ktot - kt * kBK;
@@ -294,25 +369,35 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     uint8_t* sSFA = sB + kBBytes;
                     uint8_t* sSFB = sSFA + kSFABytes;
                     mbar_expect_tx(&full_bar[stage], kABytes + kBBytes + 3u * 512u * n_atoms);
-                    tma_load_2d(sA, &tmap_a, kt * (kBK / 2), (int)T.row0, &full_bar[stage]);
-                    tma_load_2d(sB, &tmap_b, kt * (kBK / 2), (int)brow0, &full_bar[stage]);
-                    tma_load_2d(sB + kBBytes / 2, &tmap_b, kt * (kBK / 2), (int)brow1, &full_bar[stage]);
-                    const uint8_t* srcA = a.a_sf + ((T.row0 >> 7) * (a.a_sf_cols >> 2) + kt * 4) * 512;
+                    tma_load_2d(sA, &tmap_a, kt * (kBK / 2), T.row0, &full_bar[stage]);
+                    tma_load_2d_hint(sB, &tmap_b, kt * (kBK / 2), (int)brow0, &full_bar[stage], pol_keep);
+                    tma_load_2d_hint(sB + kBBytes / 2, &tmap_b, kt * (kBK / 2), (int)brow1, &full_bar[stage], pol_keep);
+                    const uint8_t* srcA = a.a_sf + ((int64_t)(T.row0 >> 7) * (a.a_sf_cols >> 2) + kt * 4) * 512;
                     bulk_load(sSFA, srcA, 512u * n_atoms, &full_bar[stage]);
                     const uint8_t* srcB0 = a.b_sf + ((brow0 >> 7) * (a.b_sf_cols >> 2) + kt * 4) * 512;
                     const uint8_t* srcB1 = a.b_sf + ((brow1 >> 7) * (a.b_sf_cols >> 2) + kt * 4) * 512;
                     bulk_load(sSFB, srcB0, 512u * n_atoms, &full_bar[stage]);
                     bulk_load(sSFB + kSFBBytes / 2, srcB1, 512u * n_atoms, &full_bar[stage]);
+                    ++issued;
                     if (++stage == kStages) { stage = 0; phase ^= 1; }
                 }
             }
-            if (*abrt) {
-                // let issued copies land before the CTA can exit
-                for (int s = 0; s < kStages; ++s) mbar_wait(&full_bar[s], 0, a, abrt, 11) || mbar_wait(&full_bar[s], 1, a, abrt, 11);
-            }
+            __syncwarp();
+        }
+        if (*abrt && lane == 0) {
+            // let the copies still in flight land before the CTA can exit: the last issue
+            // on each stage is the phase (phase ^ 1) for stages before `stage`, else `phase`
+            for (int s = 0; s < kStages; ++s)
+                if (issued > (uint32_t)s) mbar_wait(&full_bar[s], s < stage ? phase : phase ^ 1, a, abrt, 11, true);
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer
+        // ---------------- MMA issuer: waits for the stage's scale factors to be in TMEM (which
+        // implies its operand tiles are in shared memory), then up to 4 MMAs and one commit
+        // that frees the stage.  Descriptors are precomputed; nothing else is in this loop.
+        const uint32_t base = smem_u32(smem);
+        const uint64_t a_desc0 = smem_desc(base, 16, 1024, 2);
+        const uint64_t b_desc0 = smem_desc(base + kABytes, 16, 1024, 2);
+        constexpr uint64_t kStageStep = kStageBytes >> 4;
         int stage = 0;
         uint32_t phase = 0, acc_phase = 0;
         bool issued_any = false;
@@ -321,27 +406,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             tc_fence_after();
             bool ok = true;
             for (int kt = 0; kt < num_kt; ++kt) {
-                if (!mbar_wait(&full_bar[stage], phase, a, abrt, 3)) { ok = false; break; }
+                if (!mbar_wait(&sf_bar[stage], phase, a, abrt, 3)) { ok = false; break; }
                 tc_fence_after();
                 const int kleft = a.ktot - kt * kBK;
                 const int n_mma = kleft >= kBK ? 4 : (kleft + 63) / 64;
                 if (lane == 0) {
-                    uint8_t* sA = smem + stage * kStageBytes;
-                    uint8_t* sB = sA + kABytes;
-                    uint8_t* sSFA = sB + kBBytes;
-                    uint8_t* sSFB = sSFA + kSFABytes;
+                    const uint64_t so = (uint64_t)stage * kStageStep;
                     const uint32_t sfa_t = tmem + kSFCol + stage * kSFColsPerStage;
                     const uint32_t sfb_t = sfa_t + 16;
-                    for (int j = 0; j < n_mma; ++j) {
-                        tc_cp_sf(sfa_t + 4 * j, smem_desc(smem_u32(sSFA + 512 * j), 0, 128, 0));
-                        tc_cp_sf(sfb_t + 8 * j, smem_desc(smem_u32(sSFB + 512 * j), 0, 128, 0));
-                        tc_cp_sf(sfb_t + 8 * j + 4, smem_desc(smem_u32(sSFB + kSFBBytes / 2 + 512 * j), 0, 128, 0));
-                    }
-                    for (int j = 0; j < n_mma; ++j) {
-                        const uint64_t ad = smem_desc(smem_u32(sA) + 32 * j, 16, 1024, 2);
-                        const uint64_t bd = smem_desc(smem_u32(sB) + 32 * j, 16, 1024, 2);
-                        mma_fp4(tmem + kAccCol, ad, bd, sfa_t + 4 * j, sfb_t + 8 * j, (kt > 0 || j > 0) ? 1u : 0u);
-                    }
+                    const uint32_t acc = (kt > 0) ? 1u : 0u;
+                    mma_fp4(tmem + kAccCol, a_desc0 + so, b_desc0 + so, sfa_t, sfb_t, acc);
+                    if (n_mma > 1) mma_fp4(tmem + kAccCol, a_desc0 + so + 2, b_desc0 + so + 2, sfa_t + 4, sfb_t + 8, 1u);
+                    if (n_mma > 2) mma_fp4(tmem + kAccCol, a_desc0 + so + 4, b_desc0 + so + 4, sfa_t + 8, sfb_t + 16, 1u);
+                    if (n_mma > 3) mma_fp4(tmem + kAccCol, a_desc0 + so + 6, b_desc0 + so + 6, sfa_t + 12, sfb_t + 24, 1u);
                     tc_commit(&empty_bar[stage]);
                     issued_any = true;
                 }
@@ -355,67 +432,126 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
         if (*abrt && issued_any && lane == 0) {
             tc_commit(&drain_bar);
-            mbar_wait(&drain_bar, 0, a, abrt, 12);
+            mbar_wait(&drain_bar, 0, a, abrt, 12, true);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ---------------- scale-factor copies: per K-tile, 12 tcgen05.cp of the stage's scale
+        // atoms into the stage's own TMEM columns, committed to sf_bar.  Issued apart from the
+        // MMA thread so that they overlap the MMAs instead of stalling their issue.
+        const uint32_t base = smem_u32(smem);
+        const uint64_t sfa_desc0 = smem_desc(base + kABytes + kBBytes, 0, 128, 0);
+        const uint64_t sfb_desc0 = smem_desc(base + kABytes + kBBytes + kSFABytes, 0, 128, 0);
+        constexpr uint64_t kStageStep = kStageBytes >> 4;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool issued_any = false;
+        for (int64_t t = blockIdx.x; t < total_tiles && !*abrt; t += gridDim.x) {
+            bool ok = true;
+            for (int kt = 0; kt < num_kt; ++kt) {
+                if (!mbar_wait(&full_bar[stage], phase, a, abrt, 5)) { ok = false; break; }
+                tc_fence_after();
+                const int kleft = a.ktot - kt * kBK;
+                const int n_mma = kleft >= kBK ? 4 : (kleft + 63) / 64;
+                if (lane == 0) {
+                    const uint64_t so = (uint64_t)stage * kStageStep;
+                    const uint32_t sfa_t = tmem + kSFCol + stage * kSFColsPerStage;
+                    const uint32_t sfb_t = sfa_t + 16;
+                    for (int j = 0; j < n_mma; ++j) {
+                        tc_cp_sf(sfa_t + 4 * j, sfa_desc0 + so + 32 * j);
+                        tc_cp_sf(sfb_t + 8 * j, sfb_desc0 + so + 32 * j);
+                        tc_cp_sf(sfb_t + 8 * j + 4, sfb_desc0 + so + 128 + 32 * j);
+                    }
+                    tc_commit(&sf_bar[stage]);
+                    issued_any = true;
+                }
+                __syncwarp();
+                if (++stage == kStages) { stage = 0; phase ^= 1; }
+            }
+            if (!ok) break;
+        }
+        if (*abrt && issued_any && lane == 0) {
+            tc_commit(&drain_sf);
+            mbar_wait(&drain_sf, 0, a, abrt, 13, true);
         }
         __syncwarp();
     } else {
-        // ---------------- epilogue (warps 2..5 -> TMEM lane quarters 2, 3, 0, 1)
+        // ---------------- epilogue: warps 3..10; TMEM lane quarter = warp % 4, column half =
+        // (warp - 3) / 4.  The accumulator is read into registers and released at once; the
+        // scaling, conversion and global stores overlap the next tile's MMAs.
         const int quarter = warp & 3;
+        const int half = (warp - 3) >> 2;
         const int r_in_tile = quarter * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         uint32_t acc_phase = 0;
         for (int64_t t = blockIdx.x; t < total_tiles && !*abrt; t += gridDim.x) {
-            const Tile T = tile_of(t, total_mtiles, mt_pre, a);
+            const Tile T = tile_of(t, n_tiles, tab, G);
+            const bool valid = r_in_tile < T.rows;
+            const int64_t grow = (int64_t)T.row0 + r_in_tile;
+            const float alpha = __fmul_rn(a.a_ts[a.a_ts_per_group ? T.g : 0].s_dec, a.b_ts[T.g].s_dec);
+            const float w = (a.epilogue == NVQ_EPI_ROW_SCALE && valid) ? a.row_w[grow] : 1.0f;
             if (!mbar_wait(&acc_full, acc_phase, a, abrt, 4)) break;
             tc_fence_after();
-            const float alpha =
-                __fmul_rn(a.a_ts[a.a_ts_per_group ? T.g : 0].s_dec, a.b_ts[T.g].s_dec);
-            const bool valid = r_in_tile < T.rows;
-            const int64_t grow = T.row0 + r_in_tile;
-            float v[32], u[32];
-            if (a.epilogue == NVQ_EPI_SWIGLU) {
-                __nv_bfloat16* orow = a.out + grow * a.ldo + (int64_t)T.nt * (kBN / 2);
+            const uint32_t tacc = tmem + kAccCol + lane_addr;
+            if (a.epilogue == NVQ_EPI_STORE_F32) {
+                float v[64];
+                float* orow = reinterpret_cast<float*>(a.out) + grow * a.ldo + (int64_t)T.nt * kBN + half * (kBN / 2);
 #pragma unroll 1
-                for (int c = 0; c < kBN / 2; c += 32) {
-                    tmem_ld32(tmem + kAccCol + lane_addr + c, v);
-                    tmem_ld32(tmem + kAccCol + lane_addr + kBN / 2 + c, u);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float g = __fmul_rn(alpha, v[i]);
-                        const float up = __fmul_rn(alpha, u[i]);
-                        v[i] = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), up);
-                    }
-                    if (valid) store_bf16x32(orow + c, v);
-                }
-            } else if (a.epilogue == NVQ_EPI_STORE_F32) {
-                float* orow = reinterpret_cast<float*>(a.out) + grow * a.ldo + (int64_t)T.nt * kBN;
-#pragma unroll 1
-                for (int c = 0; c < kBN; c += 32) {
-                    tmem_ld32(tmem + kAccCol + lane_addr + c, v);
+                for (int c = 0; c < kBN / 2; c += 64) {
+                    tmem_ld64(tacc + half * (kBN / 2) + c, v);
                     if (valid) {
                         float4* d = reinterpret_cast<float4*>(orow + c);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
+                        for (int i = 0; i < 16; ++i)
                             d[i] = make_float4(__fmul_rn(alpha, v[4 * i]), __fmul_rn(alpha, v[4 * i + 1]),
                                                __fmul_rn(alpha, v[4 * i + 2]), __fmul_rn(alpha, v[4 * i + 3]));
                     }
                 }
-            } else {
-                const float w = (a.epilogue == NVQ_EPI_ROW_SCALE && valid) ? a.row_w[grow] : 1.0f;
-                __nv_bfloat16* orow = a.out + grow * a.ldo + (int64_t)T.nt * kBN;
-#pragma unroll 1
-                for (int c = 0; c < kBN; c += 32) {
-                    tmem_ld32(tmem + kAccCol + lane_addr + c, v);
+                tc_fence_before();
+                mbar_arrive(&acc_empty);
+            } else if (a.epilogue == NVQ_EPI_SWIGLU) {
+                // gate columns [half*64, +64), up columns [128 + half*64, +64) -> h columns [half*64, +64)
+                float g[64], u[64];
+                tmem_ld64(tacc + half * 64, g);
+                tmem_ld64(tacc + kBN / 2 + half * 64, u);
+                tc_fence_before();
+                mbar_arrive(&acc_empty);
+                uint32_t pk[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        v[i] = __fmul_rn(alpha, v[i]);
-                        if (a.epilogue == NVQ_EPI_ROW_SCALE) v[i] = __fmul_rn(v[i], w);
+                for (int i = 0; i < 32; ++i) {
+                    const float g0 = __fmul_rn(alpha, g[2 * i]), u0 = __fmul_rn(alpha, u[2 * i]);
+                    const float g1 = __fmul_rn(alpha, g[2 * i + 1]), u1 = __fmul_rn(alpha, u[2 * i + 1]);
+                    pk[i] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u0, __fdividef(g1, 1.0f + __expf(-g1)) * u1);
+                }
+                if (valid) {
+                    uint4* d = reinterpret_cast<uint4*>(a.out + grow * a.ldo + (int64_t)T.nt * (kBN / 2) + half * 64);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) d[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+            } else {
+                float v0[64], v1[64];
+                tmem_ld64(tacc + half * (kBN / 2), v0);
+                tmem_ld64(tacc + half * (kBN / 2) + 64, v1);
+                tc_fence_before();
+                mbar_arrive(&acc_empty);
+                const float sc = (a.epilogue == NVQ_EPI_ROW_SCALE) ? w : 1.0f;
+                uint32_t pk[64];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float y0 = __fmul_rn(alpha, v0[2 * i]), y1 = __fmul_rn(alpha, v0[2 * i + 1]);
+                    float z0 = __fmul_rn(alpha, v1[2 * i]), z1 = __fmul_rn(alpha, v1[2 * i + 1]);
+                    if (a.epilogue == NVQ_EPI_ROW_SCALE) {
+                        y0 = __fmul_rn(y0, sc); y1 = __fmul_rn(y1, sc); z0 = __fmul_rn(z0, sc); z1 = __fmul_rn(z1, sc);
                     }
-                    if (valid) store_bf16x32(orow + c, v);
+                    pk[i] = pack_bf16x2(y0, y1);
+                    pk[32 + i] = pack_bf16x2(z0, z1);
+                }
+                if (valid) {
+                    uint4* d = reinterpret_cast<uint4*>(a.out + grow * a.ldo + (int64_t)T.nt * kBN + half * (kBN / 2));
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) d[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&acc_empty);
             acc_phase ^= 1;
         }
     }
@@ -440,13 +576,16 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode()
     return fn;
 }
 
-static nvq_status make_map(CUtensorMap* m, const void* base, int64_t inner_bytes, int64_t rows, int64_t ld)
+// 2D byte tensor map over FP4 codes, 128-byte swizzle; box = 128 bytes x box_rows rows
+// (box_rows = 1 for the four-row gathers).
+static nvq_status make_map(CUtensorMap* m, const void* base, int64_t inner_bytes, int64_t rows, int64_t ld,
+                           uint32_t box_rows = 128)
 {
     auto enc = get_encode();
     NVQ_CHECK_ARG(enc, NVQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[2] = {(cuuint64_t)inner_bytes, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)ld};
-    cuuint32_t box[2] = {128, 128};
+    cuuint32_t box[2] = {128, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

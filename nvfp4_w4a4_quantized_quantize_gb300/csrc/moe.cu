@@ -73,29 +73,48 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int32_t* __restrict
     if (threadIdx.x == blockDim.x - 1) grp_rows[e] = run;
 }
 
-// One CTA: 128-padded group offsets and the padding rows.
-__global__ void dispatch_offsets_kernel(int G, const int64_t* __restrict__ grp_rows, int64_t* __restrict__ grp_off,
-                                        int32_t* __restrict__ row_src, float* __restrict__ row_w, int64_t capacity)
+// One CTA of 1024 threads: 128-padded group offsets (block scan) and the padding rows.
+__global__ void __launch_bounds__(1024) dispatch_offsets_kernel(int G, const int64_t* __restrict__ grp_rows,
+                                                                int64_t* __restrict__ grp_off, int32_t* __restrict__ row_src,
+                                                                float* __restrict__ row_w, int64_t capacity)
 {
+    __shared__ int64_t warp_sums[32];
     __shared__ int64_t off[1025];
-    if (threadIdx.x == 0) {
-        int64_t s = 0;
-        for (int i = 0; i < G; ++i) {
-            off[i] = s;
-            s += (grp_rows[i] + 127) / 128 * 128;
+    const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+    const int64_t padded = e < G ? (grp_rows[e] + 127) / 128 * 128 : 0;
+    int64_t x = padded;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int64_t w = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
         }
-        off[G] = s;
+        warp_sums[lane] = w;
     }
     __syncthreads();
-    for (int e = threadIdx.x; e <= G; e += blockDim.x) grp_off[e] = off[e];
-    for (int e = threadIdx.x; e < G; e += blockDim.x) {
-        const int64_t end = off[e] + grp_rows[e];
-        for (int64_t r = end; r < off[e + 1]; ++r) {
+    const int64_t excl = (warp ? warp_sums[warp - 1] : 0) + x - padded;
+    if (e < G) off[e] = excl;
+    if (e == G - 1) off[G] = excl + padded;
+    __syncthreads();
+    if (e <= G) grp_off[e] = off[e];
+    // padding rows: inside each group after its routed rows, then up to the capacity
+    const int64_t total = off[G];
+    for (int g = warp; g < G; g += 32) {
+        const int64_t end = off[g] + grp_rows[g];
+        for (int64_t r = end + lane; r < off[g + 1]; r += 32) {
             row_src[r] = -1;
             if (row_w) row_w[r] = 0.0f;
         }
     }
-    for (int64_t r = off[G] + threadIdx.x; r < capacity; r += blockDim.x) {
+    for (int64_t r = total + e; r < capacity; r += 1024) {
         row_src[r] = -1;
         if (row_w) row_w[r] = 0.0f;
     }
@@ -138,33 +157,42 @@ __global__ void dispatch_scatter_kernel(const int32_t* __restrict__ ids, const f
     }
 }
 
-// Warp per routed row: codes as 16-byte vectors, scales as the 4-byte words of the blocked layout.
-__global__ void gather_rows_kernel(const uint8_t* __restrict__ codes, int64_t ld_codes, const uint8_t* __restrict__ sf,
-                                   int64_t sf_cols, const int32_t* __restrict__ row_src, int topk, int64_t capacity,
-                                   int64_t ktot, uint8_t* __restrict__ out_codes, int64_t ld_out, uint8_t* __restrict__ out_sf)
+// CTA per 128-row block of the routed layout.  Codes: warp per row, 16-byte vectors.  Scales:
+// the block's output words are written in the blocked layout's own order (coalesced); each
+// reads its word from the source row's scales (token scales: small and L2 resident).
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restrict__ codes, int64_t ld_codes,
+                                                          const uint8_t* __restrict__ sf, int64_t sf_cols,
+                                                          const int32_t* __restrict__ row_src, int topk, int64_t ktot,
+                                                          uint8_t* __restrict__ out_codes, int64_t ld_out,
+                                                          uint8_t* __restrict__ out_sf)
 {
-    const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (r >= capacity) return;
-    const int32_t s = row_src[r];
-    const int64_t src = s >= 0 ? s / topk : -1;
-    const int64_t nvec = ktot / 32;  // 16-byte vectors of codes
-    uint4* dst = reinterpret_cast<uint4*>(out_codes + r * ld_out);
-    if (src >= 0) {
-        const uint4* srcp = reinterpret_cast<const uint4*>(codes + src * ld_codes);
-        for (int64_t v = lane; v < nvec; v += 32) dst[v] = __ldg(srcp + v);
-        if (lane == 0 && (ktot % 32) != 0) {
-            const uint2* s2 = reinterpret_cast<const uint2*>(codes + src * ld_codes) + nvec * 2;
-            reinterpret_cast<uint2*>(out_codes + r * ld_out)[nvec * 2] = *s2;
-        }
-    } else {
-        for (int64_t v = lane; v < nvec; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
-        if (lane == 0 && (ktot % 32) != 0) reinterpret_cast<uint2*>(out_codes + r * ld_out)[nvec * 2] = make_uint2(0, 0);
+    __shared__ int src[128];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t r0 = (int64_t)blockIdx.x * 128;
+    if (tid < 128) {
+        const int32_t s = row_src[r0 + tid];
+        src[tid] = s >= 0 ? s / topk : -1;
     }
-    for (int64_t c4 = lane; c4 < sf_cols / 4; c4 += 32) {
-        uint32_t v = 0;
-        if (src >= 0) v = *reinterpret_cast<const uint32_t*>(sf + sf_offset(src, c4 * 4, sf_cols));
-        *reinterpret_cast<uint32_t*>(out_sf + sf_offset(r, c4 * 4, sf_cols)) = v;
+    __syncthreads();
+    if (out_codes != nullptr) {
+        const int nvec = (int)(ktot / 32);  // 16-byte vectors of codes
+        const bool tail8 = (ktot % 32) != 0;
+        for (int r = warp; r < 128; r += 8) {
+            const int sr = src[r];
+            uint4* dst = reinterpret_cast<uint4*>(out_codes + (r0 + r) * ld_out);
+            const uint4* sp = reinterpret_cast<const uint4*>(codes + (int64_t)(sr >= 0 ? sr : 0) * ld_codes);
+            for (int v = lane; v < nvec; v += 32) dst[v] = sr >= 0 ? __ldg(sp + v) : make_uint4(0, 0, 0, 0);
+            if (tail8 && lane == 0)
+                reinterpret_cast<uint2*>(dst)[nvec * 2] = sr >= 0 ? reinterpret_cast<const uint2*>(sp)[nvec * 2] : make_uint2(0, 0);
+        }
+    }
+    const int natoms = (int)(sf_cols / 4);
+    uint32_t* outw = reinterpret_cast<uint32_t*>(out_sf + blockIdx.x * (int64_t)natoms * 512);
+    for (int w = tid; w < natoms * 128; w += 256) {
+        const int a = w >> 7, pos = w & 127;
+        const int r = (pos >> 2) + 32 * (pos & 3);
+        const int sr = src[r];
+        outw[w] = sr >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(sf + sf_offset(sr, 4 * a, sf_cols))) : 0u;
     }
 }
 
@@ -247,18 +275,18 @@ extern "C" nvq_status nvfp4_gather_rows(const uint8_t* codes, int64_t ld_codes, 
                                         int64_t src_rows, const int32_t* row_src, int32_t topk, int64_t capacity,
                                         int64_t ktot, uint8_t* out_codes, int64_t ld_out, uint8_t* out_sf, void* stream)
 {
-    NVQ_CHECK_ARG(codes && sf && row_src && out_codes && out_sf, NVQ_ERR_ARG, "nvfp4_gather_rows: null pointer argument");
+    NVQ_CHECK_ARG(codes && sf && row_src && out_sf, NVQ_ERR_ARG, "nvfp4_gather_rows: null pointer argument");
     NVQ_CHECK_ARG(ktot >= 16 && ktot % 16 == 0 && sf_cols >= ktot / 16 && sf_cols % 4 == 0, NVQ_ERR_SHAPE,
                   "nvfp4_gather_rows: bad ktot / sf_cols");
     NVQ_CHECK_ARG(capacity >= 1 && capacity % 128 == 0 && src_rows >= 1 && topk >= 1, NVQ_ERR_SHAPE,
                   "nvfp4_gather_rows: capacity must be a positive multiple of 128");
-    NVQ_CHECK_ARG(ld_codes % 16 == 0 && ld_out % 16 == 0 && ld_codes >= ktot / 2 && ld_out >= ktot / 2 &&
-                      aligned(codes, 16) && aligned(out_codes, 16) && aligned(sf, 4) && aligned(out_sf, 4),
+    NVQ_CHECK_ARG(ld_codes % 16 == 0 && ld_codes >= ktot / 2 && aligned(codes, 16) && aligned(sf, 4) && aligned(out_sf, 4) &&
+                      (!out_codes || (ld_out % 16 == 0 && ld_out >= ktot / 2 && aligned(out_codes, 16))),
                   NVQ_ERR_ALIGN, "nvfp4_gather_rows: codes need 16-byte aligned rows");
     set_error("");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    gather_rows_kernel<<<(unsigned)((capacity + 7) / 8), 256, 0, st>>>(codes, ld_codes, sf, sf_cols, row_src, topk,
-                                                                      capacity, ktot, out_codes, ld_out, out_sf);
+    gather_rows_kernel<<<(unsigned)(capacity / 128), 256, 0, st>>>(codes, ld_codes, sf, sf_cols, row_src, topk, ktot,
+                                                                   out_codes, ld_out, out_sf);
     NVQ_LAUNCH_CHECK("gather_rows_kernel");
     return NVQ_OK;
 }

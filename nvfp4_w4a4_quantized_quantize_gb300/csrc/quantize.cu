@@ -2,47 +2,74 @@
 // Q_W of Eq. (7) and the trainer's QDQ_W of Eq. (12)) with the per-channel residual score of
 // Eq. (23) fused into the same pass over the input.
 //
-// Two kernels per call:
-//   amax_kernel          per-group max |x| (the FP32 tensor scale's statistic), one atomicMax
-//                        per (CTA, group run);
+// Two kernels per call, both HBM-bound:
+//   amax_kernel          per-group max |x| (the FP32 tensor scale's statistic): 16-byte loads,
+//                        8 in flight per thread, one atomicMax per (CTA, group run);
 //   quant_score_kernel   codes + blocked E4M3 scales + residual + integer channel score (+ the
-//                        dequantized values for the trainer-side QDQ), one thread per
-//                        16-element block, 32-byte coalesced loads.
-// Both are HBM-bound: the input is read twice (the second read is mostly served by L2 for
-// inputs up to ~100 MB), codes and scales are written once.
+//                        dequantized values for the trainer-side QDQ).  One CTA per SM: a
+//                        producer warp streams the CTA's band of rows into an 8-stage shared
+//                        memory ring with cp.async.bulk (128 KB in flight per SM, independent
+//                        of register pressure), eight compute warps quantize one 16-element
+//                        block per thread per row from shared memory.  The CTA re-reads the
+//                        rows amax_kernel's CTAs just streamed, so most of that second read is
+//                        served by L2.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
 
 namespace nvq {
 
-static constexpr int kQuantThreads = 256;
-
 // ------------------------------------------------------------------------ amax
-__global__ void __launch_bounds__(kQuantThreads) amax_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx,
-                                                              int K, Groups gr, int64_t rows_per_cta,
-                                                              nvq_tensor_scale* __restrict__ ts)
+static constexpr int kAmaxThreads = 256;
+static constexpr int kAmaxUnroll = 8;
+
+__device__ __forceinline__ float amax_u4(uint4 w)
 {
-    __shared__ float red[kQuantThreads / 32];
+    // |bf16| pairs as bf16x2 maxima (exact), then the two halves
+    const uint32_t m = 0x7fff7fffu;
+    __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&(w.x = w.x & m));
+    __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&(w.y = w.y & m));
+    __nv_bfloat162 c = *reinterpret_cast<__nv_bfloat162*>(&(w.z = w.z & m));
+    __nv_bfloat162 d = *reinterpret_cast<__nv_bfloat162*>(&(w.w = w.w & m));
+    __nv_bfloat162 r = __hmax2(__hmax2(a, b), __hmax2(c, d));
+    return fmaxf(__low2float(r), __high2float(r));
+}
+
+__global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, int K,
+                                                             Groups gr, int64_t rows_per_cta,
+                                                             nvq_tensor_scale* __restrict__ ts)
+{
+    __shared__ float red[kAmaxThreads / 32];
     const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
     const int64_t r1 = min(r0 + rows_per_cta, gr.total_rows);
     if (r0 >= r1) return;
-    const int vec_per_row = K / 8;
+    const int vpr = K / 8;  // 16-byte vectors per row
     int g = group_of_row(gr, r0);
     int64_t row = r0;
     while (row < r1 && g < gr.G) {
         int64_t gb, ge;
         group_range(gr, g, gb, ge);
-        int64_t a = max(row, gb), b = min(r1, ge);
+        const int64_t a = max(row, gb), b = min(r1, ge);
         float m = 0.0f;
         if (a < b) {
-            const int64_t n = (b - a) * vec_per_row;
-            for (int64_t i = threadIdx.x; i < n; i += kQuantThreads) {
-                int64_t rr = a + i / vec_per_row;
-                int v = (int)(i % vec_per_row);
-                uint4 w = __ldg(reinterpret_cast<const uint4*>(x + rr * ldx) + v);
-                m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16lo(w.x)), fabsf(bf16hi(w.x))), fmaxf(fabsf(bf16lo(w.y)), fabsf(bf16hi(w.y)))));
-                m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16lo(w.z)), fabsf(bf16hi(w.z))), fmaxf(fabsf(bf16lo(w.w)), fabsf(bf16hi(w.w)))));
+            if (ldx == K) {
+                // contiguous rows: one flat range of vectors
+                const uint4* p = reinterpret_cast<const uint4*>(x + a * ldx);
+                const int64_t n = (b - a) * vpr;
+                int64_t i = threadIdx.x;
+                for (; i + (kAmaxUnroll - 1) * kAmaxThreads < n; i += kAmaxUnroll * kAmaxThreads) {
+                    uint4 w[kAmaxUnroll];
+#pragma unroll
+                    for (int u = 0; u < kAmaxUnroll; ++u) w[u] = __ldg(p + i + u * kAmaxThreads);
+#pragma unroll
+                    for (int u = 0; u < kAmaxUnroll; ++u) m = fmaxf(m, amax_u4(w[u]));
+                }
+                for (; i < n; i += kAmaxThreads) m = fmaxf(m, amax_u4(__ldg(p + i)));
+            } else {
+                for (int64_t r = a; r < b; ++r) {
+                    const uint4* p = reinterpret_cast<const uint4*>(x + r * ldx);
+                    for (int v = threadIdx.x; v < vpr; v += kAmaxThreads) m = fmaxf(m, amax_u4(__ldg(p + v)));
+                }
             }
         }
 #pragma unroll
@@ -51,7 +78,7 @@ __global__ void __launch_bounds__(kQuantThreads) amax_kernel(const __nv_bfloat16
         __syncthreads();
         if (threadIdx.x == 0) {
             float mm = 0.0f;
-            for (int w = 0; w < kQuantThreads / 32; ++w) mm = fmaxf(mm, red[w]);
+            for (int w = 0; w < kAmaxThreads / 32; ++w) mm = fmaxf(mm, red[w]);
             if (a < b && mm > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(&ts[g].amax), __float_as_uint(mm));
         }
         __syncthreads();
@@ -61,103 +88,296 @@ __global__ void __launch_bounds__(kQuantThreads) amax_kernel(const __nv_bfloat16
 }
 
 // ------------------------------------------------------------------------ quantize + score
-// BPT = 16-element blocks per thread along K (1 when K <= 4096, 2 when K <= 8192).
-template <int BPT, bool kScores, int kWhat>  // kWhat: 0 none, 1 bf16 w_hat, 2 fp32 w_hat
-__global__ void __launch_bounds__(kQuantThreads) quant_score_kernel(
-    const __nv_bfloat16* __restrict__ x, int64_t ldx, int K, Groups gr, int64_t rows_per_cta,
-    uint8_t* __restrict__ codes, int64_t ld_codes, uint8_t* __restrict__ sf, int64_t sf_cols, int zero_pad,
-    nvq_tensor_scale* __restrict__ ts, unsigned long long* __restrict__ scores, void* __restrict__ w_hat)
+static constexpr int kQStages = 8;
+static constexpr int kQStageBytes = 16384;
+static constexpr int kQCompute = 512;            // 16 compute warps: one thread per 16-element block up to K = 8192
+static constexpr int kQThreads = kQCompute + 32; // + producer warp
+
+__device__ __forceinline__ uint32_t sa32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void q_mbar_init(uint64_t* bar, uint32_t count)
 {
-    extern __shared__ unsigned long long red_scores[];  // [kQuantThreads][16 * BPT] when needed
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ bool q_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(sa32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: false after recording a timeout, or (unless draining) as soon as another warp
+// of the CTA gave up.
+__device__ __forceinline__ bool q_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, DeviceStatus* st,
+                                       unsigned long long limit, int where, bool draining = false)
+{
+    if (q_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        for (int i = 0; i < 32; ++i)
+            if (q_try_wait(bar, parity)) return true;
+        if (!draining && *abort_flag) return false;
+        if ((unsigned long long)(clock64() - t0) > limit) {
+            report_timeout(st, where);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void q_bulk_row(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(sa32(dst)),
+                 "l"(src), "r"(bytes), "r"(sa32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kQCompute) : "memory"); }
+
+// max |x| of a 16-element bf16 block (exact): a bf16x2 maximum tree over the sign-cleared words.
+__device__ __forceinline__ float amax_block(const uint4& w0, const uint4& w1)
+{
+    const uint32_t m = 0x7fff7fffu;
+    uint32_t u[8] = {w0.x & m, w0.y & m, w0.z & m, w0.w & m, w1.x & m, w1.y & m, w1.z & m, w1.w & m};
+    __nv_bfloat162 h[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = *reinterpret_cast<__nv_bfloat162*>(&u[i]);
+    const __nv_bfloat162 r = __hmax2(__hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3])),
+                                     __hmax2(__hmax2(h[4], h[5]), __hmax2(h[6], h[7])));
+    return fmaxf(__low2float(r), __high2float(r));
+}
+
+// fl(a / 6) for a non-negative bf16 value a: q1 = fl(a * fl(1/6)), one FMA residual correction.
+// Checked exhaustively against IEEE division for every finite non-negative bf16 value.
+__device__ __forceinline__ float div6_bf16(float a)
+{
+    constexpr float kInv6 = 1.0f / 6.0f;
+    const float q1 = __fmul_rn(a, kInv6);
+    const float r = __fmaf_rn(-q1, 6.0f, a);
+    return __fmaf_rn(r, kInv6, q1);
+}
+
+// acc += rint(|r| * sc)^2 (sc = 2^(20-E), a normal power of two): one FMA puts the rounded
+// integer in the low mantissa bits, one multiply-add accumulates its square in 64 bits.
+__device__ __forceinline__ void score_acc(unsigned long long& acc, float r, float sc)
+{
+    const float y = __fmaf_rn(fabsf(r), sc, 8388608.0f);
+    const uint32_t q = __float_as_uint(y) & 0x7fffffu;
+    asm("mad.wide.u32 %0, %1, %1, %0;" : "+l"(acc) : "r"(q));
+}
+
+struct QuantArgs {
+    const __nv_bfloat16* x;
+    int64_t ldx;
+    int K;
+    Groups gr;
+    int64_t rows_per_cta;
+    uint8_t* codes;
+    int64_t ld_codes;
+    uint8_t* sf;
+    int64_t sf_cols;
+    int zero_pad;
+    nvq_tensor_scale* ts;
+    unsigned long long* scores;
+    void* w_hat;
+    DeviceStatus* status;
+    unsigned long long wait_limit;
+};
+
+// BPT = 16-element blocks per thread along K (1: K / 16 <= kQCompute).
+template <int BPT, bool kScores, int kWhat>  // kWhat: 0 none, 1 bf16 w_hat, 2 fp32 w_hat
+__global__ void __launch_bounds__(kQThreads, 1) quant_score_kernel(const QuantArgs qa)
+{
+    extern __shared__ __align__(128) uint8_t ring[];
+    __shared__ __align__(8) uint64_t full_bar[kQStages], empty_bar[kQStages];
+    __shared__ float eb_tab[128], db_tab[128];
+    __shared__ int abort_flag;
+
+    const int K = qa.K;
     const int nb = K / 16;
-    const int lanes_per_row = (BPT == 1) ? nb : kQuantThreads;
-    const int rows_per_iter = (BPT == 1) ? (kQuantThreads / nb) : 1;
+    const int row_bytes = 2 * K;
+    const int R = max(1, kQStageBytes / row_bytes);  // rows per stage
     const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    unsigned long long* red_scores = reinterpret_cast<unsigned long long*>(ring + kQStages * kQStageBytes);
+
+    if (tid == 0) {
+        for (int i = 0; i < kQStages; ++i) {
+            q_mbar_init(&full_bar[i], 1);
+            q_mbar_init(&empty_bar[i], kQCompute / 32);
+        }
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // CTA 0 publishes every group's scale fields (amax is final: amax_kernel ran before).
+    if (blockIdx.x == 0) {
+        for (int g = tid; g < qa.gr.G; g += kQThreads) {
+            TScale t = tscale_from_amax(qa.ts[g].amax);
+            qa.ts[g].s_enc = t.s_enc;
+            qa.ts[g].s_dec = t.s_dec;
+            qa.ts[g].shift_e = t.shift_e;
+        }
+    }
+    __syncthreads();
+    volatile int* abrt = &abort_flag;
+
+    const int64_t r0 = (int64_t)blockIdx.x * qa.rows_per_cta;
+    const int64_t r1 = min(r0 + qa.rows_per_cta, qa.gr.total_rows);
+    if (r0 >= r1) return;
+
+    if (warp == kQCompute / 32) {
+        // ---------------- producer: stream the band's rows, group run by group run
+        if (lane == 0) {
+            uint32_t it = 0;
+            int g = group_of_row(qa.gr, r0);
+            int64_t row = r0;
+            while (row < r1 && g < qa.gr.G && !*abrt) {
+                int64_t gb, ge;
+                group_range(qa.gr, g, gb, ge);
+                const int64_t a = max(row, gb), b = min(r1, ge);
+                for (int64_t r = a; r < b && !*abrt; r += R) {
+                    const int s = it % kQStages;
+                    if (!q_wait(&empty_bar[s], ((it / kQStages) & 1) ^ 1, abrt, qa.status, qa.wait_limit, 21)) break;
+                    const int nr = (int)min((int64_t)R, b - r);
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa32(&full_bar[s])),
+                                 "r"((uint32_t)(nr * row_bytes))
+                                 : "memory");
+                    for (int j = 0; j < nr; ++j)
+                        q_bulk_row(ring + s * kQStageBytes + j * row_bytes, qa.x + (r + j) * qa.ldx, row_bytes, &full_bar[s]);
+                    ++it;
+                }
+                row = max(row, ge);
+                ++g;
+            }
+            if (*abrt) {
+                // let the copies still in flight land before the CTA exits (the last issue on each stage)
+                for (uint32_t j = it > kQStages ? it - kQStages : 0; j < it; ++j)
+                    q_wait(&full_bar[j % kQStages], (j / kQStages) & 1, abrt, qa.status, qa.wait_limit, 22, true);
+            }
+        }
+        return;
+    }
+
+    // ---------------- compute warps
+    const int lanes_per_row = (BPT == 1) ? nb : kQCompute;
+    const int rows_per_iter = (BPT == 1) ? (kQCompute / nb) : 1;
     const int rl = tid / lanes_per_row;
     const int bc0 = tid % lanes_per_row;
     const bool active = rl < rows_per_iter;
-
-    // CTA 0 publishes every group's scale fields (amax is final: amax_kernel ran before).
-    if (blockIdx.x == 0) {
-        for (int g = tid; g < gr.G; g += kQuantThreads) {
-            TScale t = tscale_from_amax(ts[g].amax);
-            ts[g].s_enc = t.s_enc;
-            ts[g].s_dec = t.s_dec;
-            ts[g].shift_e = t.shift_e;
-        }
-    }
-
-    const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
-    const int64_t r1 = min(r0 + rows_per_cta, gr.total_rows);
-    if (r0 >= r1) return;
-    int g = group_of_row(gr, r0);
+    bool dead = false;
+    uint32_t it = 0;
+    int g = group_of_row(qa.gr, r0);
     int64_t row = r0;
-    while (row < r1 && g < gr.G) {
+    while (row < r1 && g < qa.gr.G) {
         int64_t gb, ge;
-        group_range(gr, g, gb, ge);
+        group_range(qa.gr, g, gb, ge);
         const int64_t a = max(row, gb), b = min(r1, ge);
-        const TScale t = tscale_from_amax(ts[g].amax);
+        const TScale t = tscale_from_amax(qa.ts[g].amax);
         const ScoreScale ss = score_scale(t.shift_e);
+        // per-group encode / decode scale of every E4M3 block-scale value
+        consumer_sync();
+        if (tid < 128) {
+            const float sbv = e4m3_value((uint32_t)tid);
+            eb_tab[tid] = (tid == 0 || tid == 127) ? 0.0f : __fdiv_rn(t.s_enc, sbv);
+            db_tab[tid] = (tid == 127) ? 0.0f : __fmul_rn(sbv, t.s_dec);
+        }
+        consumer_sync();
         unsigned long long part[BPT][16];
 #pragma unroll
         for (int p = 0; p < BPT; ++p)
 #pragma unroll
             for (int i = 0; i < 16; ++i) part[p][i] = 0ull;
 
-        if (active) {
-            for (int64_t r = a + rl; r < b; r += rows_per_iter) {
-                const __nv_bfloat16* xr = x + r * ldx;
+        for (int64_t r = a; r < b; r += R, ++it) {
+            const int s = it % kQStages;
+            // a warp that gives up keeps walking the same sequence (so that no named barrier is
+            // left waiting for it) but skips the work
+            if (!dead && !q_wait(&full_bar[s], (it / kQStages) & 1, abrt, qa.status, qa.wait_limit, 23)) dead = true;
+            const int nr = (int)min((int64_t)R, b - r);
+            const uint8_t* stage = ring + s * kQStageBytes;
+            if (active && !dead) {
+                for (int rr = rl; rr < nr; rr += rows_per_iter) {
+                    const int64_t grow = r + rr;
+                    uint8_t* crow = qa.codes + grow * qa.ld_codes;
+                    const int64_t sfrow = (grow >> 7) * (qa.sf_cols >> 2) * 512 + (grow & 31) * 16 + ((grow >> 5) & 3) * 4;
 #pragma unroll
-                for (int p = 0; p < BPT; ++p) {
-                    const int bc = bc0 + p * kQuantThreads;
-                    if (bc >= nb) continue;
-                    const uint4* src = reinterpret_cast<const uint4*>(xr + bc * 16);
-                    uint4 w0 = __ldg(src), w1 = __ldg(src + 1);
-                    float v[16] = {bf16lo(w0.x), bf16hi(w0.x), bf16lo(w0.y), bf16hi(w0.y),
-                                   bf16lo(w0.z), bf16hi(w0.z), bf16lo(w0.w), bf16hi(w0.w),
-                                   bf16lo(w1.x), bf16hi(w1.x), bf16lo(w1.y), bf16hi(w1.y),
-                                   bf16lo(w1.z), bf16hi(w1.z), bf16lo(w1.w), bf16hi(w1.w)};
-                    BlockOut o = quantize16(v, t.s_enc, t.s_dec);
-                    *reinterpret_cast<uint2*>(codes + r * ld_codes + bc * 8) = make_uint2(o.code_lo, o.code_hi);
-                    sf[sf_offset(r, bc, sf_cols)] = (uint8_t)o.sb;
-                    if (kScores || kWhat) {
-                        float dq[16];
+                    for (int p = 0; p < BPT; ++p) {
+                        const int bc = bc0 + p * kQCompute;
+                        if (bc >= nb) continue;
+                        const uint4* src = reinterpret_cast<const uint4*>(stage + rr * row_bytes + bc * 32);
+                        const uint4 w0 = src[0], w1 = src[1];
+                        const float v[16] = {bf16lo(w0.x), bf16hi(w0.x), bf16lo(w0.y), bf16hi(w0.y),
+                                             bf16lo(w0.z), bf16hi(w0.z), bf16lo(w0.w), bf16hi(w0.w),
+                                             bf16lo(w1.x), bf16hi(w1.x), bf16lo(w1.y), bf16hi(w1.y),
+                                             bf16lo(w1.z), bf16hi(w1.z), bf16lo(w1.w), bf16hi(w1.w)};
+                        const uint32_t sb = e4m3(__fmul_rn(div6_bf16(amax_block(w0, w1)), t.s_enc));
+                        const float e_b = eb_tab[sb], d_b = db_tab[sb];
+                        uint32_t c[8];
+                        if (sb == 0) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) dq[i] = __fmul_rn(e2m1_value(block_code(o, i)), o.d_b);
-                        if (kScores) {
+                            for (int i = 0; i < 8; ++i)
+                                c[i] = ((__float_as_uint(v[2 * i]) >> 28) & 0x8u) | ((__float_as_uint(v[2 * i + 1]) >> 24) & 0x80u);
+                        } else {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) part[p][i] += score_term(__fsub_rn(v[i], dq[i]), ss);
+                            for (int i = 0; i < 8; ++i) c[i] = e2m1x2(__fmul_rn(v[2 * i], e_b), __fmul_rn(v[2 * i + 1], e_b));
                         }
-                        if (kWhat == 1) {
-                            uint32_t pk[8];
+                        const uint32_t lo = __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
+                        const uint32_t hi = __byte_perm(__byte_perm(c[4], c[5], 0x0040), __byte_perm(c[6], c[7], 0x0040), 0x5410);
+                        *reinterpret_cast<uint2*>(crow + bc * 8) = make_uint2(lo, hi);
+                        qa.sf[sfrow + (bc >> 2) * 512 + (bc & 3)] = (uint8_t)sb;
+                        if (kScores || kWhat) {
+                            float dq[16];
 #pragma unroll
                             for (int i = 0; i < 8; ++i) {
-                                __nv_bfloat162 h2 = __floats2bfloat162_rn(dq[2 * i], dq[2 * i + 1]);
-                                pk[i] = *reinterpret_cast<uint32_t*>(&h2);
+                                const float2 vv = e2m1x2_value(c[i]);
+                                dq[2 * i] = __fmul_rn(vv.x, d_b);
+                                dq[2 * i + 1] = __fmul_rn(vv.y, d_b);
                             }
-                            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(w_hat) + r * (int64_t)K + bc * 16);
-                            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                        } else if (kWhat == 2) {
-                            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(w_hat) + r * (int64_t)K + bc * 16);
+                            if (kScores) {
+                                if (!ss.split) {
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) dst[i] = make_float4(dq[4 * i], dq[4 * i + 1], dq[4 * i + 2], dq[4 * i + 3]);
+                                    for (int i = 0; i < 16; ++i) score_acc(part[p][i], __fsub_rn(v[i], dq[i]), ss.sc_a);
+                                } else {
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i) part[p][i] += score_term(__fsub_rn(v[i], dq[i]), ss);
+                                }
+                            }
+                            if (kWhat == 1) {
+                                uint32_t pk[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    __nv_bfloat162 h2 = __floats2bfloat162_rn(dq[2 * i], dq[2 * i + 1]);
+                                    pk[i] = *reinterpret_cast<uint32_t*>(&h2);
+                                }
+                                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(qa.w_hat) + grow * (int64_t)K + bc * 16);
+                                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                            } else if (kWhat == 2) {
+                                float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(qa.w_hat) + grow * (int64_t)K + bc * 16);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) dst[i] = make_float4(dq[4 * i], dq[4 * i + 1], dq[4 * i + 2], dq[4 * i + 3]);
+                            }
                         }
                     }
-                }
-                if (zero_pad && bc0 == 0) {
-                    for (int64_t c = nb; c < sf_cols; ++c) sf[sf_offset(r, c, sf_cols)] = 0;
+                    if (qa.zero_pad && bc0 == 0)
+                        for (int64_t cc = nb; cc < qa.sf_cols; ++cc) qa.sf[sf_offset(grow, cc, qa.sf_cols)] = 0;
                 }
             }
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sa32(&empty_bar[s])) : "memory");
         }
 
         if (kScores) {
-            unsigned long long* dst = scores + (int64_t)g * K;
+            unsigned long long* dst = qa.scores + (int64_t)g * K;
             if (rows_per_iter == 1) {
-                if (active && a < b) {
+                if (active && a < b && !dead) {
 #pragma unroll
                     for (int p = 0; p < BPT; ++p) {
-                        const int bc = bc0 + p * kQuantThreads;
+                        const int bc = bc0 + p * kQCompute;
                         if (bc >= nb) continue;
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
@@ -165,19 +385,19 @@ __global__ void __launch_bounds__(kQuantThreads) quant_score_kernel(
                     }
                 }
             } else {
-                // BPT == 1: fold the rows_per_iter row lanes of each block column in shared memory.
+                // BPT == 1: fold the rows_per_iter row lanes of each block column in shared memory
 #pragma unroll
                 for (int i = 0; i < 16; ++i) red_scores[tid * 16 + i] = part[0][i];
-                __syncthreads();
-                if (rl == 0 && a < b) {
+                consumer_sync();
+                if (rl == 0 && a < b && !dead) {
 #pragma unroll 1
                     for (int i = 0; i < 16; ++i) {
-                        unsigned long long s = 0;
-                        for (int l = 0; l < rows_per_iter; ++l) s += red_scores[(l * nb + bc0) * 16 + i];
-                        if (s) atomicAdd(dst + bc0 * 16 + i, s);
+                        unsigned long long sum = 0;
+                        for (int l = 0; l < rows_per_iter; ++l) sum += red_scores[(l * nb + bc0) * 16 + i];
+                        if (sum) atomicAdd(dst + bc0 * 16 + i, sum);
                     }
                 }
-                __syncthreads();
+                consumer_sync();
             }
         }
         row = max(row, ge);
@@ -186,49 +406,29 @@ __global__ void __launch_bounds__(kQuantThreads) quant_score_kernel(
 }
 
 // ------------------------------------------------------------------------ host side
-struct QuantLaunch {
-    int grid_amax, grid_quant;
-    int64_t rpc_amax, rpc_quant;
-};
-
-static QuantLaunch plan(int64_t rows, int K)
+static int sm_count()
 {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    QuantLaunch q;
-    // amax: ~4 CTAs per SM, whole rows per CTA.
-    int64_t want = (int64_t)sms * 4;
-    q.rpc_amax = (rows + want - 1) / want;
-    if (q.rpc_amax < 1) q.rpc_amax = 1;
-    q.grid_amax = (int)((rows + q.rpc_amax - 1) / q.rpc_amax);
-    // quantize: at least ~16 rows per CTA so that the score flush (K atomics per CTA) stays
-    // small next to the data, and ~4 CTAs per SM.
-    int64_t rpc = (rows + want - 1) / want;
-    int64_t min_rows = (K >= 2048) ? 16 : 32;
-    if (rpc < min_rows) rpc = min_rows;
-    q.rpc_quant = rpc;
-    q.grid_quant = (int)((rows + rpc - 1) / rpc);
-    return q;
+    return sms;
 }
 
 template <int BPT, bool S, int W>
-static void launch_quant(const QuantLaunch& q, cudaStream_t st, const __nv_bfloat16* x, int64_t ldx, int K,
-                         Groups gr, uint8_t* codes, int64_t ld_codes, uint8_t* sf, int64_t sf_cols,
-                         int zero_pad, nvq_tensor_scale* ts, unsigned long long* scores, void* w_hat)
+static cudaError_t launch_quant(int grid, cudaStream_t st, const QuantArgs& qa)
 {
-    size_t smem = (S && BPT == 1 && (kQuantThreads / (K / 16)) > 1) ? kQuantThreads * 16 * sizeof(unsigned long long) : 0;
-    if (smem > 48 * 1024)
-        cudaFuncSetAttribute(quant_score_kernel<BPT, S, W>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    quant_score_kernel<BPT, S, W><<<q.grid_quant, kQuantThreads, smem, st>>>(
-        x, ldx, K, gr, q.rpc_quant, codes, ld_codes, sf, sf_cols, zero_pad, ts, scores, w_hat);
+    const size_t smem = (size_t)kQStages * kQStageBytes + (S ? kQCompute * 16 * sizeof(unsigned long long) : 0);
+    cudaError_t e = cudaFuncSetAttribute(quant_score_kernel<BPT, S, W>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    quant_score_kernel<BPT, S, W><<<grid, kQThreads, smem, st>>>(qa);
+    return cudaGetLastError();
 }
 
 nvq_status quantize_impl(const void* x, int64_t rows, int64_t K, int64_t ldx, Groups gr, uint8_t* codes,
                          int64_t ld_codes, uint8_t* sf, int64_t sf_cols, int zero_pad, nvq_tensor_scale* ts,
                          uint64_t* scores, void* w_hat, int w_hat_dtype, cudaStream_t st)
 {
-    const QuantLaunch q = plan(rows, (int)K);
+    const int sms = sm_count();
     cudaError_t e = cudaMemsetAsync(ts, 0, sizeof(nvq_tensor_scale) * gr.G, st);
     if (e != cudaSuccess) return cuda_status(e, "cudaMemsetAsync(tscale)");
     if (scores) {
@@ -236,23 +436,41 @@ nvq_status quantize_impl(const void* x, int64_t rows, int64_t K, int64_t ldx, Gr
         if (e != cudaSuccess) return cuda_status(e, "cudaMemsetAsync(scores)");
     }
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-    amax_kernel<<<q.grid_amax, kQuantThreads, 0, st>>>(xb, ldx, (int)K, gr, q.rpc_amax, ts);
-    NVQ_LAUNCH_CHECK("amax_kernel");
-    unsigned long long* sc = reinterpret_cast<unsigned long long*>(scores);
-    const int k = (int)K;
-    const int what = w_hat ? (w_hat_dtype == NVQ_F32 ? 2 : 1) : 0;
-    if (K <= 4096) {
-        if (sc) launch_quant<1, true, 0>(q, st, xb, ldx, k, gr, codes, ld_codes, sf, sf_cols, zero_pad, ts, sc, nullptr);
-        else if (what == 0) launch_quant<1, false, 0>(q, st, xb, ldx, k, gr, codes, ld_codes, sf, sf_cols, zero_pad, ts, nullptr, nullptr);
-        else if (what == 1) launch_quant<1, false, 1>(q, st, xb, ldx, k, gr, codes, ld_codes, sf, sf_cols, zero_pad, ts, nullptr, w_hat);
-        else launch_quant<1, false, 2>(q, st, xb, ldx, k, gr, codes, ld_codes, sf, sf_cols, zero_pad, ts, nullptr, w_hat);
-    } else {
-        if (sc) launch_quant<2, true, 0>(q, st, xb, ldx, k, gr, codes, ld_codes, sf, sf_cols, zero_pad, ts, sc, nullptr);
-        else if (what == 0) launch_quant<2, false, 0>(q, st, xb, ldx, k, gr, codes, ld_codes, sf, sf_cols, zero_pad, ts, nullptr, nullptr);
-        else if (what == 1) launch_quant<2, false, 1>(q, st, xb, ldx, k, gr, codes, ld_codes, sf, sf_cols, zero_pad, ts, nullptr, w_hat);
-        else launch_quant<2, false, 2>(q, st, xb, ldx, k, gr, codes, ld_codes, sf, sf_cols, zero_pad, ts, nullptr, w_hat);
+    // amax: ~8 CTAs per SM, whole rows per CTA
+    {
+        const int64_t want = (int64_t)sms * 8;
+        int64_t rpc = (rows + want - 1) / want;
+        if (rpc < 1) rpc = 1;
+        const int grid = (int)((rows + rpc - 1) / rpc);
+        amax_kernel<<<grid, kAmaxThreads, 0, st>>>(xb, ldx, (int)K, gr, rpc, ts);
+        NVQ_LAUNCH_CHECK("amax_kernel");
     }
-    NVQ_LAUNCH_CHECK("quant_score_kernel");
+    QuantArgs qa;
+    qa.x = xb;
+    qa.ldx = ldx;
+    qa.K = (int)K;
+    qa.gr = gr;
+    qa.rows_per_cta = (rows + sms - 1) / sms;
+    qa.codes = codes;
+    qa.ld_codes = ld_codes;
+    qa.sf = sf;
+    qa.sf_cols = sf_cols;
+    qa.zero_pad = zero_pad;
+    qa.ts = ts;
+    qa.scores = reinterpret_cast<unsigned long long*>(scores);
+    qa.w_hat = w_hat;
+    qa.status = device_status_ptr();
+    qa.wait_limit = wait_limit();
+    NVQ_CHECK_ARG(qa.status, NVQ_ERR_CUDA, "quantize: device status word unavailable");
+    const int grid = (int)((rows + qa.rows_per_cta - 1) / qa.rows_per_cta);
+    const bool sc = scores != nullptr;
+    const int what = w_hat ? (w_hat_dtype == NVQ_F32 ? 2 : 1) : 0;
+    static_assert(kQCompute * 16 >= 8192, "one 16-element block per thread must cover K <= 8192");
+    if (sc) e = launch_quant<1, true, 0>(grid, st, qa);
+    else if (what == 0) e = launch_quant<1, false, 0>(grid, st, qa);
+    else if (what == 1) e = launch_quant<1, false, 1>(grid, st, qa);
+    else e = launch_quant<1, false, 2>(grid, st, qa);
+    if (e != cudaSuccess) return cuda_status(e, "quant_score_kernel");
     return NVQ_OK;
 }
 

@@ -47,10 +47,16 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
     return base + x - v;
 }
 
+// Radix select of the k-th largest score, MSB first, 8 bits per pass.  Every thread keeps its
+// (at most 8) channels' scores in registers; per pass each warp folds equal digits with
+// __match_any_sync before one shared atomic per distinct digit, so the histogram sees no
+// contention.  The threshold T is exact; channels above T are all taken and the lowest-index
+// channels equal to T fill the rest (ties to the lower channel index).
+static constexpr int kTopkPer = 8;  // channels per thread: K <= 8192
+
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const unsigned long long* __restrict__ scores, int K, int k,
                                                              int32_t* __restrict__ idx)
 {
-    extern __shared__ unsigned long long s[];  // [K]
     __shared__ unsigned int hist[256];
     __shared__ int warp_sums[32];
     __shared__ unsigned long long s_prefix, s_or;
@@ -58,28 +64,36 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const unsigned long 
     const int g = blockIdx.x;
     const unsigned long long* src = scores + (int64_t)g * K;
     int32_t* out = idx + (int64_t)g * k;
-    const int tid = threadIdx.x;
-
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int per = (K + kTopkThreads - 1) / kTopkThreads;
+    const int j0 = tid * per;
+    unsigned long long key[kTopkPer];
     unsigned long long orv = 0;
-    for (int j = tid; j < K; j += kTopkThreads) {
-        unsigned long long v = src[j];
-        s[j] = v;
-        orv |= v;
+#pragma unroll
+    for (int q = 0; q < kTopkPer; ++q) {
+        const int j = j0 + q;
+        key[q] = (q < per && j < K) ? src[j] : 0ull;
+        orv |= key[q];
     }
     if (tid == 0) { s_or = 0; s_prefix = 0; s_remaining = k; }
     __syncthreads();
+#pragma unroll
     for (int o = 16; o > 0; o >>= 1) orv |= __shfl_xor_sync(0xffffffffu, orv, o);
-    if ((tid & 31) == 0 && orv) atomicOr(&s_or, orv);
+    if (lane == 0 && orv) atomicOr(&s_or, orv);
     __syncthreads();
     const int top_bit = s_or ? 63 - __clzll(s_or) : 0;
     unsigned long long mask = 0;
     for (int shift = (top_bit / 8) * 8; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
+        if (tid < 256) hist[tid] = 0;
         __syncthreads();
         const unsigned long long prefix = s_prefix;
-        for (int j = tid; j < K; j += kTopkThreads) {
-            unsigned long long v = s[j];
-            if ((v & mask) == prefix) atomicAdd(&hist[(v >> shift) & 255u], 1u);
+#pragma unroll
+        for (int q = 0; q < kTopkPer; ++q) {
+            if (q >= per) break;  // uniform across the block
+            const int j = j0 + q;
+            const int d = (j < K && (key[q] & mask) == prefix) ? (int)((key[q] >> shift) & 255u) : 256;
+            const unsigned peers = __match_any_sync(0xffffffffu, d);
+            if (d < 256 && lane == __ffs(peers) - 1) atomicAdd(&hist[d], (unsigned)__popc(peers));
         }
         __syncthreads();
         if (tid < 32) {
@@ -114,78 +128,87 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const unsigned long 
         mask |= 255ull << shift;
         __syncthreads();
     }
-    // s_prefix is now the k-th largest score T; s_remaining of the channels equal to T are taken.
     const unsigned long long T = s_prefix;
     const int take_eq = s_remaining;
-    // Each thread owns a contiguous run of channels so that scans follow channel order.
-    const int per = (K + kTopkThreads - 1) / kTopkThreads;
-    const int j0 = tid * per, j1 = min(K, j0 + per);
     int n_eq = 0;
-    for (int j = j0; j < j1; ++j) n_eq += (s[j] == T);
+#pragma unroll
+    for (int q = 0; q < kTopkPer; ++q)
+        if (q < per && j0 + q < K) n_eq += (key[q] == T);
     int total;
-    int eq_rank = block_exclusive_scan(n_eq, warp_sums, &total);
+    const int eq_rank = block_exclusive_scan(n_eq, warp_sums, &total);
     int n_sel = 0;
     {
         int r = eq_rank;
-        for (int j = j0; j < j1; ++j) {
-            unsigned long long v = s[j];
-            bool sel = v > T || (v == T && r < take_eq);
-            r += (v == T);
+#pragma unroll
+        for (int q = 0; q < kTopkPer; ++q) {
+            if (q >= per || j0 + q >= K) continue;
+            const bool sel = key[q] > T || (key[q] == T && r < take_eq);
+            r += (key[q] == T);
             n_sel += sel;
         }
     }
     int pos = block_exclusive_scan(n_sel, warp_sums, &total);
     {
         int r = eq_rank;
-        for (int j = j0; j < j1; ++j) {
-            unsigned long long v = s[j];
-            bool sel = v > T || (v == T && r < take_eq);
-            r += (v == T);
-            if (sel) out[pos++] = j;
+#pragma unroll
+        for (int q = 0; q < kTopkPer; ++q) {
+            if (q >= per || j0 + q >= K) continue;
+            const bool sel = key[q] > T || (key[q] == T && r < take_eq);
+            r += (key[q] == T);
+            if (sel) out[pos++] = j0 + q;
         }
     }
 }
 
 // ------------------------------------------------------------------------ activation tail
-// One warp per row; lane b handles tail block b (16 selected channels).
+// One thread per (row, tail block of 16 selected channels).
 __global__ void __launch_bounds__(256) act_tail_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, int K, int k,
                                                         Groups gr, const nvq_tensor_scale* __restrict__ ts,
                                                         const int32_t* __restrict__ idx, uint8_t* __restrict__ codes,
                                                         int64_t ld_codes, uint8_t* __restrict__ sf, int64_t sf_cols)
 {
-    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
+    const int nbt = k > 0 ? k / 16 : 1;  // k == 0: one thread per row zeroes the scale padding
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t row = t / nbt;
+    const int b = (int)(t % nbt);
     if (row >= gr.total_rows) return;
     const int g = group_of_row(gr, row);
     int64_t gb, ge;
     group_range(gr, g, gb, ge);
     if (row < gb || row >= ge) return;
-    const float s_enc = ts[g].s_enc, s_dec = ts[g].s_dec;
-    const int32_t* sel = idx + (int64_t)g * k;
-    const int nbt = k / 16;
-    const __nv_bfloat16* xr = x + row * ldx;
-    for (int b = lane; b < nbt; b += 32) {
+    if (k > 0) {
+        const float s_enc = ts[g].s_enc, s_dec = ts[g].s_dec;
+        const int32_t* sel = idx + (int64_t)g * k + b * 16;
+        const __nv_bfloat16* xr = x + row * ldx;
+        int j[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) j[i] = sel[i];
+        float xv[16];
+        uint32_t sb[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            xv[i] = __bfloat162float(xr[j[i]]);
+            sb[i] = sf[sf_offset(row, j[i] >> 4, sf_cols)];
+        }
         float rv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const int j = sel[b * 16 + i];
-            const float xv = __bfloat162float(xr[j]);
-            const uint32_t sb = sf[sf_offset(row, j >> 4, sf_cols)];
-            const float sbv = e4m3_value(sb);
+            const float sbv = e4m3_value(sb[i]);
             uint32_t code;
-            if (sb == 0) {
-                code = (__float_as_uint(xv) >> 28) & 0x8u;
+            if (sb[i] == 0) {
+                code = (__float_as_uint(xv[i]) >> 28) & 0x8u;
             } else {
                 const float e_b = __fdiv_rn(s_enc, sbv);
-                code = e2m1x2(__fmul_rn(xv, e_b), 0.0f) & 0xfu;
+                code = e2m1x2(__fmul_rn(xv[i], e_b), 0.0f) & 0xfu;
             }
-            rv[i] = residual(xv, code, __fmul_rn(sbv, s_dec));
+            rv[i] = residual(xv[i], code, __fmul_rn(sbv, s_dec));
         }
         BlockOut o = quantize16(rv, s_enc, s_dec);
         *reinterpret_cast<uint2*>(codes + row * ld_codes + (K + 16 * b) / 2) = make_uint2(o.code_lo, o.code_hi);
         sf[sf_offset(row, K / 16 + b, sf_cols)] = (uint8_t)o.sb;
     }
-    for (int64_t c = (K + k) / 16 + lane; c < sf_cols; c += 32) sf[sf_offset(row, c, sf_cols)] = 0;
+    if (b == 0)
+        for (int64_t c = (K + k) / 16; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
 }
 
 // ------------------------------------------------------------------------ weight tail
@@ -257,16 +280,12 @@ extern "C" nvq_status rac_select_quantize(const void* x, int64_t rows, int64_t K
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Groups gr{grp_off, grp_rows, groups, rows};
     if (k > 0) {
-        size_t smem = sizeof(unsigned long long) * (size_t)K;
-        if (smem > 32 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(topk_kernel)");
-        }
-        topk_kernel<<<groups, kTopkThreads, smem, st>>>(reinterpret_cast<const unsigned long long*>(scores), (int)K, k, idx);
+        topk_kernel<<<groups, kTopkThreads, 0, st>>>(reinterpret_cast<const unsigned long long*>(scores), (int)K, k, idx);
         NVQ_LAUNCH_CHECK("topk_kernel");
     }
-    act_tail_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), ldx, (int)K, k, gr,
-                                                                tscale, idx, codes, ld_codes, sf, sf_cols);
+    const int64_t threads = rows * (k > 0 ? k / 16 : 1);
+    act_tail_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), ldx, (int)K,
+                                                                       k, gr, tscale, idx, codes, ld_codes, sf, sf_cols);
     NVQ_LAUNCH_CHECK("act_tail_kernel");
     return NVQ_OK;
 }

@@ -72,9 +72,13 @@ def _check_layer(L, T, H, E, topk, I, k, routing, seed, sample_rows=None):
     routed = np.nonzero(row_src >= 0)[0]
     if sample_rows is not None and routed.size > sample_rows:
         routed = np.sort(np.random.default_rng(seed).choice(routed, sample_rows, replace=False))
+    tok_of = np.where(row_src >= 0, row_src // topk, 0)
     arc, ars = _operand_rows(layer.a_routed, routed, H + k)
-    tok = row_src[routed] // topk
-    assert np.array_equal(arc, a1c[tok]) and np.array_equal(ars, a1s[tok])
+    assert np.array_equal(arc, a1c[tok_of[routed]]) and np.array_equal(ars, a1s[tok_of[routed]])
+    pad = np.nonzero(row_src < 0)[0][:64]
+    if pad.size:
+        pc, ps = _operand_rows(layer.a_routed, pad, H + k)
+        assert not pc.any() and not ps.any()
 
     # weights as the GEMM saw them (tails rebuilt inside the calls): check them against the oracle
     _, _, w13_sdec, _ = tscale_fields(layer.w13.tscale)
