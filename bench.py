@@ -163,18 +163,52 @@ def run_ours(args, world, rank, local):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    probes = {}
-
-    def step(events=None):
+    def step_eager(events=None):
         layer.forward(x, ids_d, tw_d, out, events=events)
 
     for _ in range(args.warmup):
         flush.zero_()
-        step()
+        step_eager()
     torch.cuda.synchronize()
     st, where = L.device_status()
     if st != 0:
         raise RuntimeError(f"device wait ran out ({where}) during warm-up")
+
+    # the whole layer as one CUDA graph (no host synchronisation inside a forward), with the
+    # per-kernel events recorded inside the graph
+    # timing events recorded inside the graph must be external (event-record nodes)
+    try:
+        graph_events = {name: (torch.cuda.Event(enable_timing=True, external=True),
+                               torch.cuda.Event(enable_timing=True, external=True))
+                        for name in ("quant_rac_tokens", "gemm_gate_up", "gemm_down")}
+    except TypeError:  # torch without external events: per-kernel times come from an eager pass
+        graph_events = None
+    graph = None
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            layer.forward(x, ids_d, tw_d, out)  # warm on the capture stream
+            torch.cuda.synchronize()
+            with torch.cuda.graph(graph, stream=cap):
+                layer.forward(x, ids_d, tw_d, out, events=graph_events)
+        if graph_events is None:
+            graph_events = {}
+        stream.wait_stream(cap)
+        for _ in range(args.warmup):
+            flush.zero_()
+            graph.replay()
+        torch.cuda.synchronize()
+
+    def step(events=None):
+        if graph is None:
+            step_eager(events)
+        else:
+            graph.replay()
+            if events is not None:
+                for k2, (e0, e1) in graph_events.items():
+                    events[k2] = (e0, e1)
 
     # ---- device-timed steps (inputs resident), L2 flushed before every step (untimed)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -185,11 +219,17 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     sampler.start()
     t_wall0 = time.perf_counter()
+    kernel_ms = {}
     for i in range(args.steps):
         flush.zero_()
         starts[i].record(stream)
         step(ev_lists[i])
         ends[i].record(stream)
+        if graph is not None:
+            # graph events are re-recorded by every replay: read them before the next one
+            ends[i].synchronize()
+            for k2, (e0, e1) in ev_lists[i].items():
+                kernel_ms.setdefault(k2, []).append(e0.elapsed_time(e1))
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
     barrier(world)
@@ -201,7 +241,10 @@ def run_ours(args, world, rank, local):
 
     # per-kernel durations of the two grouped GEMMs inside the timed steps
     def avg(name):
-        v = [ev[name][0].elapsed_time(ev[name][1]) for ev in ev_lists if name in ev]
+        if graph is not None:
+            v = kernel_ms.get(name, [])
+        else:
+            v = [ev[name][0].elapsed_time(ev[name][1]) for ev in ev_lists if name in ev]
         return sum(v) / len(v) if v else None
 
     t_gu, t_dn = avg("gemm_gate_up"), avg("gemm_down")
@@ -236,6 +279,8 @@ def run_ours(args, world, rank, local):
         e.synchronize()
         if i >= args.warmup:
             e2e_ms.append(s.elapsed_time(e))
+    # the result read back to the host is the layer output itself
+    assert torch.equal(out_h.view(torch.int16), out.cpu().view(torch.int16))
     e2e_tot = max_over_ranks(sum(e2e_ms), world)
     e2e_tps = T * world / (e2e_tot / len(e2e_ms) * 1e-3)
     st, where = L.device_status()
@@ -269,6 +314,7 @@ def run_ours(args, world, rank, local):
                      "peak_source": f"{src} bf16 burst {peaks['bf16_tflops']} x nominal NVFP4/BF16 ratio 6"},
         "e2e": {"value": round(e2e_tps, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
+        "launch_mode": "cuda graph (one replay per step)" if graph is not None else "eager stream launches",
         "clocks": clocks,
         "wall_s_timed_region": round(t_wall, 3),
     }
@@ -429,6 +475,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="launch the kernels one by one instead of a CUDA graph")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()

@@ -203,6 +203,25 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v)
     for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// n32 consecutive 32-byte pieces of packed words to global memory: 256-bit stores when the
+// destination is 32-byte aligned (wide), 128-bit stores otherwise.
+template <int kWords>
+__device__ __forceinline__ void store_row(void* dst, const uint32_t* w, bool wide)
+{
+    if (wide) {
+#pragma unroll
+        for (int i = 0; i < kWords / 8; ++i)
+            asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(reinterpret_cast<uint32_t*>(dst) + 8 * i),
+                         "r"(w[8 * i]), "r"(w[8 * i + 1]), "r"(w[8 * i + 2]), "r"(w[8 * i + 3]), "r"(w[8 * i + 4]),
+                         "r"(w[8 * i + 5]), "r"(w[8 * i + 6]), "r"(w[8 * i + 7])
+                         : "memory");
+    } else {
+        uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int i = 0; i < kWords / 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -483,6 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const int half = (warp - 3) >> 2;
         const int r_in_tile = quarter * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        const bool wide = (a.ldo % 16) == 0 && (reinterpret_cast<uintptr_t>(a.out) % 32) == 0;
         uint32_t acc_phase = 0;
         for (int64_t t = blockIdx.x; t < total_tiles && !*abrt; t += gridDim.x) {
             const Tile T = tile_of(t, n_tiles, tab, G);
@@ -523,11 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     const float g1 = __fmul_rn(alpha, g[2 * i + 1]), u1 = __fmul_rn(alpha, u[2 * i + 1]);
                     pk[i] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u0, __fdividef(g1, 1.0f + __expf(-g1)) * u1);
                 }
-                if (valid) {
-                    uint4* d = reinterpret_cast<uint4*>(a.out + grow * a.ldo + (int64_t)T.nt * (kBN / 2) + half * 64);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) d[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                }
+                if (valid) store_row<32>(a.out + grow * a.ldo + (int64_t)T.nt * (kBN / 2) + half * 64, pk, wide);
             } else {
                 float v0[64], v1[64];
                 tmem_ld64(tacc + half * (kBN / 2), v0);
@@ -546,11 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     pk[i] = pack_bf16x2(y0, y1);
                     pk[32 + i] = pack_bf16x2(z0, z1);
                 }
-                if (valid) {
-                    uint4* d = reinterpret_cast<uint4*>(a.out + grow * a.ldo + (int64_t)T.nt * kBN + half * (kBN / 2));
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) d[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                }
+                if (valid) store_row<64>(a.out + grow * a.ldo + (int64_t)T.nt * kBN + half * (kBN / 2), pk, wide);
             }
             acc_phase ^= 1;
         }

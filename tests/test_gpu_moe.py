@@ -25,14 +25,18 @@ def L():
 
 
 def _operand_rows(op, rows, ktot):
-    codes = op.codes.cpu().numpy()[rows, :ktot // 2]
+    rows = np.asarray(rows)
+    codes = op.codes[torch.from_numpy(rows).to(op.codes.device)].cpu().numpy()[:, :ktot // 2]
     sfl = unswizzle(op.sf, int(rows.max()) + 1, ktot // 16, op.sf_cols)[rows]
     return codes, sfl
 
 
-def _check_layer(L, T, H, E, topk, I, k, routing, seed, sample_rows=None):
+def _check_layer(L, T, H, E, topk, I, k, routing, seed, sample_rows=None, n_outliers=None, max_experts=None):
+    """sample_rows: routed rows checked in the gate/up GEMM (None: all); max_experts: experts
+    checked in the gate/up and down stages (None: all)."""
     from nvfp4_w4a4_quantized_quantize_gb300.layers import MoERacLayer
-    cfg = wl.MoELayer("t", T=T, H=H, E=E, topk=topk, I=I, k=k, seed=seed, routing=routing, n_outliers=max(1, H // 100))
+    cfg = wl.MoELayer("t", T=T, H=H, E=E, topk=topk, I=I, k=k, seed=seed, routing=routing,
+                      n_outliers=max(1, H // 100) if n_outliers is None else n_outliers)
     x_bits, ids, tw, _ = cfg.make_tokens()
     w13_bits, w2_bits = cfg.make_weights()
     dev = "cuda"
@@ -68,8 +72,18 @@ def _check_layer(L, T, H, E, topk, I, k, routing, seed, sample_rows=None):
     assert np.array_equal(a1c, np.concatenate([q1.codes, q1.tail_codes], 1))
     assert np.array_equal(a1s, np.concatenate([q1.scales, q1.tail_scales], 1))
 
+    # experts checked in the GEMM stages: all, or a few (the largest, the smallest non-empty, random)
+    nonempty = np.nonzero(grp_rows)[0]
+    if max_experts is not None and nonempty.size > max_experts:
+        by_size = nonempty[np.argsort(grp_rows[nonempty])]
+        pick = [by_size[-1], by_size[0]] + list(np.random.default_rng(seed).choice(by_size[1:-1], max_experts - 2, replace=False))
+        experts = np.array(sorted(set(int(e) for e in pick)))
+    else:
+        experts = nonempty
+
     # 3. gather into the routed layout
     routed = np.nonzero(row_src >= 0)[0]
+    routed = routed[np.isin(np.searchsorted(grp_off, routed, side="right") - 1, experts)]
     if sample_rows is not None and routed.size > sample_rows:
         routed = np.sort(np.random.default_rng(seed).choice(routed, sample_rows, replace=False))
     tok_of = np.where(row_src >= 0, row_src // topk, 0)
@@ -106,10 +120,8 @@ def _check_layer(L, T, H, E, topk, I, k, routing, seed, sample_rows=None):
     idx2 = layer.idx2.cpu().numpy()
     y_gpu = bf16_bits(layer.y)
     worst_y = 0.0
-    for g in range(E):
+    for g in experts:
         c = int(grp_rows[g])
-        if c == 0:
-            continue
         rows_g = np.arange(grp_off[g], grp_off[g] + c)
         hq = oracle.rac_quantize(h_gpu[rows_g], k)
         assert np.float32(hq.ts.amax) == a2_amax[g] and np.float32(hq.ts.s_dec) == a2_sdec[g]
