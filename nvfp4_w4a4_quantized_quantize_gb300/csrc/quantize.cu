@@ -167,7 +167,7 @@ __device__ __forceinline__ void score_acc(unsigned long long& acc, float r, floa
 {
     const float y = __fmaf_rn(fabsf(r), sc, 8388608.0f);
     const uint32_t q = __float_as_uint(y) & 0x7fffffu;
-    asm("mad.wide.u32 %0, %1, %1, %0;" : "+l"(acc) : "r"(q));
+    acc += (unsigned long long)q * q;  // one wide multiply-add
 }
 
 struct QuantArgs {

@@ -57,10 +57,10 @@ static constexpr int kTopkPer = 8;  // channels per thread: K <= 8192
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const unsigned long long* __restrict__ scores, int K, int k,
                                                              int32_t* __restrict__ idx)
 {
-    __shared__ unsigned int hist[256];
+    __shared__ unsigned int hist2[2][256];
     __shared__ int warp_sums[32];
     __shared__ unsigned long long s_prefix, s_or;
-    __shared__ int s_remaining, s_digit, s_above;
+    __shared__ int s_remaining;
     const int g = blockIdx.x;
     const unsigned long long* src = scores + (int64_t)g * K;
     int32_t* out = idx + (int64_t)g * k;
@@ -83,9 +83,12 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const unsigned long 
     __syncthreads();
     const int top_bit = s_or ? 63 - __clzll(s_or) : 0;
     unsigned long long mask = 0;
-    for (int shift = (top_bit / 8) * 8; shift >= 0; shift -= 8) {
-        if (tid < 256) hist[tid] = 0;
-        __syncthreads();
+    if (tid < 256) hist2[0][tid] = 0;
+    __syncthreads();
+    int par = 0;
+    for (int shift = (top_bit / 8) * 8; shift >= 0; shift -= 8, par ^= 1) {
+        unsigned int* hist = hist2[par];
+        if (tid < 256) hist2[par ^ 1][tid] = 0;  // the next pass's histogram
         const unsigned long long prefix = s_prefix;
 #pragma unroll
         for (int q = 0; q < kTopkPer; ++q) {
@@ -109,21 +112,17 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const unsigned long 
             }
             int above = incl - tot;
             const int rem = s_remaining;
+            __syncwarp();  // every lane has read s_remaining before the one owner lane rewrites it
             if (above < rem && rem <= incl) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     if (above < rem && rem <= above + cnt[i]) {
-                        s_digit = 255 - 8 * tid - i;
-                        s_above = above;
+                        s_prefix = prefix | ((unsigned long long)(255 - 8 * tid - i) << shift);
+                        s_remaining = rem - above;
                     }
                     above += cnt[i];
                 }
             }
-        }
-        __syncthreads();
-        if (tid == 0) {
-            s_prefix = prefix | ((unsigned long long)s_digit << shift);
-            s_remaining -= s_above;
         }
         mask |= 255ull << shift;
         __syncthreads();
@@ -161,54 +160,64 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const unsigned long 
 }
 
 // ------------------------------------------------------------------------ activation tail
-// One thread per (row, tail block of 16 selected channels).
+// Half a warp per (row, tail block of 16 selected channels): lane i of the half gathers channel
+// idx[16 b + i], recomputes its residual (bit-identical to the first pass), and the 16 lanes
+// quantize the block together (max by shuffles, codes packed by shuffles).
 __global__ void __launch_bounds__(256) act_tail_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, int K, int k,
                                                         Groups gr, const nvq_tensor_scale* __restrict__ ts,
                                                         const int32_t* __restrict__ idx, uint8_t* __restrict__ codes,
                                                         int64_t ld_codes, uint8_t* __restrict__ sf, int64_t sf_cols)
 {
-    const int nbt = k > 0 ? k / 16 : 1;  // k == 0: one thread per row zeroes the scale padding
-    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t row = t / nbt;
-    const int b = (int)(t % nbt);
-    if (row >= gr.total_rows) return;
-    const int g = group_of_row(gr, row);
-    int64_t gb, ge;
-    group_range(gr, g, gb, ge);
-    if (row < gb || row >= ge) return;
-    if (k > 0) {
-        const float s_enc = ts[g].s_enc, s_dec = ts[g].s_dec;
-        const int32_t* sel = idx + (int64_t)g * k + b * 16;
-        const __nv_bfloat16* xr = x + row * ldx;
-        int j[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) j[i] = sel[i];
-        float xv[16];
-        uint32_t sb[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            xv[i] = __bfloat162float(xr[j[i]]);
-            sb[i] = sf[sf_offset(row, j[i] >> 4, sf_cols)];
-        }
-        float rv[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float sbv = e4m3_value(sb[i]);
-            uint32_t code;
-            if (sb[i] == 0) {
-                code = (__float_as_uint(xv[i]) >> 28) & 0x8u;
-            } else {
-                const float e_b = __fdiv_rn(s_enc, sbv);
-                code = e2m1x2(__fmul_rn(xv[i], e_b), 0.0f) & 0xfu;
-            }
-            rv[i] = residual(xv[i], code, __fmul_rn(sbv, s_dec));
-        }
-        BlockOut o = quantize16(rv, s_enc, s_dec);
-        *reinterpret_cast<uint2*>(codes + row * ld_codes + (K + 16 * b) / 2) = make_uint2(o.code_lo, o.code_hi);
-        sf[sf_offset(row, K / 16 + b, sf_cols)] = (uint8_t)o.sb;
+    const int nbt = k > 0 ? k / 16 : 1;  // k == 0: one half-warp per row zeroes the scale padding
+    const int64_t hw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 4;  // half-warp id
+    const int i = threadIdx.x & 15;
+    const int64_t row = hw / nbt;
+    const int b = (int)(hw % nbt);
+    const bool in_range = row < gr.total_rows;
+    int64_t gb = 0, ge = 0;
+    int g = 0;
+    if (in_range) {
+        g = group_of_row(gr, row);
+        group_range(gr, g, gb, ge);
     }
-    if (b == 0)
-        for (int64_t c = (K + k) / 16; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
+    const bool active = in_range && row >= gb && row < ge;
+    if (k > 0) {
+        float rv = 0.0f, s_enc = 1.0f, s_dec = 1.0f;
+        if (active) {
+            s_enc = ts[g].s_enc;
+            s_dec = ts[g].s_dec;
+            const int j = idx[(int64_t)g * k + b * 16 + i];
+            const float xv = __bfloat162float(x[row * ldx + j]);
+            const uint32_t sb = sf[sf_offset(row, j >> 4, sf_cols)];
+            const float sbv = e4m3_value(sb);
+            const float e_b = sb == 0 ? 0.0f : __fdiv_rn(s_enc, sbv);
+            const uint32_t code = e2m1x2(__fmul_rn(xv, e_b), 0.0f) & 0xfu;
+            rv = residual(xv, code, __fmul_rn(sbv, s_dec));
+        }
+        // block scale from the 16 lanes' residuals
+        float m = fabsf(rv);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o, 16));
+        const uint32_t sb2 = e4m3(__fmul_rn(__fdiv_rn(m, 6.0f), s_enc));
+        const float sbv2 = e4m3_value(sb2);
+        const float e2 = sb2 == 0 ? 0.0f : __fdiv_rn(s_enc, sbv2);
+        uint32_t c = e2m1x2(__fmul_rn(rv, e2), 0.0f) & 0xfu;   // sb2 == 0: +-0 keeps the sign
+        // pack: byte i/2 = c(i) | c(i+1) << 4, then 8 bytes of the block from lanes 0..7
+        const uint32_t c_hi = __shfl_down_sync(0xffffffffu, c, 1, 16);
+        const uint32_t byte = c | (c_hi << 4);
+        uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            w0 |= __shfl_sync(0xffffffffu, byte, 2 * q, 16) << (8 * q);
+            w1 |= __shfl_sync(0xffffffffu, byte, 8 + 2 * q, 16) << (8 * q);
+        }
+        if (active && i == 0) {
+            *reinterpret_cast<uint2*>(codes + row * ld_codes + (K + 16 * b) / 2) = make_uint2(w0, w1);
+            sf[sf_offset(row, K / 16 + b, sf_cols)] = (uint8_t)sb2;
+        }
+    }
+    if (active && b == 0)
+        for (int64_t c = (K + k) / 16 + i; c < sf_cols; c += 16) sf[sf_offset(row, c, sf_cols)] = 0;
 }
 
 // ------------------------------------------------------------------------ weight tail
@@ -283,7 +292,7 @@ extern "C" nvq_status rac_select_quantize(const void* x, int64_t rows, int64_t K
         topk_kernel<<<groups, kTopkThreads, 0, st>>>(reinterpret_cast<const unsigned long long*>(scores), (int)K, k, idx);
         NVQ_LAUNCH_CHECK("topk_kernel");
     }
-    const int64_t threads = rows * (k > 0 ? k / 16 : 1);
+    const int64_t threads = rows * (k > 0 ? k / 16 : 1) * 16;
     act_tail_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), ldx, (int)K,
                                                                        k, gr, tscale, idx, codes, ld_codes, sf, sf_cols);
     NVQ_LAUNCH_CHECK("act_tail_kernel");
