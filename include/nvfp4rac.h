@@ -239,6 +239,40 @@ nvq_status moe_dispatch(const int32_t* topk_ids, const float* topk_w, int64_t to
                         size_t workspace_bytes, void* stream);
 
 /*
+ * moe_dispatch_static_scratch -- moe_dispatch that allocates nothing.  The paper has no
+ * counterpart: this is a library convenience.  Arguments and outputs are those of moe_dispatch,
+ * minus the workspace.  The histogram moe_dispatch keeps in its workspace lives here in one
+ * file-scope device array of NVQ_DISPATCH_STATIC_SCRATCH_BYTES (1 MiB).
+ *
+ * Who needs it: callers that cannot allocate device memory, or thread a workspace, at the
+ * point of the call.  Examples are a serving engine that hands its whole HBM budget to a
+ * KV cache up front, and a fixed-signature plugin or custom-op interface with no workspace
+ * argument.  Another is code that must not pay for cudaMalloc/cudaFree, which can synchronize
+ * the device.  The call makes no cudaMalloc, cudaFree or other allocating call.
+ *
+ * Limit: moe_dispatch_workspace_size(tokens, topk, groups) must be <= 1 MiB; otherwise the call
+ * returns NVQ_ERR_SHAPE, launches nothing, and nvq_last_error() names the sizes.  At 128
+ * experts the limit is 2048 units of 256 (token, slot) pairs: 65536 tokens at top-8.  groups
+ * must be in [1, 768].
+ *
+ * First call: on each device, the first call looks up the array's device address with
+ * cudaGetSymbolAddress, with that device current, and caches it.  Make that first call before
+ * any stream capture.  A failed lookup returns NVQ_ERR_CUDA.
+ *
+ * Sharing: all calls on one device share the array.  Nothing in it needs to start at zero,
+ * because each call writes every word it later reads.  Calls that may overlap on the device
+ * race on the array and corrupt each other's output.  Examples are calls on two streams
+ * without an ordering between them, or a replay that overlaps another call.  Calls
+ * serialized on one stream are safe.
+ */
+#define NVQ_DISPATCH_STATIC_SCRATCH_BYTES (1u << 20)
+nvq_status moe_dispatch_static_scratch(const int32_t* topk_ids, const float* topk_w,
+                                       int64_t tokens, int32_t topk, int32_t groups,
+                                       int64_t* grp_off, int64_t* grp_rows, int32_t* row_src,
+                                       int64_t* row_of, float* row_w, int64_t capacity,
+                                       void* stream);
+
+/*
  * nvfp4_gather_rows -- copies quantized rows (codes and blocked scales of K_tot columns) into
  * the routed layout: out row r = source row row_src[r] / topk, padding rows (row_src < 0) get
  * zero codes and zero scales.  out_sf uses the same sf_cols as sf.  With out_codes NULL only

@@ -32,6 +32,7 @@ _SIGS = {
     "moe_capacity": ([_I64, _I32, _I32], _I64),
     "moe_dispatch_workspace_size": ([_I64, _I32, _I32], C.c_size_t),
     "moe_dispatch": ([_P, _P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _I64, _P, C.c_size_t, _P], C.c_int),
+    "moe_dispatch_static_scratch": ([_P, _P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _I64, _P], C.c_int),
     "nvfp4_gather_rows": ([_P, _I64, _P, _I64, _I64, _P, _I32, _I64, _I64, _P, _I64, _P, _P], C.c_int),
     "moe_combine": ([_P, _I64, _P, _I64, _I32, _I64, _P, _I64, _P], C.c_int),
 }
@@ -168,6 +169,17 @@ def moe_dispatch(topk_ids, topk_w, groups, grp_off, grp_rows, row_src, row_of, r
     _check("moe_dispatch", LIB.moe_dispatch(
         _ptr(topk_ids), _ptr(topk_w), T, topk, groups, _ptr(grp_off), _ptr(grp_rows), _ptr(row_src), _ptr(row_of),
         _ptr(row_w), row_src.numel(), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def moe_dispatch_static_scratch(topk_ids, topk_w, groups, grp_off, grp_rows, row_src, row_of, row_w, stream=None):
+    """moe_dispatch with no workspace: the library's own 1 MiB device array holds the scratch.
+    For callers that cannot allocate, or pass a workspace, where they dispatch. Calls that
+    overlap on one device race on that array; the first call on a device does a one-time
+    symbol lookup and should come before any stream capture."""
+    T, topk = topk_ids.shape
+    _check("moe_dispatch_static_scratch", LIB.moe_dispatch_static_scratch(
+        _ptr(topk_ids), _ptr(topk_w), T, topk, groups, _ptr(grp_off), _ptr(grp_rows), _ptr(row_src), _ptr(row_of),
+        _ptr(row_w), row_src.numel(), _stream(stream)))
 
 
 def nvfp4_gather_rows(codes, sf, sf_cols_, src_rows, row_src, topk, ktot, out_codes, out_sf, stream=None):

@@ -10,6 +10,8 @@
 //   combine    sums each token's topk expert outputs in slot order (fp32) and rounds to bf16.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace nvq {
@@ -304,5 +306,85 @@ extern "C" nvq_status moe_combine(const void* y, int64_t ldy, const int64_t* row
     combine_kernel<<<(unsigned)tokens, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(y), ldy, row_of, topk, hidden,
                                                      static_cast<__nv_bfloat16*>(out), ldo);
     NVQ_LAUNCH_CHECK("combine_kernel");
+    return NVQ_OK;
+}
+
+// ------------------------------------------------------------------------ dispatch, static scratch
+// moe_dispatch_static_scratch: the same four kernels as moe_dispatch, with the per-unit expert
+// histogram (counts[units][groups], int32) kept in one file-scope device array instead of a
+// caller workspace, so that the call allocates nothing.  Its address is looked up once per device
+// (first call on that device, with the device current) and cached.
+namespace nvq {
+
+static constexpr size_t kDispatchScratchBytes = NVQ_DISPATCH_STATIC_SCRATCH_BYTES;
+static constexpr int kScratchMaxDevices = 64;
+
+static __device__ __align__(256) int32_t g_dispatch_scratch[kDispatchScratchBytes / sizeof(int32_t)];
+
+static std::mutex g_scratch_mu;
+static void* g_scratch_addr[kScratchMaxDevices];
+
+// Device address of g_dispatch_scratch on the current device (set-up on the first call).
+static nvq_status dispatch_scratch_ptr(int32_t** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e, "moe_dispatch_static_scratch: cudaGetDevice");
+    if (dev < 0 || dev >= kScratchMaxDevices) {
+        set_error("moe_dispatch_static_scratch: device ordinal %d outside [0, %d)", dev, kScratchMaxDevices);
+        return NVQ_ERR_ARG;
+    }
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+        if (e != cudaSuccess) return cuda_status(e, "moe_dispatch_static_scratch: cudaGetSymbolAddress(g_dispatch_scratch)");
+        g_scratch_addr[dev] = p;
+    }
+    *out = static_cast<int32_t*>(g_scratch_addr[dev]);
+    return NVQ_OK;
+}
+
+}  // namespace nvq
+
+extern "C" nvq_status moe_dispatch_static_scratch(const int32_t* topk_ids, const float* topk_w, int64_t tokens,
+                                                  int32_t topk, int32_t groups, int64_t* grp_off, int64_t* grp_rows,
+                                                  int32_t* row_src, int64_t* row_of, float* row_w, int64_t capacity,
+                                                  void* stream)
+{
+    NVQ_CHECK_ARG(topk_ids && grp_off && grp_rows && row_src && row_of, NVQ_ERR_ARG,
+                  "moe_dispatch_static_scratch: null pointer argument");
+    NVQ_CHECK_ARG(tokens >= 1 && topk >= 1 && topk <= 64 && tokens * topk <= (1ll << 26), NVQ_ERR_SHAPE,
+                  "moe_dispatch_static_scratch: tokens*topk outside [1, 2^26] or topk outside [1, 64]");
+    // groups <= 768 keeps the scatter kernel's shared histogram (8 warps x groups x 8 bytes) within
+    // the 48 KB a launch gets without an attribute call
+    NVQ_CHECK_ARG(groups >= 1 && groups <= 768, NVQ_ERR_SHAPE, "moe_dispatch_static_scratch: groups outside [1, 768]");
+    NVQ_CHECK_ARG(capacity >= moe_capacity(tokens, topk, groups), NVQ_ERR_SHAPE,
+                  "moe_dispatch_static_scratch: capacity %lld < moe_capacity() = %lld", (long long)capacity,
+                  (long long)moe_capacity(tokens, topk, groups));
+    const size_t need = moe_dispatch_workspace_size(tokens, topk, groups);
+    NVQ_CHECK_ARG(need <= kDispatchScratchBytes, NVQ_ERR_SHAPE,
+                  "moe_dispatch_static_scratch: tokens=%lld topk=%d groups=%d need %zu bytes of scratch, more than the "
+                  "%zu-byte static array; call moe_dispatch with a workspace instead",
+                  (long long)tokens, (int)topk, (int)groups, need, kDispatchScratchBytes);
+    int32_t* counts = nullptr;
+    const nvq_status s = dispatch_scratch_ptr(&counts);
+    if (s != NVQ_OK) return s;
+    set_error("");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t n = tokens * topk;
+    const int units = (int)((n + kUnit - 1) / kUnit);
+    const int ctas = (units + kWarpsPerCta - 1) / kWarpsPerCta;
+    // every counts word the later kernels read is written by the histogram kernel of this call:
+    // nothing in the scratch has to start at zero
+    dispatch_hist_kernel<<<ctas, 32 * kWarpsPerCta, kWarpsPerCta * groups * sizeof(int32_t), st>>>(topk_ids, n, groups, counts);
+    NVQ_LAUNCH_CHECK("dispatch_hist_kernel");
+    dispatch_scan_kernel<<<groups, units >= 1024 ? 1024 : ((units + 31) / 32) * 32, 0, st>>>(counts, units, groups, grp_rows);
+    NVQ_LAUNCH_CHECK("dispatch_scan_kernel");
+    dispatch_offsets_kernel<<<1, 1024, 0, st>>>(groups, grp_rows, grp_off, row_src, row_w, capacity);
+    NVQ_LAUNCH_CHECK("dispatch_offsets_kernel");
+    dispatch_scatter_kernel<<<ctas, 32 * kWarpsPerCta, kWarpsPerCta * groups * sizeof(int64_t), st>>>(
+        topk_ids, topk_w, n, groups, counts, grp_off, row_src, row_of, row_w);
+    NVQ_LAUNCH_CHECK("dispatch_scatter_kernel");
     return NVQ_OK;
 }
