@@ -468,6 +468,44 @@ def run_reference(args, world, rank):
     }
 
 
+def profile_case(name: str):
+    """Small cases for ncu captures (no timing, no JSON line): 'moe_small' runs two MoE layer
+    forwards at E=32, T=4096, H=2048, I=768, top-8, k=32 (about 1 GB on the device);
+    'act_256mb' quantizes and selects twice on a 32768 x 4096 bf16 activation (256 MB, larger
+    than L2), k=64."""
+    import torch
+    from nvfp4_w4a4_quantized_quantize_gb300 import _lib as L
+    from nvfp4_w4a4_quantized_quantize_gb300 import workloads as wl
+    from nvfp4_w4a4_quantized_quantize_gb300.layers import MoERacLayer, Operand
+    dev = "cuda"
+    if name == "moe_small":
+        E, T, H, I, k, topk = 32, 4096, 2048, 768, 32, 8
+        cfg = wl.MoELayer("moe_small", T=T, H=H, E=E, topk=topk, I=I, k=k, seed=7, routing="zipf", n_outliers=20)
+        x_bits, ids, tw, _ = cfg.make_tokens()
+        w13_bits, w2_bits = cfg.make_weights()
+        layer = MoERacLayer(_bf16(w13_bits.reshape(E * 2 * I, H), dev).view(E, 2 * I, H),
+                            _bf16(w2_bits.reshape(E * H, I), dev).view(E, H, I), k, topk, T)
+        x = _bf16(x_bits, dev)
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        ids_d, tw_d = torch.from_numpy(ids).to(dev), torch.from_numpy(tw).to(dev)
+        for _ in range(2):
+            layer.forward(x, ids_d, tw_d, out)
+    else:
+        M, K, k = 32768, 4096, 64
+        gen = torch.Generator(device=dev).manual_seed(11)
+        x = torch.randn(M, K, device=dev, generator=gen).bfloat16()
+        op = Operand.empty(M, K, k)
+        sc = torch.empty(K, dtype=torch.int64, device=dev)
+        idx = torch.empty(k, dtype=torch.int32, device=dev)
+        for _ in range(2):
+            L.nvfp4_quantize(x, op.codes, op.sf, op.sf_cols, op.tscale, scores=sc)
+            L.rac_select_quantize(x, op.tscale, sc, k, op.codes, op.sf, op.sf_cols, idx)
+    torch.cuda.synchronize()
+    if L.device_status() != (0, 0):
+        raise SystemExit(f"device status {L.device_status()}")
+    print("profile case", name, "ok", flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -476,7 +514,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch the kernels one by one instead of a CUDA graph")
+    ap.add_argument("--profile-case", choices=["moe_small", "act_256mb"],
+                    help="run a small case twice for an ncu capture and exit (no timing)")
     args = ap.parse_args()
+    if args.profile_case:
+        profile_case(args.profile_case)
+        return
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()
     if args.impl == "reference":

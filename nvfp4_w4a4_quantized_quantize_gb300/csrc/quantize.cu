@@ -6,11 +6,11 @@
 //   amax_kernel          per-group max |x| (the FP32 tensor scale's statistic): 16-byte loads,
 //                        8 in flight per thread, one atomicMax per (CTA, group run);
 //   quant_score_kernel   codes + blocked E4M3 scales + residual + integer channel score (+ the
-//                        dequantized values for the trainer-side QDQ).  One CTA per SM: a
-//                        producer warp streams the CTA's band of rows into an 8-stage shared
-//                        memory ring with cp.async.bulk (128 KB in flight per SM, independent
-//                        of register pressure), eight compute warps quantize one 16-element
-//                        block per thread per row from shared memory.  The CTA re-reads the
+//                        dequantized values for the trainer-side QDQ).  One CTA of 16 warps per
+//                        SM: one lane streams the CTA's band of rows into an 8-stage shared
+//                        memory ring with cp.async.bulk (up to 96 KB in flight per SM,
+//                        independent of register pressure), every thread quantizes one
+//                        16-element block per row from shared memory.  The CTA re-reads the
 //                        rows amax_kernel's CTAs just streamed, so most of that second read is
 //                        served by L2.
 #include <cuda_bf16.h>
@@ -90,8 +90,10 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const __nv_bfloat16*
 // ------------------------------------------------------------------------ quantize + score
 static constexpr int kQStages = 8;
 static constexpr int kQStageBytes = 16384;
-static constexpr int kQCompute = 512;            // 16 compute warps: one thread per 16-element block up to K = 8192
-static constexpr int kQThreads = kQCompute + 32; // + producer warp
+static constexpr int kQCompute = 512;  // 16 warps: one thread per 16-element block up to K = 8192
+static constexpr int kQThreads = kQCompute;
+static constexpr int kQAhead = kQStages - 2;  // stages the loads run ahead of the compute
+static constexpr int kQLoader = kQThreads - 32;  // the thread that issues the bulk copies (warp 15, lane 0)
 
 __device__ __forceinline__ uint32_t sa32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -189,6 +191,63 @@ struct QuantArgs {
 };
 
 // BPT = 16-element blocks per thread along K (1: K / 16 <= kQCompute).
+// Producer cursor: walks the CTA's band of rows in the same order as the compute loop (group run
+// by group run, R rows per stage) and issues each stage's bulk copies.
+struct LoadCursor {
+    int g;
+    int64_t row, r, b;  // current group run [r, b) of the band, next stage starts at r
+    uint32_t it;        // stages issued so far
+    bool done;
+};
+
+__device__ __forceinline__ void cursor_next_run(const QuantArgs& qa, LoadCursor& c, int64_t r1)
+{
+    // advance to the first non-empty group run at or after c.row
+    while (c.row < r1 && c.g < qa.gr.G) {
+        int64_t gb, ge;
+        group_range(qa.gr, c.g, gb, ge);
+        const int64_t a = max(c.row, gb), b = min(r1, ge);
+        if (a < b) {
+            c.r = a;
+            c.b = b;
+            return;
+        }
+        c.row = max(c.row, ge);
+        ++c.g;
+    }
+    c.done = true;
+}
+
+// Issue the loads of stage c.it if the compute has released its ring slot (bounded wait).
+__device__ __forceinline__ bool cursor_issue(const QuantArgs& qa, LoadCursor& c, int64_t r1, int R, int row_bytes,
+                                             uint8_t* ring, uint64_t* full_bar, uint64_t* empty_bar, volatile int* abrt)
+{
+    const int s = c.it % kQStages;
+    if (c.it >= kQStages &&
+        !q_wait(&empty_bar[s], ((c.it / kQStages) & 1) ^ 1, abrt, qa.status, qa.wait_limit, 21))
+        return false;
+    const int nr = (int)min((int64_t)R, c.b - c.r);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa32(&full_bar[s])),
+                 "r"((uint32_t)(nr * row_bytes))
+                 : "memory");
+    for (int j = 0; j < nr; ++j)
+        q_bulk_row(ring + s * kQStageBytes + j * row_bytes, qa.x + (c.r + j) * qa.ldx, row_bytes, &full_bar[s]);
+    ++c.it;
+    c.r += R;
+    if (c.r >= c.b) {
+        c.row = c.b;
+        int64_t gb, ge;
+        group_range(qa.gr, c.g, gb, ge);
+        c.row = max(c.row, ge);
+        ++c.g;
+        cursor_next_run(qa, c, r1);
+    }
+    return true;
+}
+
+// One CTA of 16 warps per SM (4 per scheduler, 128 registers a thread: the 16 exact 64-bit
+// channel-score accumulators a thread holds stay in registers).  Every warp computes; lane 0 of
+// warp 15 also issues the bulk copies kQAhead stages ahead of the compute.
 template <int BPT, bool kScores, int kWhat>  // kWhat: 0 none, 1 bf16 w_hat, 2 fp32 w_hat
 __global__ void __launch_bounds__(kQThreads, 1) quant_score_kernel(const QuantArgs qa)
 {
@@ -202,7 +261,7 @@ __global__ void __launch_bounds__(kQThreads, 1) quant_score_kernel(const QuantAr
     const int row_bytes = 2 * K;
     const int R = max(1, kQStageBytes / row_bytes);  // rows per stage
     const int tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31;
+    const int lane = tid & 31;
     unsigned long long* red_scores = reinterpret_cast<unsigned long long*>(ring + kQStages * kQStageBytes);
 
     if (tid == 0) {
@@ -229,40 +288,22 @@ __global__ void __launch_bounds__(kQThreads, 1) quant_score_kernel(const QuantAr
     const int64_t r1 = min(r0 + qa.rows_per_cta, qa.gr.total_rows);
     if (r0 >= r1) return;
 
-    if (warp == kQCompute / 32) {
-        // ---------------- producer: stream the band's rows, group run by group run
-        if (lane == 0) {
-            uint32_t it = 0;
-            int g = group_of_row(qa.gr, r0);
-            int64_t row = r0;
-            while (row < r1 && g < qa.gr.G && !*abrt) {
-                int64_t gb, ge;
-                group_range(qa.gr, g, gb, ge);
-                const int64_t a = max(row, gb), b = min(r1, ge);
-                for (int64_t r = a; r < b && !*abrt; r += R) {
-                    const int s = it % kQStages;
-                    if (!q_wait(&empty_bar[s], ((it / kQStages) & 1) ^ 1, abrt, qa.status, qa.wait_limit, 21)) break;
-                    const int nr = (int)min((int64_t)R, b - r);
-                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa32(&full_bar[s])),
-                                 "r"((uint32_t)(nr * row_bytes))
-                                 : "memory");
-                    for (int j = 0; j < nr; ++j)
-                        q_bulk_row(ring + s * kQStageBytes + j * row_bytes, qa.x + (r + j) * qa.ldx, row_bytes, &full_bar[s]);
-                    ++it;
-                }
-                row = max(row, ge);
-                ++g;
-            }
-            if (*abrt) {
-                // let the copies still in flight land before the CTA exits (the last issue on each stage)
-                for (uint32_t j = it > kQStages ? it - kQStages : 0; j < it; ++j)
-                    q_wait(&full_bar[j % kQStages], (j / kQStages) & 1, abrt, qa.status, qa.wait_limit, 22, true);
-            }
-        }
-        return;
+    // ---------------- loader prologue: the first kQAhead stages
+    const bool loader = tid == kQLoader;
+    LoadCursor cur;
+    cur.g = group_of_row(qa.gr, r0);
+    cur.row = r0;
+    cur.r = cur.b = 0;
+    cur.it = 0;
+    cur.done = false;
+    bool load_ok = true;
+    if (loader) {
+        cursor_next_run(qa, cur, r1);
+        while (load_ok && !cur.done && cur.it < (uint32_t)kQAhead)
+            load_ok = cursor_issue(qa, cur, r1, R, row_bytes, ring, full_bar, empty_bar, abrt);
     }
 
-    // ---------------- compute warps
+    // ---------------- compute (all warps)
     const int lanes_per_row = (BPT == 1) ? nb : kQCompute;
     const int rows_per_iter = (BPT == 1) ? (kQCompute / nb) : 1;
     const int rl = tid / lanes_per_row;
@@ -294,6 +335,9 @@ __global__ void __launch_bounds__(kQThreads, 1) quant_score_kernel(const QuantAr
 
         for (int64_t r = a; r < b; r += R, ++it) {
             const int s = it % kQStages;
+            // keep the loads kQAhead stages ahead (the slot refilled here was released two stages ago)
+            if (loader && load_ok && !cur.done && !*abrt)
+                load_ok = cursor_issue(qa, cur, r1, R, row_bytes, ring, full_bar, empty_bar, abrt);
             // a warp that gives up keeps walking the same sequence (so that no named barrier is
             // left waiting for it) but skips the work
             if (!dead && !q_wait(&full_bar[s], (it / kQStages) & 1, abrt, qa.status, qa.wait_limit, 23)) dead = true;
@@ -385,16 +429,16 @@ __global__ void __launch_bounds__(kQThreads, 1) quant_score_kernel(const QuantAr
                     }
                 }
             } else {
-                // BPT == 1: fold the rows_per_iter row lanes of each block column in shared memory
+                // BPT == 1: fold the rows_per_iter row lanes of each channel in shared memory,
+                // one channel per compute thread at a time
 #pragma unroll
                 for (int i = 0; i < 16; ++i) red_scores[tid * 16 + i] = part[0][i];
                 consumer_sync();
-                if (rl == 0 && a < b && !dead) {
-#pragma unroll 1
-                    for (int i = 0; i < 16; ++i) {
+                if (a < b && !dead) {
+                    for (int ch = tid; ch < K; ch += kQCompute) {
                         unsigned long long sum = 0;
-                        for (int l = 0; l < rows_per_iter; ++l) sum += red_scores[(l * nb + bc0) * 16 + i];
-                        if (sum) atomicAdd(dst + bc0 * 16 + i, sum);
+                        for (int l = 0; l < rows_per_iter; ++l) sum += red_scores[l * K + ch];
+                        if (sum) atomicAdd(dst + ch, sum);
                     }
                 }
                 consumer_sync();
@@ -402,6 +446,12 @@ __global__ void __launch_bounds__(kQThreads, 1) quant_score_kernel(const QuantAr
         }
         row = max(row, ge);
         ++g;
+    }
+    if (loader && *abrt) {
+        // after a timeout, let the copies still in flight land before the CTA exits (the last
+        // issue on each slot)
+        for (uint32_t j = cur.it > kQStages ? cur.it - kQStages : 0; j < cur.it; ++j)
+            q_wait(&full_bar[j % kQStages], (j / kQStages) & 1, abrt, qa.status, qa.wait_limit, 22, true);
     }
 }
 
