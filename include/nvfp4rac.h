@@ -212,10 +212,29 @@ nvq_status w4a4_rac_grouped_gemm(int32_t groups, const int64_t* grp_off, const i
  * b_codes and scale columns [K / 16, (K + k) / 16) of b_sf; scale columns beyond are zeroed.
  *   b_codes, ldb, b_sf, b_sf_cols, b_tscale   weight_qdq output for groups x N rows.
  *   idx       int32 [groups][k] if idx_per_group else [k].  1 <= k <= min(K, 512), k % 16 == 0.
+ *   cm_codes, cm_sf   NULL, or the nvfp4_channel_major copy of the same weights (both or
+ *             neither; N % 64 == 0).  With the copy the selected channels are read in
+ *             coalesced runs (about 1.5 N bytes per selected channel instead of scattered
+ *             bytes of every row); the result is identical.
  */
 nvq_status rac_weight_tail(int32_t groups, int64_t N, int64_t K, int32_t k, const int32_t* idx,
                            int32_t idx_per_group, uint8_t* b_codes, int64_t ldb, uint8_t* b_sf,
-                           int64_t b_sf_cols, const nvq_tensor_scale* b_tscale, void* stream);
+                           int64_t b_sf_cols, const nvq_tensor_scale* b_tscale,
+                           const uint8_t* cm_codes, const uint8_t* cm_sf, void* stream);
+
+/*
+ * nvfp4_channel_major -- a channel-major copy of quantized weights (layout only; the paper's
+ * weights are static at rollout, so the copy is made once per weight update next to
+ * weight_qdq).  It serves rac_weight_tail, which gathers whole channels of W.
+ *   b_codes, ldb, b_sf, b_sf_cols   groups x N rows of K codes / K/16 blocked scales.
+ *   cm_codes  uint8 [groups][K][N / 2] out: byte (g, j, m) = code of row 2m of channel j
+ *             (low nibble) | code of row 2m + 1 (high nibble).  16-byte aligned.
+ *   cm_sf     uint8 [groups][K / 16][N] out: scale byte of (row n, block c) at (g, c, n).
+ *   N % 64 == 0, groups * N <= 2^24, K % 16 == 0, K <= 8192.
+ */
+nvq_status nvfp4_channel_major(int32_t groups, int64_t N, int64_t K, const uint8_t* b_codes,
+                               int64_t ldb, const uint8_t* b_sf, int64_t b_sf_cols,
+                               uint8_t* cm_codes, uint8_t* cm_sf, void* stream);
 
 /*
  * moe_dispatch -- routing plumbing of the MoE expert layer (not described by the paper):

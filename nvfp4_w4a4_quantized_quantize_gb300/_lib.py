@@ -28,7 +28,8 @@ _SIGS = {
     "weight_qdq": ([_P, _I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _I32, _P], C.c_int),
     "w4a4_rac_grouped_gemm": ([_I32, _P, _P, _I64, _P, _I64, _P, _I64, _P, _I32, _P, _I64, _P, _I64, _P, _I64, _I64,
                                _I32, _P, _I32, _I32, _P, _P, _I64, _P], C.c_int),
-    "rac_weight_tail": ([_I32, _I64, _I64, _I32, _P, _I32, _P, _I64, _P, _I64, _P, _P], C.c_int),
+    "rac_weight_tail": ([_I32, _I64, _I64, _I32, _P, _I32, _P, _I64, _P, _I64, _P, _P, _P, _P], C.c_int),
+    "nvfp4_channel_major": ([_I32, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _P], C.c_int),
     "moe_capacity": ([_I64, _I32, _I32], _I64),
     "moe_dispatch_workspace_size": ([_I64, _I32, _I32], C.c_size_t),
     "moe_dispatch": ([_P, _P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _I64, _P, C.c_size_t, _P], C.c_int),
@@ -158,10 +159,17 @@ def w4a4_rac_grouped_gemm(a_codes, a_sf, a_sf_cols, a_tscale, b_codes, b_sf, b_s
         out.stride(0), _stream(stream)))
 
 
-def rac_weight_tail(groups, N, K, k, idx, b_codes, b_sf, b_sf_cols, b_tscale, idx_per_group=False, stream=None):
+def rac_weight_tail(groups, N, K, k, idx, b_codes, b_sf, b_sf_cols, b_tscale, idx_per_group=False, cm_codes=None,
+                    cm_sf=None, stream=None):
     _check("rac_weight_tail", LIB.rac_weight_tail(
         groups, N, K, k, _ptr(idx), int(bool(idx_per_group)), _ptr(b_codes), b_codes.stride(0), _ptr(b_sf),
-        b_sf_cols, _ptr(b_tscale), _stream(stream)))
+        b_sf_cols, _ptr(b_tscale), _ptr(cm_codes), _ptr(cm_sf), _stream(stream)))
+
+
+def nvfp4_channel_major(groups, N, K, b_codes, b_sf, b_sf_cols, cm_codes, cm_sf, stream=None):
+    _check("nvfp4_channel_major", LIB.nvfp4_channel_major(
+        groups, N, K, _ptr(b_codes), b_codes.stride(0), _ptr(b_sf), b_sf_cols, _ptr(cm_codes), _ptr(cm_sf),
+        _stream(stream)))
 
 
 def moe_dispatch(topk_ids, topk_w, groups, grp_off, grp_rows, row_src, row_of, row_w, workspace, stream=None):

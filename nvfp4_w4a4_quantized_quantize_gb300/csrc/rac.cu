@@ -252,6 +252,95 @@ __global__ void __launch_bounds__(256) weight_tail_kernel(uint8_t* __restrict__ 
         for (int64_t c = (K + k) / 16; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
 }
 
+// Same tail from the channel-major copy (nvfp4_channel_major): thread per (group, tail block,
+// weight row n), n fastest, so a warp reads each selected channel's 32 codes (16 bytes) and 32
+// block scales (32 bytes) of consecutive rows in one coalesced access.
+__global__ void __launch_bounds__(256) weight_tail_cm_kernel(uint8_t* __restrict__ codes, int64_t ld_codes,
+                                                              uint8_t* __restrict__ sf, int64_t sf_cols, int64_t N,
+                                                              int K, int k, int G, const nvq_tensor_scale* __restrict__ ts,
+                                                              const int32_t* __restrict__ idx, int idx_per_group,
+                                                              const uint8_t* __restrict__ cm_codes,
+                                                              const uint8_t* __restrict__ cm_sf)
+{
+    const int nbt = k / 16;
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= (int64_t)G * nbt * N) return;
+    const int64_t n = t % N;
+    const int b = (int)((t / N) % nbt);
+    const int g = (int)(t / (N * nbt));
+    const float s_enc = ts[g].s_enc, s_dec = ts[g].s_dec;
+    const int32_t* sel = idx + (idx_per_group ? (int64_t)g * k : 0) + b * 16;
+    const int nsb = K / 16;
+    float wv[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int j = sel[i];
+        const uint32_t c = (cm_codes[((int64_t)g * K + j) * (N / 2) + (n >> 1)] >> ((n & 1) * 4)) & 0xfu;
+        const uint32_t sb = cm_sf[((int64_t)g * nsb + (j >> 4)) * N + n];
+        wv[i] = __fmul_rn(e2m1_value(c), __fmul_rn(e4m3_value(sb), s_dec));
+    }
+    const int64_t row = (int64_t)g * N + n;
+    BlockOut o = quantize16(wv, s_enc, s_dec);
+    *reinterpret_cast<uint2*>(codes + row * ld_codes + (K + 16 * b) / 2) = make_uint2(o.code_lo, o.code_hi);
+    sf[sf_offset(row, K / 16 + b, sf_cols)] = (uint8_t)o.sb;
+    if (b == 0)
+        for (int64_t c = (K + k) / 16; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
+}
+
+// Channel-major copy of the codes: CTA per (group, 64 rows, 128 channels) tile, transposed
+// through shared memory.  Out byte (g, j, m) packs channel j of rows 2m (low nibble) and 2m + 1.
+__global__ void __launch_bounds__(256) channel_major_codes_kernel(const uint8_t* __restrict__ codes, int64_t ld_codes,
+                                                                   int64_t N, int K, uint8_t* __restrict__ cm_codes)
+{
+    __shared__ uint8_t tile[64][64 + 4];  // 64 rows x 64 bytes (128 channels)
+    const int g = blockIdx.z;
+    const int64_t n0 = (int64_t)blockIdx.y * 64;
+    const int j0 = blockIdx.x * 128;
+    const int tid = threadIdx.x;
+    const int kb = K / 2;  // code bytes per row
+    // load: 64 rows x 4 words of 16 bytes
+    {
+        const int r = tid >> 2, q = tid & 3;
+        const int off = j0 / 2 + q * 16;
+        const uint8_t* src = codes + ((int64_t)g * N + n0 + r) * ld_codes + off;
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (off + 16 <= kb) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src);
+            w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+        } else {
+            for (int i = 0; i < 16 && off + i < kb; ++i) w[i >> 2] |= (uint32_t)src[i] << (8 * (i & 3));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) *reinterpret_cast<uint32_t*>(&tile[r][q * 16 + 4 * i]) = w[i];
+    }
+    __syncthreads();
+    // store: channel j = j0 + tid / 2, bytes [16 h, 16 h + 16) of its 32-byte row segment
+    const int jl = tid >> 1, h = tid & 1;
+    const int j = j0 + jl;
+    if (j >= K) return;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        const int ra = 2 * (16 * h + m);
+        const uint32_t lo = (tile[ra][jl >> 1] >> ((jl & 1) * 4)) & 0xfu;
+        const uint32_t hi = (tile[ra + 1][jl >> 1] >> ((jl & 1) * 4)) & 0xfu;
+        w[m >> 2] |= (lo | (hi << 4)) << (8 * (m & 3));
+    }
+    *reinterpret_cast<uint4*>(cm_codes + ((int64_t)g * K + j) * (N / 2) + n0 / 2 + 16 * h) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Channel-major copy of the block scales: out byte (g, block c, row n), n fastest.
+__global__ void __launch_bounds__(256) channel_major_sf_kernel(const uint8_t* __restrict__ sf, int64_t sf_cols, int64_t N,
+                                                                int nsb, int G, uint8_t* __restrict__ cm_sf)
+{
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= (int64_t)G * nsb * N) return;
+    const int64_t n = t % N;
+    const int64_t c = (t / N) % nsb;
+    const int64_t g = t / (N * nsb);
+    cm_sf[t] = sf[sf_offset(g * N + n, c, sf_cols)];
+}
+
 nvq_status weight_tail_impl(uint8_t* codes, int64_t ld_codes, uint8_t* sf, int64_t sf_cols, int64_t N, int K, int k,
                             int G, const nvq_tensor_scale* ts, const int32_t* idx, int idx_per_group, cudaStream_t st)
 {
@@ -299,11 +388,36 @@ extern "C" nvq_status rac_select_quantize(const void* x, int64_t rows, int64_t K
     return NVQ_OK;
 }
 
+extern "C" nvq_status nvfp4_channel_major(int32_t groups, int64_t N, int64_t K, const uint8_t* b_codes, int64_t ldb,
+                                          const uint8_t* b_sf, int64_t b_sf_cols, uint8_t* cm_codes, uint8_t* cm_sf,
+                                          void* stream)
+{
+    NVQ_CHECK_ARG(b_codes && b_sf && cm_codes && cm_sf, NVQ_ERR_ARG, "nvfp4_channel_major: null pointer argument");
+    NVQ_CHECK_ARG(groups >= 1 && groups <= 4096 && N >= 64 && N % 64 == 0 && (int64_t)groups * N <= (1ll << 24),
+                  NVQ_ERR_SHAPE, "nvfp4_channel_major: N must be a positive multiple of 64 and groups*N <= 2^24");
+    NVQ_CHECK_ARG(K >= 16 && K <= 8192 && K % 16 == 0, NVQ_ERR_SHAPE, "nvfp4_channel_major: K must be a multiple of 16 in [16, 8192]");
+    NVQ_CHECK_ARG(ldb % 16 == 0 && ldb >= K / 2 && aligned(b_codes, 16) && aligned(cm_codes, 16), NVQ_ERR_ALIGN,
+                  "nvfp4_channel_major: b_codes and cm_codes must be 16-byte aligned, ldb a multiple of 16");
+    NVQ_CHECK_ARG(b_sf_cols % 4 == 0 && b_sf_cols >= K / 16, NVQ_ERR_SHAPE, "nvfp4_channel_major: b_sf_cols too small");
+    set_error("");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const dim3 grid((unsigned)((K + 127) / 128), (unsigned)(N / 64), (unsigned)groups);
+    channel_major_codes_kernel<<<grid, 256, 0, st>>>(b_codes, ldb, N, (int)K, cm_codes);
+    NVQ_LAUNCH_CHECK("channel_major_codes_kernel");
+    const int64_t total = (int64_t)groups * (K / 16) * N;
+    channel_major_sf_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(b_sf, b_sf_cols, N, (int)(K / 16), groups, cm_sf);
+    NVQ_LAUNCH_CHECK("channel_major_sf_kernel");
+    return NVQ_OK;
+}
+
 extern "C" nvq_status rac_weight_tail(int32_t groups, int64_t N, int64_t K, int32_t k, const int32_t* idx,
                                       int32_t idx_per_group, uint8_t* b_codes, int64_t ldb, uint8_t* b_sf,
-                                      int64_t b_sf_cols, const nvq_tensor_scale* b_tscale, void* stream)
+                                      int64_t b_sf_cols, const nvq_tensor_scale* b_tscale, const uint8_t* cm_codes,
+                                      const uint8_t* cm_sf, void* stream)
 {
     NVQ_CHECK_ARG(idx && b_codes && b_sf && b_tscale, NVQ_ERR_ARG, "rac_weight_tail: null pointer argument");
+    NVQ_CHECK_ARG(!cm_codes == !cm_sf, NVQ_ERR_ARG, "rac_weight_tail: give both channel-major arrays or neither");
+    NVQ_CHECK_ARG(!cm_codes || N % 64 == 0, NVQ_ERR_SHAPE, "rac_weight_tail: the channel-major path needs N % 64 == 0");
     NVQ_CHECK_ARG(groups >= 1 && groups <= 4096 && N >= 1 && (int64_t)groups * N <= (1ll << 24), NVQ_ERR_SHAPE,
                   "rac_weight_tail: groups*N outside [1, 2^24]");
     NVQ_CHECK_ARG(K >= 16 && K <= 8192 && K % 16 == 0, NVQ_ERR_SHAPE, "rac_weight_tail: K must be a multiple of 16 in [16, 8192]");
@@ -312,6 +426,11 @@ extern "C" nvq_status rac_weight_tail(int32_t groups, int64_t N, int64_t K, int3
                   "rac_weight_tail: ldb must be a multiple of 16 covering (K+k)/2 bytes");
     NVQ_CHECK_ARG(b_sf_cols % 4 == 0 && b_sf_cols >= (K + k) / 16, NVQ_ERR_SHAPE, "rac_weight_tail: b_sf_cols too small");
     set_error("");
-    return weight_tail_impl(b_codes, ldb, b_sf, b_sf_cols, N, (int)K, k, groups, b_tscale, idx, idx_per_group,
-                            static_cast<cudaStream_t>(stream));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!cm_codes) return weight_tail_impl(b_codes, ldb, b_sf, b_sf_cols, N, (int)K, k, groups, b_tscale, idx, idx_per_group, st);
+    const int64_t total = (int64_t)groups * (k / 16) * N;
+    weight_tail_cm_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(b_codes, ldb, b_sf, b_sf_cols, N, (int)K, k, groups,
+                                                                           b_tscale, idx, idx_per_group, cm_codes, cm_sf);
+    NVQ_LAUNCH_CHECK("weight_tail_cm_kernel");
+    return NVQ_OK;
 }

@@ -45,6 +45,24 @@ class Operand:
         return Operand(codes, sf, cols, ts, rows, K, k_max)
 
 
+@dataclass
+class ChannelMajor:
+    """Channel-major copy of a quantized weight operand (nvfp4_channel_major), read by the
+    weight tail: codes [G, K, N/2] (rows 2m, 2m+1 of a channel in one byte), scales [G, K/16, N]."""
+    codes: torch.Tensor
+    sf: torch.Tensor
+
+    @staticmethod
+    def of(op: Operand, G: int, N: int, stream=None) -> Optional["ChannelMajor"]:
+        if N % 64:
+            return None
+        K = op.K
+        cm = ChannelMajor(torch.empty(G, K, N // 2, dtype=torch.uint8, device=op.codes.device),
+                          torch.empty(G, K // 16, N, dtype=torch.uint8, device=op.codes.device))
+        L.nvfp4_channel_major(G, N, K, op.codes, op.sf, op.sf_cols, cm.codes, cm.sf, stream=stream)
+        return cm
+
+
 def quantize_weights(w: torch.Tensor, k_max: int, w_hat: Optional[torch.Tensor] = None,
                      w_hat_dtype: int = L.NVQ_BF16) -> Operand:
     """W [G, N, K] (or [N, K]) bf16 -> NVFP4 operand with room for a k_max-column RAC tail."""
@@ -55,6 +73,12 @@ def quantize_weights(w: torch.Tensor, k_max: int, w_hat: Optional[torch.Tensor] 
     return op
 
 
+def _weight_tail(op: Operand, cm: Optional[ChannelMajor], G: int, N: int, k: int, idx: torch.Tensor,
+                 idx_per_group: bool = False, stream=None):
+    L.rac_weight_tail(G, N, op.K, k, idx, op.codes, op.sf, op.sf_cols, op.tscale, idx_per_group=idx_per_group,
+                      cm_codes=cm.codes if cm else None, cm_sf=cm.sf if cm else None, stream=stream)
+
+
 class RacLinear:
     """Dense rollout linear layer Y = X W^T with NVFP4 W4A4 + RAC (k compensated channels)."""
 
@@ -62,6 +86,7 @@ class RacLinear:
         self.N, self.K = w.shape
         self.k = k
         self.w = quantize_weights(w, k)
+        self.w_cm = ChannelMajor.of(self.w, 1, self.N) if k else None
         self.a = Operand.empty(max_rows, self.K, k, 1, device=w.device)
         self.scores = torch.zeros(self.K, dtype=torch.int64, device=w.device)
         self.idx = torch.zeros(max(k, 1), dtype=torch.int32, device=w.device)
@@ -74,8 +99,9 @@ class RacLinear:
         if k:
             L.rac_select_quantize(x, self.a.tscale, self.scores, k, self.a.codes, self.a.sf, self.a.sf_cols,
                                   self.idx, stream=stream)
+            _weight_tail(self.w, self.w_cm, 1, self.N, k, self.idx, stream=stream)
         L.w4a4_rac_grouped_gemm(self.a.codes, self.a.sf, self.a.sf_cols, self.a.tscale, self.w.codes, self.w.sf,
-                                self.w.sf_cols, self.w.tscale, self.N, self.K, k, self.idx if k else None, out,
+                                self.w.sf_cols, self.w.tscale, self.N, self.K, k, None, out,
                                 rows=M, stream=stream)
         return out
 
@@ -98,6 +124,8 @@ class MoERacLayer:
         self.k, self.topk, self.T = k, topk, max_tokens
         self.w13 = quantize_weights(w13, k)
         self.w2 = quantize_weights(w2, k)
+        self.w13_cm = ChannelMajor.of(self.w13, self.E, twoI) if k else None
+        self.w2_cm = ChannelMajor.of(self.w2, self.E, self.H) if k else None
         cap = L.moe_capacity(max_tokens, topk, self.E)
         self.cap = cap
         E = self.E
@@ -149,8 +177,7 @@ class MoERacLayer:
         L.nvfp4_gather_rows(self.a_tok.codes, self.a_tok.sf, self.a_tok.sf_cols, T, self.row_src, self.topk, H + k,
                             self.a_routed.codes, self.a_routed.sf, stream=stream)
         if k:
-            L.rac_weight_tail(E, 2 * I, H, k, self.idx1, self.w13.codes, self.w13.sf, self.w13.sf_cols,
-                              self.w13.tscale, stream=stream)
+            _weight_tail(self.w13, self.w13_cm, E, 2 * I, k, self.idx1, stream=stream)
         mark("gemm_gate_up", 0)
         L.w4a4_rac_grouped_gemm(self.a_routed.codes, self.a_routed.sf, self.a_routed.sf_cols, self.a_tok.tscale,
                                 self.w13.codes, self.w13.sf, self.w13.sf_cols, self.w13.tscale, 2 * I, H, k,
@@ -165,8 +192,7 @@ class MoERacLayer:
             L.rac_select_quantize(self.h, self.a2.tscale, self.scores2, k, self.a2.codes, self.a2.sf,
                                   self.a2.sf_cols, self.idx2, grp_off=self.grp_off, grp_rows=self.grp_rows,
                                   groups=E, stream=stream)
-            L.rac_weight_tail(E, H, I, k, self.idx2, self.w2.codes, self.w2.sf, self.w2.sf_cols, self.w2.tscale,
-                              idx_per_group=True, stream=stream)
+            _weight_tail(self.w2, self.w2_cm, E, H, k, self.idx2, idx_per_group=True, stream=stream)
         mark("gemm_down", 0)
         L.w4a4_rac_grouped_gemm(self.a2.codes, self.a2.sf, self.a2.sf_cols, self.a2.tscale, self.w2.codes,
                                 self.w2.sf, self.w2.sf_cols, self.w2.tscale, H, I, k, None,

@@ -234,3 +234,45 @@ def test_argument_errors_are_reported_before_launch(L):
                                         torch.zeros(32, dtype=torch.int64, device="cuda"), 8, codes, sf, 4,
                                         torch.zeros(8, dtype=torch.int32, device="cuda"))
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("G,N,K,k,per_group", [(3, 384, 272, 32, True), (1, 256, 2048, 64, False),
+                                               (2, 128, 16, 16, True), (4, 128, 1536, 48, True)])
+def test_weight_tail_channel_major_path(L, G, N, K, k, per_group):
+    """nvfp4_channel_major holds every code and scale of the weights at its channel-major place,
+    and rac_weight_tail from that copy writes the same bytes as the row-major path and the oracle
+    (ragged K: 272 = 17 blocks, 136 code bytes per row)."""
+    from nvfp4_w4a4_quantized_quantize_gb300.layers import ChannelMajor, quantize_weights
+    w = wl.weights((G, N, K), 0.02, seed=G + N + K + k)
+    op = quantize_weights(bf16_tensor(w.reshape(G * N, K)).view(G, N, K), k)
+    cm = ChannelMajor.of(op, G, N)
+    rng = np.random.default_rng(K + k)
+    idx_np = np.stack([np.sort(rng.choice(K, k, replace=False)) for _ in range(G if per_group else 1)]).astype(np.int32)
+    idx = torch.from_numpy(idx_np).cuda()
+    codes_rm, sf_rm = op.codes.clone(), op.sf.clone()
+    L.rac_weight_tail(G, N, K, k, idx, codes_rm, sf_rm, op.sf_cols, op.tscale, idx_per_group=per_group)
+    codes_cm, sf_cm = op.codes.clone(), op.sf.clone()
+    L.rac_weight_tail(G, N, K, k, idx, codes_cm, sf_cm, op.sf_cols, op.tscale, idx_per_group=per_group,
+                      cm_codes=cm.codes, cm_sf=cm.sf)
+    torch.cuda.synchronize()
+    assert L.device_status() == (0, 0)
+    # the copy: byte (g, j, m) = channel j of rows 2m | 2m+1; scale (g, c, n)
+    c = op.codes.cpu().numpy()[:, :K // 2]
+    nib = np.empty((G * N, K), np.uint8)
+    nib[:, 0::2], nib[:, 1::2] = c & 0xF, c >> 4
+    nib = nib.reshape(G, N, K).transpose(0, 2, 1)  # [G, K, N]
+    assert np.array_equal(cm.codes.cpu().numpy(), nib[:, :, 0::2] | (nib[:, :, 1::2] << 4))
+    sfl = unswizzle(op.sf, G * N, K // 16, op.sf_cols).reshape(G, N, K // 16).transpose(0, 2, 1)
+    assert np.array_equal(cm.sf.cpu().numpy(), sfl)
+    # both tail paths agree byte for byte, and with the oracle
+    assert torch.equal(codes_rm, codes_cm) and torch.equal(sf_rm, sf_cm)
+    tc_all = codes_cm.cpu().numpy()
+    tsc_all = unswizzle(sf_cm, G * N, op.sf_cols, op.sf_cols)
+    for g in range(G):
+        wts = oracle.tensor_scale(w[g])
+        wc, ws = oracle.quantize(w[g], wts)
+        tc, tsc = oracle.weight_tail(wc, ws, wts, idx_np[g if per_group else 0])
+        rows = slice(g * N, (g + 1) * N)
+        assert np.array_equal(tc_all[rows, K // 2:(K + k) // 2], tc)
+        assert np.array_equal(tsc_all[rows, K // 16:(K + k) // 16], tsc)
+        assert not tsc_all[rows, (K + k) // 16:].any()
