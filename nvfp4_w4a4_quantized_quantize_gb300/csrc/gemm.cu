@@ -5,15 +5,24 @@
 // Y[r, n] = alpha_g * sum_{c < K+k} V[a_rc] sa_{r,c/16} V[b_nc] sb_{n,c/16},
 // alpha_g = S_dec(A_g) * S_dec(W_g), for the rows r of group g and the weight rows of group g.
 //
-// sm_103a design (one CTA per SM, persistent):
-//   tile 128 x 256 x 256 (M x N x K-tile of FP4 elements = 128 bytes per row);
+// sm_103a design (one CTA per SM, persistent, clusters of two CTAs):
+//   tile 128 x 256 x 256 (M x N x K-tile of FP4 elements = 128 bytes per row) per CTA; the two
+//   CTAs of a cluster take adjacent 128-row tiles of the same group and the same N tile, so
+//   they need the same weight tile: each loads one 128-row half of it (and of its scales)
+//   and multicasts it into both CTAs' shared memory.  That cuts the L2-to-SM traffic per
+//   MMA by a third, the limit of the single-CTA kernel;
 //   warp 0     TMA producer: A and B code tiles by cp.async.bulk.tensor (128-byte swizzle,
 //              out-of-range columns zero-filled), scale atoms by cp.async.bulk (the blocked
 //              scale layout makes every 128-row x 64-column scale tile one contiguous 512 B);
-//   warp 1     TMEM allocator and MMA issuer: per K-tile, tcgen05.cp of the scale atoms into
-//              TMEM, then tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (K = 64 each,
-//              UE4M3 scales, FP32 accumulation in TMEM), tcgen05.commit to free the stage;
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator, alpha scaling, bf16 store, with the
+//   warp 1     TMEM allocator and MMA issuer: per K-tile, once the stage's scales are in
+//              TMEM, tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (K = 64 each, UE4M3
+//              scales, FP32 accumulation in TMEM), tcgen05.commit to free the stage;
+//   warps 2-5  scale staging, one warp per TMEM lane quarter: the stage's scale atoms from
+//              shared memory into registers and into TMEM with tcgen05.st (the layout the
+//              block-scaled MMA reads: every lane quarter holds each atom's 32 x 16 bytes).
+//              Register stores keep the scales off the tensor pipe's copy path, which at
+//              12 small copies per K-tile cost about 40% of the MMA rate;
+//   warps 6-13 epilogue: tcgen05.ld of the accumulator, alpha scaling, bf16 store, with the
 //              SwiGLU or routing-weight variants.
 // Every mbarrier wait is bounded; on expiry the kernel records NVQ_ERR_TIMEOUT and unwinds.
 #include <cuda.h>
@@ -32,9 +41,11 @@ constexpr int kSFABytes = kBM * kBK / 16;  // 2048: 4 atoms of 512 B
 constexpr int kSFBBytes = kBN * kBK / 16;  // 4096: 2 row blocks x 4 atoms
 constexpr int kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;  // 55296 (54 x 1024)
 constexpr int kSmemBytes = kStages * kStageBytes + 1024;
-constexpr int kThreads = 352;  // warp 0 TMA, warp 1 MMA, warp 2 scale copies, warps 3-10 epilogue
+constexpr int kThreads = 448;  // warp 0 TMA, warp 1 MMA, warps 2-5 scale staging, warps 6-13 epilogue
+constexpr int kFirstEpiWarp = 6;
 constexpr int kEpiThreads = 256;
 constexpr int kMaxGroups = 512;
+constexpr int kCluster = 2;  // CTAs sharing one weight tile by multicast
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;                  // 256 fp32 columns
 constexpr uint32_t kSFCol = 256;                 // + stage * 48: SFA 16 columns, SFB 32 columns
@@ -136,6 +147,39 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar)
                  : "memory");
 }
 
+// Commit that arrives on the barrier at the same offset in both CTAs of the cluster.
+__device__ __forceinline__ void tc_commit_both(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                     smem_u32(bar)),
+                 "h"((uint16_t)0x3)
+                 : "memory");
+}
+
+// Weight tile half and scale atoms into the same offset of both CTAs' shared memory; each
+// destination's barrier at the same offset receives the byte count.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"((uint16_t)0x3), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_load_mc(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], %4;" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar)), "h"((uint16_t)0x3)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor (tcgen05 format): start >> 4, LBO >> 4, SBO >> 4, version 1,
 // layout type in bits 61-63 (0 = no swizzle, 2 = 128-byte swizzle).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout)
@@ -159,35 +203,15 @@ __device__ __forceinline__ void mma_fp4(uint32_t d_tmem, uint64_t a_desc, uint64
         : "memory");
 }
 
-__device__ __forceinline__ void tc_cp_sf(uint32_t tmem, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem), "l"(sdesc) : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v)
-{
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 64 consecutive accumulator columns of this thread's TMEM lane (one load, then the wait).
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v)
+// Two 32-column accumulator loads, one wait.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float* va, float* vb)
 {
     uint32_t r[64];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,"
-        "%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
         "tcgen05.wait::ld.sync.aligned;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
@@ -197,10 +221,35 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v)
           "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
           "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
           "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-        : "r"(taddr)
+        : "r"(ta), "r"(tb)
         : "memory");
 #pragma unroll
-    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 32; ++i) {
+        va[i] = __uint_as_float(r[i]);
+        vb[i] = __uint_as_float(r[32 + i]);
+    }
+}
+
+// 16 / 32 consecutive TMEM columns of this warp's 32 lanes from registers.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+        "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+        "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
 }
 
 // n32 consecutive 32-byte pieces of packed words to global memory: 256-bit stores when the
@@ -244,35 +293,38 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v
 // ------------------------------------------------------------------ tile scheduling
 struct Tile {
     int g;
-    int row0;       // first A row of the tile (rows < 2^24)
-    int rows;       // valid rows in the tile (<= 128)
+    int row0;       // first A row of this CTA's 128-row tile (rows < 2^24)
+    int rows;       // valid rows in the tile (0..128; 0: the group has no second tile here)
+    int lrow0;      // first A row loaded (row0, or the pair's first tile when rows == 0)
     int nt;         // N tile
 };
 
 // Per-group tables in shared memory, filled once per CTA: first row, row count and the prefix
-// of 128-row tiles.  Tiles run N-fastest inside each 128-row block so that the CTAs working at
-// the same time share one A tile (read from HBM once) and one group's weights (kept in L2).
+// of 256-row tile pairs (one pair per cluster).  Pairs run N-fastest inside each 256-row block
+// so that the clusters working at the same time share one A block (read from HBM once) and one
+// group's weights (kept in L2).
 struct GroupTab {
     int start[kMaxGroups];
     int rows[kMaxGroups];
     int mt_pre[kMaxGroups + 1];
 };
 
-__device__ __forceinline__ Tile tile_of(int64_t t, int n_tiles, const GroupTab& tab, int G)
+__device__ __forceinline__ Tile tile_of(int64_t t, int n_tiles, const GroupTab& tab, int G, int rank)
 {
     Tile T;
     T.nt = (int)(t % n_tiles);
-    const int gm = (int)(t / n_tiles);
+    const int gp = (int)(t / n_tiles);
     int lo = 0, hi = G - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (tab.mt_pre[mid] <= gm) lo = mid; else hi = mid - 1;
+        if (tab.mt_pre[mid] <= gp) lo = mid; else hi = mid - 1;
     }
     T.g = lo;
-    const int mt = gm - tab.mt_pre[lo];
+    const int mt = kCluster * (gp - tab.mt_pre[lo]) + rank;
     T.row0 = tab.start[lo] + mt * kBM;
     const int left = tab.rows[lo] - mt * kBM;
-    T.rows = left < kBM ? left : kBM;
+    T.rows = left <= 0 ? 0 : (left < kBM ? left : kBM);
+    T.lrow0 = T.rows > 0 ? T.row0 : tab.start[lo] + (mt - rank) * kBM;
     return T;
 }
 
@@ -291,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                                                            const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[kStages], sf_bar[kStages], empty_bar[kStages], acc_full, acc_empty, drain_bar, drain_sf;
+    __shared__ __align__(8) uint64_t full_bar[kStages], sf_bar[kStages], empty_bar[kStages], acc_full, acc_empty, drain_bar;
     __shared__ uint32_t tmem_base_slot;
     __shared__ GroupTab tab;
     __shared__ int abort_flag;
@@ -299,6 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = a.gr.G;
+    uint32_t rank;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    const int64_t cluster_id = blockIdx.x / kCluster, n_clusters = gridDim.x / kCluster;
 
     // per-group tables: rows and starts in parallel, the tile prefix by warp 0
     for (int g = threadIdx.x; g < G; g += kThreads) {
@@ -311,13 +366,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         abort_flag = 0;
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&full_bar[i], 1);
-            mbar_init(&sf_bar[i], 1);
-            mbar_init(&empty_bar[i], 1);
+            mbar_init(&sf_bar[i], 4);  // the four scale-staging warps
+            mbar_init(&empty_bar[i], kCluster);  // both CTAs' MMAs release a stage
         }
         mbar_init(&acc_full, 1);
         mbar_init(&acc_empty, kEpiThreads);
         mbar_init(&drain_bar, 1);
-        mbar_init(&drain_sf, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -328,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
         for (int i = 0; i < kPer; ++i) {
             const int g = lane * kPer + i;
-            cnt[i] = g < G ? (tab.rows[g] + kBM - 1) / kBM : 0;
+            cnt[i] = g < G ? ((tab.rows[g] + kBM - 1) / kBM + kCluster - 1) / kCluster : 0;
             sum += cnt[i];
         }
         int incl = sum;
@@ -353,6 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();  // the peer's barriers are initialised before any multicast reaches them
     tc_fence_after();
     const uint32_t tmem = tmem_base_slot;
     const int total_mtiles = tab.mt_pre[G];
@@ -368,8 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
         int stage = 0;
         uint32_t phase = 0, issued = 0;
-        for (int64_t t = blockIdx.x; t < total_tiles && !*abrt; t += gridDim.x) {
-            const Tile T = tile_of(t, n_tiles, tab, G);
+        for (int64_t t = cluster_id; t < total_tiles && !*abrt; t += n_clusters) {
+            const Tile T = tile_of(t, n_tiles, tab, G, (int)rank);
             int64_t brow0, brow1;
             if (a.epilogue == NVQ_EPI_SWIGLU) {
                 brow0 = (int64_t)T.g * a.N + (int64_t)T.nt * (kBN / 2);
@@ -388,15 +443,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     uint8_t* sSFA = sB + kBBytes;
                     uint8_t* sSFB = sSFA + kSFABytes;
                     mbar_expect_tx(&full_bar[stage], kABytes + kBBytes + 3u * 512u * n_atoms);
-                    tma_load_2d(sA, &tmap_a, kt * (kBK / 2), T.row0, &full_bar[stage]);
-                    tma_load_2d_hint(sB, &tmap_b, kt * (kBK / 2), (int)brow0, &full_bar[stage], pol_keep);
-                    tma_load_2d_hint(sB + kBBytes / 2, &tmap_b, kt * (kBK / 2), (int)brow1, &full_bar[stage], pol_keep);
-                    const uint8_t* srcA = a.a_sf + ((int64_t)(T.row0 >> 7) * (a.a_sf_cols >> 2) + kt * 4) * 512;
+                    // own A tile and scales; this CTA's half of the weight tile and its scales
+                    // into both CTAs (the peer sends the other half)
+                    tma_load_2d(sA, &tmap_a, kt * (kBK / 2), T.lrow0, &full_bar[stage]);
+                    const int64_t brow = rank ? brow1 : brow0;
+                    tma_load_2d_mc(sB + rank * (kBBytes / 2), &tmap_b, kt * (kBK / 2), (int)brow, &full_bar[stage], pol_keep);
+                    const uint8_t* srcA = a.a_sf + ((int64_t)(T.lrow0 >> 7) * (a.a_sf_cols >> 2) + kt * 4) * 512;
                     bulk_load(sSFA, srcA, 512u * n_atoms, &full_bar[stage]);
-                    const uint8_t* srcB0 = a.b_sf + ((brow0 >> 7) * (a.b_sf_cols >> 2) + kt * 4) * 512;
-                    const uint8_t* srcB1 = a.b_sf + ((brow1 >> 7) * (a.b_sf_cols >> 2) + kt * 4) * 512;
-                    bulk_load(sSFB, srcB0, 512u * n_atoms, &full_bar[stage]);
-                    bulk_load(sSFB + kSFBBytes / 2, srcB1, 512u * n_atoms, &full_bar[stage]);
+                    const uint8_t* srcB = a.b_sf + ((brow >> 7) * (a.b_sf_cols >> 2) + kt * 4) * 512;
+                    bulk_load_mc(sSFB + rank * (kSFBBytes / 2), srcB, 512u * n_atoms, &full_bar[stage]);
                     ++issued;
                     if (++stage == kStages) { stage = 0; phase ^= 1; }
                 }
@@ -420,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         int stage = 0;
         uint32_t phase = 0, acc_phase = 0;
         bool issued_any = false;
-        for (int64_t t = blockIdx.x; t < total_tiles && !*abrt; t += gridDim.x) {
+        for (int64_t t = cluster_id; t < total_tiles && !*abrt; t += n_clusters) {
             if (!mbar_wait(&acc_empty, acc_phase ^ 1, a, abrt, 2)) break;
             tc_fence_after();
             bool ok = true;
@@ -438,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     if (n_mma > 1) mma_fp4(tmem + kAccCol, a_desc0 + so + 2, b_desc0 + so + 2, sfa_t + 4, sfb_t + 8, 1u);
                     if (n_mma > 2) mma_fp4(tmem + kAccCol, a_desc0 + so + 4, b_desc0 + so + 4, sfa_t + 8, sfb_t + 16, 1u);
                     if (n_mma > 3) mma_fp4(tmem + kAccCol, a_desc0 + so + 6, b_desc0 + so + 6, sfa_t + 12, sfb_t + 24, 1u);
-                    tc_commit(&empty_bar[stage]);
+                    tc_commit_both(&empty_bar[stage]);  // the stage also holds the peer's weight half
                     issued_any = true;
                 }
                 __syncwarp();
@@ -454,58 +509,54 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             mbar_wait(&drain_bar, 0, a, abrt, 12, true);
         }
         __syncwarp();
-    } else if (warp == 2) {
-        // ---------------- scale-factor copies: per K-tile, 12 tcgen05.cp of the stage's scale
-        // atoms into the stage's own TMEM columns, committed to sf_bar.  Issued apart from the
-        // MMA thread so that they overlap the MMAs instead of stalling their issue.
-        const uint32_t base = smem_u32(smem);
-        const uint64_t sfa_desc0 = smem_desc(base + kABytes + kBBytes, 0, 128, 0);
-        const uint64_t sfb_desc0 = smem_desc(base + kABytes + kBBytes + kSFABytes, 0, 128, 0);
-        constexpr uint64_t kStageStep = kStageBytes >> 4;
+    } else if (warp < kFirstEpiWarp) {
+        // ---------------- scale staging (warps 2-5, TMEM lane quarter = warp % 4): per K-tile,
+        // lane i loads row i (16 bytes) of each of the stage's 12 scale atoms from shared memory
+        // and stores them to its TMEM lane, SFA atom j at columns 4j, SFB atom j of weight half
+        // h at 16 + 8j + 4h; then fence and arrive on sf_bar for the MMA warp.
+        const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
         int stage = 0;
         uint32_t phase = 0;
-        bool issued_any = false;
-        for (int64_t t = blockIdx.x; t < total_tiles && !*abrt; t += gridDim.x) {
+        for (int64_t t = cluster_id; t < total_tiles && !*abrt; t += n_clusters) {
             bool ok = true;
             for (int kt = 0; kt < num_kt; ++kt) {
                 if (!mbar_wait(&full_bar[stage], phase, a, abrt, 5)) { ok = false; break; }
-                tc_fence_after();
-                const int kleft = a.ktot - kt * kBK;
-                const int n_mma = kleft >= kBK ? 4 : (kleft + 63) / 64;
-                if (lane == 0) {
-                    const uint64_t so = (uint64_t)stage * kStageStep;
-                    const uint32_t sfa_t = tmem + kSFCol + stage * kSFColsPerStage;
-                    const uint32_t sfb_t = sfa_t + 16;
-                    for (int j = 0; j < n_mma; ++j) {
-                        tc_cp_sf(sfa_t + 4 * j, sfa_desc0 + so + 32 * j);
-                        tc_cp_sf(sfb_t + 8 * j, sfb_desc0 + so + 32 * j);
-                        tc_cp_sf(sfb_t + 8 * j + 4, sfb_desc0 + so + 128 + 32 * j);
+                const uint8_t* sf = smem + stage * kStageBytes + kABytes + kBBytes + lane * 16;
+                uint32_t va[16], vb[32];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 x = *reinterpret_cast<const uint4*>(sf + j * 512);
+                    va[4 * j] = x.x; va[4 * j + 1] = x.y; va[4 * j + 2] = x.z; va[4 * j + 3] = x.w;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 y = *reinterpret_cast<const uint4*>(sf + kSFABytes + h * (kSFBBytes / 2) + j * 512);
+                        vb[8 * j + 4 * h] = y.x; vb[8 * j + 4 * h + 1] = y.y; vb[8 * j + 4 * h + 2] = y.z; vb[8 * j + 4 * h + 3] = y.w;
                     }
-                    tc_commit(&sf_bar[stage]);
-                    issued_any = true;
                 }
+                const uint32_t sfa_t = tmem + kSFCol + stage * kSFColsPerStage + lane_addr;
+                tmem_st16(sfa_t, va);
+                tmem_st32(sfa_t + 16, vb);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
                 __syncwarp();
+                if (lane == 0) mbar_arrive(&sf_bar[stage]);
                 if (++stage == kStages) { stage = 0; phase ^= 1; }
             }
             if (!ok) break;
         }
-        if (*abrt && issued_any && lane == 0) {
-            tc_commit(&drain_sf);
-            mbar_wait(&drain_sf, 0, a, abrt, 13, true);
-        }
-        __syncwarp();
     } else {
-        // ---------------- epilogue: warps 3..10; TMEM lane quarter = warp % 4, column half =
-        // (warp - 3) / 4.  The accumulator is read into registers and released at once; the
-        // scaling, conversion and global stores overlap the next tile's MMAs.
+        // ---------------- epilogue: warps 6..13; TMEM lane quarter = warp % 4, column half =
+        // (warp - 6) / 4.  The accumulator is read in 32-column pieces, packed to bf16 as it
+        // comes, and released after the last piece; the global stores overlap the next tile's
+        // MMAs.
         const int quarter = warp & 3;
-        const int half = (warp - 3) >> 2;
+        const int half = (warp - kFirstEpiWarp) >> 2;
         const int r_in_tile = quarter * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const bool wide = (a.ldo % 16) == 0 && (reinterpret_cast<uintptr_t>(a.out) % 32) == 0;
         uint32_t acc_phase = 0;
-        for (int64_t t = blockIdx.x; t < total_tiles && !*abrt; t += gridDim.x) {
-            const Tile T = tile_of(t, n_tiles, tab, G);
+        for (int64_t t = cluster_id; t < total_tiles && !*abrt; t += n_clusters) {
+            const Tile T = tile_of(t, n_tiles, tab, G, (int)rank);
             const bool valid = r_in_tile < T.rows;
             const int64_t grow = (int64_t)T.row0 + r_in_tile;
             const float alpha = __fmul_rn(a.a_ts[a.a_ts_per_group ? T.g : 0].s_dec, a.b_ts[T.g].s_dec);
@@ -514,54 +565,61 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             tc_fence_after();
             const uint32_t tacc = tmem + kAccCol + lane_addr;
             if (a.epilogue == NVQ_EPI_STORE_F32) {
-                float v[64];
                 float* orow = reinterpret_cast<float*>(a.out) + grow * a.ldo + (int64_t)T.nt * kBN + half * (kBN / 2);
 #pragma unroll 1
                 for (int c = 0; c < kBN / 2; c += 64) {
-                    tmem_ld64(tacc + half * (kBN / 2) + c, v);
+                    float v0[32], v1[32];
+                    tmem_ld32x2(tacc + half * (kBN / 2) + c, tacc + half * (kBN / 2) + c + 32, v0, v1);
                     if (valid) {
                         float4* d = reinterpret_cast<float4*>(orow + c);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            d[i] = make_float4(__fmul_rn(alpha, v[4 * i]), __fmul_rn(alpha, v[4 * i + 1]),
-                                               __fmul_rn(alpha, v[4 * i + 2]), __fmul_rn(alpha, v[4 * i + 3]));
+                        for (int i = 0; i < 8; ++i) {
+                            d[i] = make_float4(__fmul_rn(alpha, v0[4 * i]), __fmul_rn(alpha, v0[4 * i + 1]),
+                                               __fmul_rn(alpha, v0[4 * i + 2]), __fmul_rn(alpha, v0[4 * i + 3]));
+                            d[8 + i] = make_float4(__fmul_rn(alpha, v1[4 * i]), __fmul_rn(alpha, v1[4 * i + 1]),
+                                                   __fmul_rn(alpha, v1[4 * i + 2]), __fmul_rn(alpha, v1[4 * i + 3]));
+                        }
                     }
                 }
                 tc_fence_before();
                 mbar_arrive(&acc_empty);
             } else if (a.epilogue == NVQ_EPI_SWIGLU) {
                 // gate columns [half*64, +64), up columns [128 + half*64, +64) -> h columns [half*64, +64)
-                float g[64], u[64];
-                tmem_ld64(tacc + half * 64, g);
-                tmem_ld64(tacc + kBN / 2 + half * 64, u);
-                tc_fence_before();
-                mbar_arrive(&acc_empty);
                 uint32_t pk[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float g0 = __fmul_rn(alpha, g[2 * i]), u0 = __fmul_rn(alpha, u[2 * i]);
-                    const float g1 = __fmul_rn(alpha, g[2 * i + 1]), u1 = __fmul_rn(alpha, u[2 * i + 1]);
-                    pk[i] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u0, __fdividef(g1, 1.0f + __expf(-g1)) * u1);
+                for (int c = 0; c < 2; ++c) {
+                    float g[32], u[32];
+                    tmem_ld32x2(tacc + half * 64 + 32 * c, tacc + kBN / 2 + half * 64 + 32 * c, g, u);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float g0 = __fmul_rn(alpha, g[2 * i]), u0 = __fmul_rn(alpha, u[2 * i]);
+                        const float g1 = __fmul_rn(alpha, g[2 * i + 1]), u1 = __fmul_rn(alpha, u[2 * i + 1]);
+                        pk[16 * c + i] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u0, __fdividef(g1, 1.0f + __expf(-g1)) * u1);
+                    }
                 }
-                if (valid) store_row<32>(a.out + grow * a.ldo + (int64_t)T.nt * (kBN / 2) + half * 64, pk, wide);
-            } else {
-                float v0[64], v1[64];
-                tmem_ld64(tacc + half * (kBN / 2), v0);
-                tmem_ld64(tacc + half * (kBN / 2) + 64, v1);
                 tc_fence_before();
                 mbar_arrive(&acc_empty);
+                if (valid) store_row<32>(a.out + grow * a.ldo + (int64_t)T.nt * (kBN / 2) + half * 64, pk, wide);
+            } else {
                 const float sc = (a.epilogue == NVQ_EPI_ROW_SCALE) ? w : 1.0f;
                 uint32_t pk[64];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float y0 = __fmul_rn(alpha, v0[2 * i]), y1 = __fmul_rn(alpha, v0[2 * i + 1]);
-                    float z0 = __fmul_rn(alpha, v1[2 * i]), z1 = __fmul_rn(alpha, v1[2 * i + 1]);
-                    if (a.epilogue == NVQ_EPI_ROW_SCALE) {
-                        y0 = __fmul_rn(y0, sc); y1 = __fmul_rn(y1, sc); z0 = __fmul_rn(z0, sc); z1 = __fmul_rn(z1, sc);
+                for (int c = 0; c < 2; ++c) {
+                    float v0[32], v1[32];
+                    tmem_ld32x2(tacc + half * (kBN / 2) + 64 * c, tacc + half * (kBN / 2) + 64 * c + 32, v0, v1);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float y0 = __fmul_rn(alpha, v0[2 * i]), y1 = __fmul_rn(alpha, v0[2 * i + 1]);
+                        float z0 = __fmul_rn(alpha, v1[2 * i]), z1 = __fmul_rn(alpha, v1[2 * i + 1]);
+                        if (a.epilogue == NVQ_EPI_ROW_SCALE) {
+                            y0 = __fmul_rn(y0, sc); y1 = __fmul_rn(y1, sc); z0 = __fmul_rn(z0, sc); z1 = __fmul_rn(z1, sc);
+                        }
+                        pk[32 * c + i] = pack_bf16x2(y0, y1);
+                        pk[32 * c + 16 + i] = pack_bf16x2(z0, z1);
                     }
-                    pk[i] = pack_bf16x2(y0, y1);
-                    pk[32 + i] = pack_bf16x2(z0, z1);
                 }
+                tc_fence_before();
+                mbar_arrive(&acc_empty);
                 if (valid) store_row<64>(a.out + grow * a.ldo + (int64_t)T.nt * kBN + half * (kBN / 2), pk, wide);
             }
             acc_phase ^= 1;
@@ -570,6 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();  // no multicast of the peer still targets this CTA's shared memory
     tc_fence_after();
     if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
@@ -681,11 +740,29 @@ extern "C" nvq_status w4a4_rac_grouped_gemm(int32_t groups, const int64_t* grp_o
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t max_tiles = (int64_t)(ga.total_mtiles_max + groups) * (N / kBN);
-    const int grid = (int)(max_tiles < sms ? max_tiles : sms);
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(gemm_kernel)");
-    gemm_kernel<<<grid, kThreads, kSmemBytes, st>>>(ma, mb, ga);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // one cluster per SM pair that can hold one at a time (persistent), no more than the work
+    cfg.gridDim = dim3((unsigned)sms);
+    int max_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, gemm_kernel, &cfg) != cudaSuccess || max_clusters < 1)
+        max_clusters = sms / kCluster;
+    const int64_t max_pairs = (int64_t)(ga.total_mtiles_max / kCluster + 1 + groups) * (N / kBN);
+    const int clusters = (int)(max_pairs < max_clusters ? max_pairs : max_clusters);
+    cfg.gridDim = dim3((unsigned)(clusters * kCluster));
+    e = cudaLaunchKernelEx(&cfg, gemm_kernel, ma, mb, ga);
+    if (e != cudaSuccess) return cuda_status(e, "cudaLaunchKernelEx(gemm_kernel)");
     NVQ_LAUNCH_CHECK("gemm_kernel");
     return NVQ_OK;
 }
