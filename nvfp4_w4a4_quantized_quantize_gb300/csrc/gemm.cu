@@ -152,7 +152,7 @@ __device__ __forceinline__ void tc_commit_both(uint64_t* bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
                      smem_u32(bar)),
-                 "h"((uint16_t)0x3)
+                 "h"((uint16_t)((1u << kCluster) - 1u))
                  : "memory");
 }
 
@@ -163,7 +163,7 @@ __device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
         " [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"((uint16_t)0x3), "l"(policy)
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"((uint16_t)((1u << kCluster) - 1u)), "l"(policy)
         : "memory");
 }
 
@@ -171,7 +171,7 @@ __device__ __forceinline__ void bulk_load_mc(void* dst, const void* src, uint32_
 {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], %4;" ::"r"(
                      smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar)), "h"((uint16_t)0x3)
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar)), "h"((uint16_t)((1u << kCluster) - 1u))
                  : "memory");
 }
 
@@ -443,15 +443,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     uint8_t* sSFA = sB + kBBytes;
                     uint8_t* sSFB = sSFA + kSFABytes;
                     mbar_expect_tx(&full_bar[stage], kABytes + kBBytes + 3u * 512u * n_atoms);
-                    // own A tile and scales; this CTA's half of the weight tile and its scales
-                    // into both CTAs (the peer sends the other half)
+                    // own A tile and scales; this CTA's halves of the weight tile and their scales
+                    // into every CTA of the cluster (the peer sends the other half)
                     tma_load_2d(sA, &tmap_a, kt * (kBK / 2), T.lrow0, &full_bar[stage]);
-                    const int64_t brow = rank ? brow1 : brow0;
-                    tma_load_2d_mc(sB + rank * (kBBytes / 2), &tmap_b, kt * (kBK / 2), (int)brow, &full_bar[stage], pol_keep);
                     const uint8_t* srcA = a.a_sf + ((int64_t)(T.lrow0 >> 7) * (a.a_sf_cols >> 2) + kt * 4) * 512;
                     bulk_load(sSFA, srcA, 512u * n_atoms, &full_bar[stage]);
-                    const uint8_t* srcB = a.b_sf + ((brow >> 7) * (a.b_sf_cols >> 2) + kt * 4) * 512;
-                    bulk_load_mc(sSFB + rank * (kSFBBytes / 2), srcB, 512u * n_atoms, &full_bar[stage]);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (h % kCluster != (int)rank) continue;
+                        const int64_t brow = h ? brow1 : brow0;
+                        tma_load_2d_mc(sB + h * (kBBytes / 2), &tmap_b, kt * (kBK / 2), (int)brow, &full_bar[stage], pol_keep);
+                        const uint8_t* srcB = a.b_sf + ((brow >> 7) * (a.b_sf_cols >> 2) + kt * 4) * 512;
+                        bulk_load_mc(sSFB + h * (kSFBBytes / 2), srcB, 512u * n_atoms, &full_bar[stage]);
+                    }
                     ++issued;
                     if (++stage == kStages) { stage = 0; phase ^= 1; }
                 }
