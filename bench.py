@@ -46,14 +46,17 @@ def _peaks():
 
 
 # ----------------------------------------------------------------------------- distributed
-def dist_setup():
+def dist_setup(backend=None):
+    """One process per GPU (torchrun): rank, world size and local rank from the environment;
+    NCCL when CUDA is available, else gloo (host-side tests)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch
         import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend is None:
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
         if backend == "nccl":
             torch.cuda.set_device(local)
         dist.init_process_group(backend=backend)
@@ -77,9 +80,15 @@ def max_over_ranks(value: float, world: int) -> float:
     return float(t.item())
 
 
+def job_throughput(units_per_rank_step: float, world: int, max_ms_per_step: float) -> float:
+    """Whole-job rate under weak scaling: every rank processes its own batch of units per step,
+    and the job's step time is the slowest rank's."""
+    return units_per_rank_step * world / (max_ms_per_step * 1e-3)
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi sampling (every 200 ms) over the timed region."""
+    """nvidia-smi sampling (every 50 ms) over the timed region."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -95,7 +104,7 @@ class ClockSampler:
         os.close(fd)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -255,7 +264,7 @@ def run_ours(args, world, rank, local):
     peaks, src = _peaks()
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
     ach_gu = flop_gu / (t_gu * 1e-3) / 1e12
-    tokens_per_s = T * world / (ms_per_step * 1e-3)
+    tokens_per_s = job_throughput(T, world, ms_per_step)
 
     # ---- end-to-end through the same API with host buffers (H2D inputs, D2H output each step)
     x_h = torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -282,7 +291,7 @@ def run_ours(args, world, rank, local):
     # the result read back to the host is the layer output itself
     assert torch.equal(out_h.view(torch.int16), out.cpu().view(torch.int16))
     e2e_tot = max_over_ranks(sum(e2e_ms), world)
-    e2e_tps = T * world / (e2e_tot / len(e2e_ms) * 1e-3)
+    e2e_tps = job_throughput(T, world, e2e_tot / len(e2e_ms))
     st, where = L.device_status()
     if st != 0:
         raise RuntimeError(f"device wait ran out ({where}) in the timed region")
@@ -424,7 +433,7 @@ def oracle_setup(tokens, ids, w13_bits, w2_bits):
     return w_q13, w_q2
 
 
-def cpu_baseline(inputs, n_tokens=6):
+def cpu_baseline(inputs, n_tokens=12):
     x_bits, ids, tw, w13_bits, w2_bits, cfg = inputs
     tokens = np.arange(n_tokens)
     w_q13, w_q2 = oracle_setup(tokens, ids, w13_bits, w2_bits)
@@ -509,7 +518,7 @@ def profile_case(name: str):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=200)  # ~0.25 s timed: several clock samples
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
