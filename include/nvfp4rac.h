@@ -122,7 +122,10 @@ int64_t nvq_sf_offset(int64_t row, int64_t col, int64_t sf_cols);
  *   sf        blocked scales with sf_cols columns (sf_cols % 4 == 0, >= K / 16); columns
  *             [0, K / 16) written; if zero_pad is non-zero, columns [K / 16, sf_cols) are
  *             zeroed as well (use it when no RAC tail follows).
- *   tscale    [groups] out.
+ *   tscale    [groups] out.  With amax_given non-zero, tscale[g].amax must already hold the
+ *             group's max |x| (as w4a4_rac_grouped_gemm's out_tscale leaves it for the tensor
+ *             it writes) and the pass that measures it is skipped; the other fields are
+ *             written from it.
  *   scores    NULL, or uint64 [groups][K] out: score_j = sum over the group's rows of
  *             rint(|r_j| * 2^(20 - E))^2, r = x - DQ(Q(x)) in fp32 (exact, order independent).
  * Ownership: all buffers caller-owned; nothing retained.  Errors: NVQ_ERR_ARG / SHAPE / ALIGN
@@ -132,7 +135,7 @@ nvq_status nvfp4_quantize(const void* x, int64_t rows, int64_t K, int64_t ldx,
                           const int64_t* grp_off, const int64_t* grp_rows, int32_t groups,
                           uint8_t* codes, int64_t ld_codes, uint8_t* sf, int64_t sf_cols,
                           int32_t zero_pad, nvq_tensor_scale* tscale, uint64_t* scores,
-                          void* stream);
+                          int32_t amax_given, void* stream);
 
 /*
  * rac_select_quantize -- channel selection of QUADS Eq. (24) and the second-pass quantization
@@ -193,6 +196,10 @@ nvq_status weight_qdq(const void* w, int32_t groups, int64_t N, int64_t K, int64
  *   epilogue  enum nvq_epilogue.   row_w  fp32 [rows] for NVQ_EPI_ROW_SCALE, else NULL.
  *   out, ldo  bf16 (fp32 for NVQ_EPI_STORE_F32) [rows][ldo], ldo in elements, ldo % 8 == 0;
  *             rows outside every group are not written.
+ *   out_tscale  NULL, or nvq_tensor_scale [groups] out (bf16 epilogues): zeroed, then
+ *             out_tscale[g].amax = max |out| over group g's rows as stored (bf16, exact), the
+ *             statistic nvfp4_quantize(..., amax_given = 1) needs to quantize `out` next
+ *             without another pass over it.
  */
 nvq_status w4a4_rac_grouped_gemm(int32_t groups, const int64_t* grp_off, const int64_t* grp_rows,
                                  int64_t rows, const uint8_t* a_codes, int64_t lda,
@@ -201,7 +208,8 @@ nvq_status w4a4_rac_grouped_gemm(int32_t groups, const int64_t* grp_off, const i
                                  uint8_t* b_codes, int64_t ldb, uint8_t* b_sf, int64_t b_sf_cols,
                                  const nvq_tensor_scale* b_tscale, int64_t N, int64_t K, int32_t k,
                                  const int32_t* idx, int32_t idx_per_group, int32_t epilogue,
-                                 const float* row_w, void* out, int64_t ldo, void* stream);
+                                 const float* row_w, void* out, int64_t ldo,
+                                 nvq_tensor_scale* out_tscale, void* stream);
 
 /*
  * rac_weight_tail -- the weight columns that multiply the RAC correction (QUADS §3.3, Eq. (21):

@@ -23,11 +23,11 @@ _SIGS = {
     "nvq_sf_cols": ([_I64], _I64),
     "nvq_sf_bytes": ([_I64, _I64], _I64),
     "nvq_sf_offset": ([_I64, _I64, _I64], _I64),
-    "nvfp4_quantize": ([_P, _I64, _I64, _I64, _P, _P, _I32, _P, _I64, _P, _I64, _I32, _P, _P, _P], C.c_int),
+    "nvfp4_quantize": ([_P, _I64, _I64, _I64, _P, _P, _I32, _P, _I64, _P, _I64, _I32, _P, _P, _I32, _P], C.c_int),
     "rac_select_quantize": ([_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _I32, _P, _I64, _P, _I64, _P, _P], C.c_int),
     "weight_qdq": ([_P, _I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _I32, _P], C.c_int),
     "w4a4_rac_grouped_gemm": ([_I32, _P, _P, _I64, _P, _I64, _P, _I64, _P, _I32, _P, _I64, _P, _I64, _P, _I64, _I64,
-                               _I32, _P, _I32, _I32, _P, _P, _I64, _P], C.c_int),
+                               _I32, _P, _I32, _I32, _P, _P, _I64, _P, _P], C.c_int),
     "rac_weight_tail": ([_I32, _I64, _I64, _I32, _P, _I32, _P, _I64, _P, _I64, _P, _P, _P, _P], C.c_int),
     "nvfp4_channel_major": ([_I32, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _P], C.c_int),
     "moe_capacity": ([_I64, _I32, _I32], _I64),
@@ -125,12 +125,12 @@ def fp4_mma_rate(mmas_per_sm: int = 65536, with_cp: bool = False, stream=None) -
 
 # --------------------------------------------------------------------------- the C ABI calls
 def nvfp4_quantize(x, codes, sf, sf_cols_, tscale, scores=None, grp_off=None, grp_rows=None, groups=1,
-                   zero_pad=False, rows=None, K=None, stream=None):
+                   zero_pad=False, rows=None, K=None, amax_given=False, stream=None):
     rows = x.shape[0] if rows is None else rows
     K = x.shape[1] if K is None else K
     _check("nvfp4_quantize", LIB.nvfp4_quantize(
         _ptr(x), rows, K, x.stride(0), _ptr(grp_off), _ptr(grp_rows), groups, _ptr(codes), codes.stride(0),
-        _ptr(sf), sf_cols_, int(bool(zero_pad)), _ptr(tscale), _ptr(scores), _stream(stream)))
+        _ptr(sf), sf_cols_, int(bool(zero_pad)), _ptr(tscale), _ptr(scores), int(bool(amax_given)), _stream(stream)))
 
 
 def rac_select_quantize(x, tscale, scores, k, codes, sf, sf_cols_, idx, grp_off=None, grp_rows=None, groups=1,
@@ -150,13 +150,13 @@ def weight_qdq(w, groups, N, K, codes, sf, sf_cols_, tscale, w_hat=None, w_hat_d
 
 def w4a4_rac_grouped_gemm(a_codes, a_sf, a_sf_cols, a_tscale, b_codes, b_sf, b_sf_cols, b_tscale, N, K, k, idx,
                           out, groups=1, grp_off=None, grp_rows=None, rows=None, a_scale_per_group=False,
-                          idx_per_group=False, epilogue=NVQ_EPI_STORE, row_w=None, stream=None):
+                          idx_per_group=False, epilogue=NVQ_EPI_STORE, row_w=None, out_tscale=None, stream=None):
     rows = a_codes.shape[0] if rows is None else rows
     _check("w4a4_rac_grouped_gemm", LIB.w4a4_rac_grouped_gemm(
         groups, _ptr(grp_off), _ptr(grp_rows), rows, _ptr(a_codes), a_codes.stride(0), _ptr(a_sf), a_sf_cols,
         _ptr(a_tscale), int(bool(a_scale_per_group)), _ptr(b_codes), b_codes.stride(0), _ptr(b_sf), b_sf_cols,
         _ptr(b_tscale), N, K, k, _ptr(idx), int(bool(idx_per_group)), epilogue, _ptr(row_w), _ptr(out),
-        out.stride(0), _stream(stream)))
+        out.stride(0), _ptr(out_tscale), _stream(stream)))
 
 
 def rac_weight_tail(groups, N, K, k, idx, b_codes, b_sf, b_sf_cols, b_tscale, idx_per_group=False, cm_codes=None,

@@ -69,6 +69,7 @@ struct GemmArgs {
     int64_t ldo;
     DeviceStatus* status;
     unsigned long long wait_limit;
+    nvq_tensor_scale* out_ts;  // NULL, or per-group max |out| (bf16 epilogues) into .amax
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -269,6 +270,29 @@ __device__ __forceinline__ void store_row(void* dst, const uint32_t* w, bool wid
 #pragma unroll
         for (int i = 0; i < kWords / 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
     }
+}
+
+// max |bf16| over n packed bf16x2 words (exact: a maximum of bf16 values).
+template <int kWords>
+__device__ __forceinline__ float amax_packed(const uint32_t* w)
+{
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < kWords; ++i) {
+        // sign-cleared bf16 values order like their bit patterns: an integer max per half
+        const uint32_t v = w[i] & 0x7fff7fffu;
+        m = __vmaxu2(m, v);
+    }
+    const uint32_t hi = m >> 16, lo = m & 0xffffu;
+    return __uint_as_float((hi > lo ? hi : lo) << 16);
+}
+
+// Warp maximum of a non-negative value, folded into *dst (float bits ordered as integers).
+__device__ __forceinline__ void warp_amax_to(float v, float* dst)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if ((threadIdx.x & 31) == 0 && v > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(dst), __float_as_uint(v));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
@@ -604,6 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 tc_fence_before();
                 mbar_arrive(&acc_empty);
                 if (valid) store_row<32>(a.out + grow * a.ldo + (int64_t)T.nt * (kBN / 2) + half * 64, pk, wide);
+                if (a.out_ts) warp_amax_to(valid ? amax_packed<32>(pk) : 0.0f, &a.out_ts[T.g].amax);
             } else {
                 const float sc = (a.epilogue == NVQ_EPI_ROW_SCALE) ? w : 1.0f;
                 uint32_t pk[64];
@@ -625,6 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 tc_fence_before();
                 mbar_arrive(&acc_empty);
                 if (valid) store_row<64>(a.out + grow * a.ldo + (int64_t)T.nt * kBN + half * (kBN / 2), pk, wide);
+                if (a.out_ts) warp_amax_to(valid ? amax_packed<64>(pk) : 0.0f, &a.out_ts[T.g].amax);
             }
             acc_phase ^= 1;
         }
@@ -682,7 +708,8 @@ extern "C" nvq_status w4a4_rac_grouped_gemm(int32_t groups, const int64_t* grp_o
                                             uint8_t* b_codes, int64_t ldb, uint8_t* b_sf, int64_t b_sf_cols,
                                             const nvq_tensor_scale* b_tscale, int64_t N, int64_t K, int32_t k,
                                             const int32_t* idx, int32_t idx_per_group, int32_t epilogue,
-                                            const float* row_w, void* out, int64_t ldo, void* stream)
+                                            const float* row_w, void* out, int64_t ldo, nvq_tensor_scale* out_tscale,
+                                            void* stream)
 {
     NVQ_CHECK_ARG(a_codes && a_sf && a_tscale && b_codes && b_sf && b_tscale && out, NVQ_ERR_ARG,
                   "w4a4_rac_grouped_gemm: null pointer argument");
@@ -739,7 +766,14 @@ extern "C" nvq_status w4a4_rac_grouped_gemm(int32_t groups, const int64_t* grp_o
     ga.ldo = ldo;
     ga.status = device_status_ptr();
     ga.wait_limit = wait_limit();
+    ga.out_ts = out_tscale;
     NVQ_CHECK_ARG(ga.status, NVQ_ERR_CUDA, "w4a4_rac_grouped_gemm: device status word unavailable");
+    NVQ_CHECK_ARG(!out_tscale || epilogue != NVQ_EPI_STORE_F32, NVQ_ERR_ARG,
+                  "w4a4_rac_grouped_gemm: out_tscale needs a bf16 epilogue");
+    if (out_tscale) {
+        const cudaError_t me = cudaMemsetAsync(out_tscale, 0, sizeof(nvq_tensor_scale) * groups, st);
+        if (me != cudaSuccess) return cuda_status(me, "cudaMemsetAsync(out_tscale)");
+    }
 
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);

@@ -476,18 +476,21 @@ static cudaError_t launch_quant(int grid, cudaStream_t st, const QuantArgs& qa)
 
 nvq_status quantize_impl(const void* x, int64_t rows, int64_t K, int64_t ldx, Groups gr, uint8_t* codes,
                          int64_t ld_codes, uint8_t* sf, int64_t sf_cols, int zero_pad, nvq_tensor_scale* ts,
-                         uint64_t* scores, void* w_hat, int w_hat_dtype, cudaStream_t st)
+                         uint64_t* scores, void* w_hat, int w_hat_dtype, cudaStream_t st, bool amax_given = false)
 {
     const int sms = sm_count();
-    cudaError_t e = cudaMemsetAsync(ts, 0, sizeof(nvq_tensor_scale) * gr.G, st);
-    if (e != cudaSuccess) return cuda_status(e, "cudaMemsetAsync(tscale)");
+    cudaError_t e = cudaSuccess;
+    if (!amax_given) {
+        e = cudaMemsetAsync(ts, 0, sizeof(nvq_tensor_scale) * gr.G, st);
+        if (e != cudaSuccess) return cuda_status(e, "cudaMemsetAsync(tscale)");
+    }
     if (scores) {
         e = cudaMemsetAsync(scores, 0, sizeof(uint64_t) * gr.G * K, st);
         if (e != cudaSuccess) return cuda_status(e, "cudaMemsetAsync(scores)");
     }
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-    // amax: ~8 CTAs per SM, whole rows per CTA
-    {
+    // amax: ~8 CTAs per SM, whole rows per CTA (skipped when the producer of x computed it)
+    if (!amax_given) {
         const int64_t want = (int64_t)sms * 8;
         int64_t rpc = (rows + want - 1) / want;
         if (rpc < 1) rpc = 1;
@@ -531,7 +534,7 @@ using namespace nvq;
 extern "C" nvq_status nvfp4_quantize(const void* x, int64_t rows, int64_t K, int64_t ldx, const int64_t* grp_off,
                                      const int64_t* grp_rows, int32_t groups, uint8_t* codes, int64_t ld_codes,
                                      uint8_t* sf, int64_t sf_cols, int32_t zero_pad, nvq_tensor_scale* tscale,
-                                     uint64_t* scores, void* stream)
+                                     uint64_t* scores, int32_t amax_given, void* stream)
 {
     NVQ_CHECK_ARG(x && codes && sf && tscale, NVQ_ERR_ARG, "nvfp4_quantize: null pointer argument");
     NVQ_CHECK_ARG(rows >= 1 && rows <= (1ll << 24), NVQ_ERR_SHAPE, "nvfp4_quantize: rows=%lld outside [1, 2^24]", (long long)rows);
@@ -546,7 +549,7 @@ extern "C" nvq_status nvfp4_quantize(const void* x, int64_t rows, int64_t K, int
     Groups gr{grp_off, grp_rows, groups, rows};
     set_error("");
     return quantize_impl(x, rows, K, ldx, gr, codes, ld_codes, sf, sf_cols, zero_pad, tscale, scores, nullptr, 0,
-                         static_cast<cudaStream_t>(stream));
+                         static_cast<cudaStream_t>(stream), amax_given != 0);
 }
 
 extern "C" nvq_status weight_qdq(const void* w, int32_t groups, int64_t N, int64_t K, int64_t ldw, uint8_t* codes,

@@ -146,10 +146,14 @@ class MoERacLayer:
         self.y = torch.zeros(cap, self.H, dtype=torch.bfloat16, device=dev)
 
     def kernel_launches_per_step(self) -> int:
-        """Kernels one forward() launches (dispatch 4; per GEMM side: quantize 2, selection and
-        residual tail 2, weight tail 1, GEMM 1; gather 1; combine 1)."""
-        side = 2 + (3 if self.k else 0) + 1
-        return 4 + 1 + 2 * side + 1
+        """Kernels one forward() launches: dispatch 4; tokens: amax + quantize 2, selection and
+        residual tail 2; gather 1; gate/up: weight tail 1, GEMM 1; h: quantize 1 (its amax comes
+        from the GEMM epilogue), selection and residual tail 2; down: weight tail 1, GEMM 1;
+        combine 1.  Without RAC (k = 0) there is no selection, no residual or weight tail."""
+        rac = 1 if self.k else 0
+        tok = 2 + 2 * rac
+        h = 1 + 2 * rac
+        return 4 + tok + 1 + (rac + 1) + h + (rac + 1) + 1
 
     def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, out: torch.Tensor,
                 stream=None, events: Optional[dict] = None):
@@ -182,12 +186,13 @@ class MoERacLayer:
         L.w4a4_rac_grouped_gemm(self.a_routed.codes, self.a_routed.sf, self.a_routed.sf_cols, self.a_tok.tscale,
                                 self.w13.codes, self.w13.sf, self.w13.sf_cols, self.w13.tscale, 2 * I, H, k,
                                 None, self.h, groups=E, grp_off=self.grp_off, grp_rows=self.grp_rows,
-                                rows=self.cap, epilogue=L.NVQ_EPI_SWIGLU, stream=stream)
+                                rows=self.cap, epilogue=L.NVQ_EPI_SWIGLU, out_tscale=self.a2.tscale, stream=stream)
         mark("gemm_gate_up", 1)
-        # down input: per-expert tensor scale and channel set
+        # down input: per-expert tensor scale (amax of h measured by the gate/up epilogue) and
+        # channel set
         L.nvfp4_quantize(self.h, self.a2.codes, self.a2.sf, self.a2.sf_cols, self.a2.tscale,
                          scores=self.scores2 if k else None, grp_off=self.grp_off, grp_rows=self.grp_rows,
-                         groups=E, zero_pad=(k == 0), stream=stream)
+                         groups=E, zero_pad=(k == 0), amax_given=True, stream=stream)
         if k:
             L.rac_select_quantize(self.h, self.a2.tscale, self.scores2, k, self.a2.codes, self.a2.sf,
                                   self.a2.sf_cols, self.idx2, grp_off=self.grp_off, grp_rows=self.grp_rows,

@@ -45,7 +45,7 @@ class Op:
         swizzle_into(self.sf, scales, self.sf_cols, row0=row0, col0=col0 // 16)
 
 
-def _run_case(L, counts, N, K, k, epilogue=0, seed=0, dense=False, rows_extra=0):
+def _run_case(L, counts, N, K, k, epilogue=0, seed=0, dense=False, rows_extra=0, out_amax=False):
     """counts: rows per group.  Groups start on multiples of 128 unless dense (one group)."""
     G = len(counts)
     off = [0]
@@ -85,12 +85,14 @@ def _run_case(L, counts, N, K, k, epilogue=0, seed=0, dense=False, rows_extra=0)
     out = torch.full((rows, out_w), float("nan"), dtype=torch.float32 if epilogue == 3 else torch.bfloat16,
                      device="cuda")
     row_w = torch.from_numpy(rng.uniform(0.1, 1.0, rows).astype(np.float32)).cuda()
+    out_ts = torch.full((G, 4), 7.0, dtype=torch.float32, device="cuda") if out_amax else None
     go = torch.tensor(off, dtype=torch.int64, device="cuda")
     gr = torch.tensor(counts, dtype=torch.int64, device="cuda")
     L.w4a4_rac_grouped_gemm(A.codes, A.sf, A.sf_cols, _ts_tensor(a_ts), B.codes, B.sf, B.sf_cols, _ts_tensor(b_ts),
                             N, K, k, idx_t if k else None, out, groups=G, grp_off=None if dense else go,
                             grp_rows=None if dense else gr, rows=rows, a_scale_per_group=True,
-                            idx_per_group=True, epilogue=epilogue, row_w=row_w if epilogue == 2 else None)
+                            idx_per_group=True, epilogue=epilogue, row_w=row_w if epilogue == 2 else None,
+                            out_tscale=out_ts)
     torch.cuda.synchronize()
     assert L.device_status() == (0, 0), "a device-side wait ran out"
     # the weight tail the call built
@@ -116,7 +118,17 @@ def _run_case(L, counts, N, K, k, epilogue=0, seed=0, dense=False, rows_extra=0)
             ref = ref * row_w[off[g]:off[g] + c].cpu().numpy()[:, None].astype(np.float64)
         got = y[off[g]:off[g] + c]
         assert np.all(np.isfinite(got))
+        if out_amax:
+            # the epilogue's per-group amax is the max |stored bf16| over the group's rows, exactly
+            ots = out_ts.cpu().numpy()
+            assert ots[g, 0] == np.float32(np.abs(got).max()), (g, ots[g, 0], np.abs(got).max())
         worst = max(worst, gemm_error(got, ref, out_bf16=(epilogue != 3)))
+    if out_amax:
+        ots = out_ts.cpu().numpy()
+        for g, c in enumerate(counts):
+            if not c:
+                assert ots[g, 0] == 0.0
+        assert not ots[:, 1:].any()  # the rest of each record is zeroed
     # rows outside every group are not written
     if not dense:
         valid = np.zeros(rows, bool)
@@ -155,3 +167,10 @@ def test_gemm_fp32_output_is_elementwise_within_2e3(L):
     elementwise rule (no rounding allowance)."""
     worst = _run_case(L, [200, 3, 128], 512, 1536, 64, epilogue=3, seed=6)
     assert worst < 1e-5
+
+
+@pytest.mark.parametrize("epilogue", [1, 2])
+def test_gemm_epilogue_amax_for_the_next_quantizer(L, epilogue):
+    """out_tscale: zeroed, then per group max |out| over the rows the call stores (bit-exact),
+    with an empty group left at 0 -- what nvfp4_quantize(amax_given) takes as the amax."""
+    _run_case(L, [300, 0, 129, 1], 512, 256, 32, epilogue=epilogue, seed=7, out_amax=True)

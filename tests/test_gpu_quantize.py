@@ -276,3 +276,32 @@ def test_weight_tail_channel_major_path(L, G, N, K, k, per_group):
         assert np.array_equal(tc_all[rows, K // 2:(K + k) // 2], tc)
         assert np.array_equal(tsc_all[rows, K // 16:(K + k) // 16], tsc)
         assert not tsc_all[rows, (K + k) // 16:].any()
+
+
+def test_quantize_with_given_amax_equals_measured(L):
+    """amax_given: tscale[g].amax set by the caller (as the GEMM epilogue leaves it) gives the
+    same tensor scales, codes, scales and scores as the call that measures amax itself."""
+    counts = [200, 0, 129]
+    off = [0, 256, 256, 512]
+    K = 768
+    x = np.zeros((512, K), np.uint16)
+    for g, c in enumerate(counts):
+        if c:
+            xg, _ = wl.activations(c, K, seed=40 + g, n_outliers=8, outlier_gain=15.0)
+            x[off[g]:off[g] + c] = xg
+    a = _gpu_quant(L, x, groups=3, grp_off=off, grp_rows=counts)
+    xt = bf16_tensor(x)
+    ts = a["ts"].clone()
+    ts[:, 1:] = 0.0  # only amax is given
+    sf_cols = a["sf_cols"]
+    codes = torch.full((512, a["codes"].shape[1]), 0xAB, dtype=torch.uint8, device="cuda")
+    sf = torch.full_like(a["sf"], 0xCD)
+    scores = torch.zeros(3, K, dtype=torch.int64, device="cuda")
+    go = torch.tensor(off, dtype=torch.int64, device="cuda")
+    gr = torch.tensor(counts, dtype=torch.int64, device="cuda")
+    L.nvfp4_quantize(xt, codes, sf, sf_cols, ts, scores=scores, grp_off=go, grp_rows=gr, groups=3, zero_pad=True,
+                     amax_given=True)
+    torch.cuda.synchronize()
+    assert torch.equal(ts.view(torch.int32), a["ts"].view(torch.int32))
+    assert np.array_equal(codes.cpu().numpy(), a["codes"]) and torch.equal(sf, a["sf"])
+    assert np.array_equal(scores.cpu().numpy().view(np.uint64), a["scores"])
