@@ -37,6 +37,25 @@ FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense ratio (NVFP4 / BF16) on GB3
 METRIC = "W4A4+RAC grouped-GEMM TFLOPS & tokens/s; act-quant+RAC HBM GB/s (1×GB300)"
 
 
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "gemm_kernel_moe_prefill_dram_traffic.md")
+GEMM_SOURCE = os.path.join(ROOT, "nvfp4_w4a4_quantized_quantize_gb300", "csrc", "gemm.cu")
+
+
+def gemm_traffic_per_launch(launch: str = "gate_up"):
+    """DRAM bytes (read + write) of one full-size launch of the grouped GEMM, from the committed
+    ncu summary, or None when the kernel source has changed since those counters were taken."""
+    import hashlib
+    import re
+    if not os.path.exists(TRAFFIC_PROFILE):
+        return None
+    src = hashlib.sha256(open(GEMM_SOURCE, "rb").read()).hexdigest()
+    for line in open(TRAFFIC_PROFILE):
+        m = re.search(r"traffic: launch=(\w+) dram_read=(\d+) dram_write=(\d+) gemm_cu_sha256=([0-9a-f]+)", line)
+        if m and m.group(1) == launch:
+            return int(m.group(2)) + int(m.group(3)) if m.group(4) == src else None
+    return None
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -319,7 +338,7 @@ def run_ours(args, world, rank, local):
         "kernel_ms": {"gemm_gate_up": t_gu, "gemm_down": t_dn, "quant_rac_tokens": t_q1},
         "roofline": {"kernel": "gemm_kernel (gate/up, SwiGLU epilogue)", "bound": "tensor",
                      "achieved": round(ach_gu, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
-                     "frac": round(ach_gu / fp4_peak, 4), "traffic": None,
+                     "frac": round(ach_gu / fp4_peak, 4), "traffic": gemm_traffic_per_launch("gate_up"),
                      "peak_source": f"{src} bf16 burst {peaks['bf16_tflops']} x nominal NVFP4/BF16 ratio 6"},
         "e2e": {"value": round(e2e_tps, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
