@@ -177,24 +177,50 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
     }
     __syncthreads();
     if (out_codes != nullptr) {
+        // four rows per warp at a time: all their loads are in flight before the stores
         const int nvec = (int)(ktot / 32);  // 16-byte vectors of codes
         const bool tail8 = (ktot % 32) != 0;
-        for (int r = warp; r < 128; r += 8) {
-            const int sr = src[r];
-            uint4* dst = reinterpret_cast<uint4*>(out_codes + (r0 + r) * ld_out);
-            const uint4* sp = reinterpret_cast<const uint4*>(codes + (int64_t)(sr >= 0 ? sr : 0) * ld_codes);
-            for (int v = lane; v < nvec; v += 32) dst[v] = sr >= 0 ? __ldg(sp + v) : make_uint4(0, 0, 0, 0);
-            if (tail8 && lane == 0)
-                reinterpret_cast<uint2*>(dst)[nvec * 2] = sr >= 0 ? reinterpret_cast<const uint2*>(sp)[nvec * 2] : make_uint2(0, 0);
+        for (int r4 = warp * 4; r4 < 128; r4 += 32) {
+            for (int v0 = 0; v0 < nvec; v0 += 32) {
+                const int v = v0 + lane;
+                uint4 val[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int sr = src[r4 + i];
+                    const uint4* sp = reinterpret_cast<const uint4*>(codes + (int64_t)(sr >= 0 ? sr : 0) * ld_codes);
+                    val[i] = (sr >= 0 && v < nvec) ? __ldg(sp + v) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (v < nvec) reinterpret_cast<uint4*>(out_codes + (r0 + r4 + i) * ld_out)[v] = val[i];
+            }
+            if (tail8 && lane < 4) {
+                const int sr = src[r4 + lane];
+                const uint2* sp = reinterpret_cast<const uint2*>(codes + (int64_t)(sr >= 0 ? sr : 0) * ld_codes);
+                reinterpret_cast<uint2*>(out_codes + (r0 + r4 + lane) * ld_out)[nvec * 2] = sr >= 0 ? sp[nvec * 2] : make_uint2(0, 0);
+            }
         }
     }
+    // scales: four words per thread at a time, loads before stores
     const int natoms = (int)(sf_cols / 4);
+    const int nwords = natoms * 128;
     uint32_t* outw = reinterpret_cast<uint32_t*>(out_sf + blockIdx.x * (int64_t)natoms * 512);
-    for (int w = tid; w < natoms * 128; w += 256) {
-        const int a = w >> 7, pos = w & 127;
-        const int r = (pos >> 2) + 32 * (pos & 3);
-        const int sr = src[r];
-        outw[w] = sr >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(sf + sf_offset(sr, 4 * a, sf_cols))) : 0u;
+    for (int w0 = tid; w0 < nwords; w0 += 4 * 256) {
+        uint32_t val[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int w = w0 + i * 256;
+            val[i] = 0u;
+            if (w < nwords) {
+                const int a = w >> 7, pos = w & 127;
+                const int r = (pos >> 2) + 32 * (pos & 3);
+                const int sr = src[r];
+                if (sr >= 0) val[i] = __ldg(reinterpret_cast<const uint32_t*>(sf + sf_offset(sr, 4 * a, sf_cols)));
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (w0 + i * 256 < nwords) outw[w0 + i * 256] = val[i];
     }
 }
 

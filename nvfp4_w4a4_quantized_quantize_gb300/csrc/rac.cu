@@ -252,9 +252,11 @@ __global__ void __launch_bounds__(256) weight_tail_kernel(uint8_t* __restrict__ 
         for (int64_t c = (K + k) / 16; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
 }
 
-// Same tail from the channel-major copy (nvfp4_channel_major): thread per (group, tail block,
-// weight row n), n fastest, so a warp reads each selected channel's 32 codes (16 bytes) and 32
-// block scales (32 bytes) of consecutive rows in one coalesced access.
+// Same tail from the channel-major copy (nvfp4_channel_major): thread per (group, weight row n),
+// n fastest, so a warp reads each selected channel's codes (16 bytes) and block scales (32
+// bytes) of 32 consecutive rows in one coalesced access.  A thread writes its row's whole tail
+// at once: k/2 code bytes, and the tail scale bytes with the zeroed padding as whole 32-bit
+// words when they start on one (K/16 % 4 == 0).
 __global__ void __launch_bounds__(256) weight_tail_cm_kernel(uint8_t* __restrict__ codes, int64_t ld_codes,
                                                               uint8_t* __restrict__ sf, int64_t sf_cols, int64_t N,
                                                               int K, int k, int G, const nvq_tensor_scale* __restrict__ ts,
@@ -262,29 +264,46 @@ __global__ void __launch_bounds__(256) weight_tail_cm_kernel(uint8_t* __restrict
                                                               const uint8_t* __restrict__ cm_codes,
                                                               const uint8_t* __restrict__ cm_sf)
 {
-    const int nbt = k / 16;
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= (int64_t)G * nbt * N) return;
+    if (t >= (int64_t)G * N) return;
     const int64_t n = t % N;
-    const int b = (int)((t / N) % nbt);
-    const int g = (int)(t / (N * nbt));
+    const int g = (int)(t / N);
     const float s_enc = ts[g].s_enc, s_dec = ts[g].s_dec;
-    const int32_t* sel = idx + (idx_per_group ? (int64_t)g * k : 0) + b * 16;
+    const int32_t* sel = idx + (idx_per_group ? (int64_t)g * k : 0);
     const int nsb = K / 16;
-    float wv[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const int j = sel[i];
-        const uint32_t c = (cm_codes[((int64_t)g * K + j) * (N / 2) + (n >> 1)] >> ((n & 1) * 4)) & 0xfu;
-        const uint32_t sb = cm_sf[((int64_t)g * nsb + (j >> 4)) * N + n];
-        wv[i] = __fmul_rn(e2m1_value(c), __fmul_rn(e4m3_value(sb), s_dec));
-    }
     const int64_t row = (int64_t)g * N + n;
-    BlockOut o = quantize16(wv, s_enc, s_dec);
-    *reinterpret_cast<uint2*>(codes + row * ld_codes + (K + 16 * b) / 2) = make_uint2(o.code_lo, o.code_hi);
-    sf[sf_offset(row, K / 16 + b, sf_cols)] = (uint8_t)o.sb;
-    if (b == 0)
-        for (int64_t c = (K + k) / 16; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
+    uint8_t* crow = codes + row * ld_codes + K / 2;
+    const bool word_sf = (nsb % 4) == 0;
+    uint32_t sfw = 0;  // tail scale bytes of the current 4-column group
+    for (int b = 0; b < k / 16; ++b) {
+        float wv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int j = sel[b * 16 + i];
+            const uint32_t c = (cm_codes[((int64_t)g * K + j) * (N / 2) + (n >> 1)] >> ((n & 1) * 4)) & 0xfu;
+            const uint32_t sb = cm_sf[((int64_t)g * nsb + (j >> 4)) * N + n];
+            wv[i] = __fmul_rn(e2m1_value(c), __fmul_rn(e4m3_value(sb), s_dec));
+        }
+        const BlockOut o = quantize16(wv, s_enc, s_dec);
+        *reinterpret_cast<uint2*>(crow + 8 * b) = make_uint2(o.code_lo, o.code_hi);
+        if (word_sf) {
+            sfw |= o.sb << (8 * (b & 3));
+            if ((b & 3) == 3) {
+                *reinterpret_cast<uint32_t*>(sf + sf_offset(row, nsb + b - 3, sf_cols)) = sfw;
+                sfw = 0;
+            }
+        } else {
+            sf[sf_offset(row, nsb + b, sf_cols)] = (uint8_t)o.sb;
+        }
+    }
+    const int64_t c0 = (K + k) / 16;
+    if (word_sf && (c0 & 3)) {
+        // the last partial group: its remaining bytes are padding (zero)
+        *reinterpret_cast<uint32_t*>(sf + sf_offset(row, c0 & ~3ll, sf_cols)) = sfw;
+        for (int64_t c = (c0 | 3) + 1; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
+    } else {
+        for (int64_t c = c0; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
+    }
 }
 
 // Channel-major copy of the codes: CTA per (group, 64 rows, 128 channels) tile, transposed
@@ -428,7 +447,7 @@ extern "C" nvq_status rac_weight_tail(int32_t groups, int64_t N, int64_t K, int3
     set_error("");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (!cm_codes) return weight_tail_impl(b_codes, ldb, b_sf, b_sf_cols, N, (int)K, k, groups, b_tscale, idx, idx_per_group, st);
-    const int64_t total = (int64_t)groups * (k / 16) * N;
+    const int64_t total = (int64_t)groups * N;
     weight_tail_cm_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(b_codes, ldb, b_sf, b_sf_cols, N, (int)K, k, groups,
                                                                            b_tscale, idx, idx_per_group, cm_codes, cm_sf);
     NVQ_LAUNCH_CHECK("weight_tail_cm_kernel");
