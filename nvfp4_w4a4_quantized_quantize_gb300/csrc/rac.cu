@@ -160,64 +160,101 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const unsigned long 
 }
 
 // ------------------------------------------------------------------------ activation tail
-// Half a warp per (row, tail block of 16 selected channels): lane i of the half gathers channel
-// idx[16 b + i], recomputes its residual (bit-identical to the first pass), and the 16 lanes
-// quantize the block together (max by shuffles, codes packed by shuffles).
-__global__ void __launch_bounds__(256) act_tail_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, int K, int k,
-                                                        Groups gr, const nvq_tensor_scale* __restrict__ ts,
-                                                        const int32_t* __restrict__ idx, uint8_t* __restrict__ codes,
-                                                        int64_t ld_codes, uint8_t* __restrict__ sf, int64_t sf_cols)
+// Thread per (row of a 64-row tile, share of the k/16 tail blocks): bsplit threads split a
+// row's blocks (1 when there are rows enough to fill the GPU, more for short inputs).  The CTA stages
+// the tile's group's selected channels and, for each of the 128 E4M3 scale codes, the encode
+// factor fl(S_enc / sb) and decode factor fl(sb * S_dec) (the tables the first pass used), so a
+// thread recomputes each gathered element's code and residual (bit-identical to the first
+// pass) with lookups instead of divisions; it then quantizes each block of 16 residuals and
+// writes its row's whole tail at once.  Rows of another group than the tile's first row (only
+// with groups that do not start on 64-row boundaries) compute the factors directly.
+constexpr int kTailRows = 64;
+
+__global__ void __launch_bounds__(512) act_tail_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, int K, int k,
+                                                       Groups gr, const nvq_tensor_scale* __restrict__ ts,
+                                                       const int32_t* __restrict__ idx, uint8_t* __restrict__ codes,
+                                                       int64_t ld_codes, uint8_t* __restrict__ sf, int64_t sf_cols, int bsplit)
 {
-    const int nbt = k > 0 ? k / 16 : 1;  // k == 0: one half-warp per row zeroes the scale padding
-    const int64_t hw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 4;  // half-warp id
-    const int i = threadIdx.x & 15;
-    const int64_t row = hw / nbt;
-    const int b = (int)(hw % nbt);
-    const bool in_range = row < gr.total_rows;
-    int64_t gb = 0, ge = 0;
-    int g = 0;
-    if (in_range) {
+    __shared__ float eb_tab[128], db_tab[128];
+    __shared__ int s_sel[512];
+    __shared__ int s_g0;
+    const int tid = threadIdx.x;
+    const int t = tid % kTailRows;   // row in the tile
+    const int part = tid / kTailRows;  // share of the row's blocks: b = part, part + bsplit, ...
+    const int64_t tile_row = (int64_t)blockIdx.x * kTailRows;
+    if (tid == 0) s_g0 = tile_row < gr.total_rows ? group_of_row(gr, tile_row) : 0;
+    __syncthreads();
+    const int g0 = s_g0;
+    const float s_enc0 = ts[g0].s_enc, s_dec0 = ts[g0].s_dec;
+    for (int e = tid; e < 128; e += blockDim.x) {
+        const float sbv = e4m3_value((uint32_t)e);
+        eb_tab[e] = (e == 0 || e == 127) ? 0.0f : __fdiv_rn(s_enc0, sbv);
+        db_tab[e] = (e == 127) ? 0.0f : __fmul_rn(sbv, s_dec0);
+    }
+    for (int c = tid; c < k; c += blockDim.x) s_sel[c] = idx[(int64_t)g0 * k + c];
+    __syncthreads();
+
+    const int64_t row = tile_row + t;
+    if (row >= gr.total_rows) return;
+    int g = g0;
+    if (gr.off != nullptr)
+        while (g + 1 < gr.G && gr.off[g + 1] <= row) ++g;
+    else
         g = group_of_row(gr, row);
-        group_range(gr, g, gb, ge);
-    }
-    const bool active = in_range && row >= gb && row < ge;
-    if (k > 0) {
-        float rv = 0.0f, s_enc = 1.0f, s_dec = 1.0f;
-        if (active) {
-            s_enc = ts[g].s_enc;
-            s_dec = ts[g].s_dec;
-            const int j = idx[(int64_t)g * k + b * 16 + i];
-            const float xv = __bfloat162float(x[row * ldx + j]);
-            const uint32_t sb = sf[sf_offset(row, j >> 4, sf_cols)];
-            const float sbv = e4m3_value(sb);
-            const float e_b = sb == 0 ? 0.0f : __fdiv_rn(s_enc, sbv);
-            const uint32_t code = e2m1x2(__fmul_rn(xv, e_b), 0.0f) & 0xfu;
-            rv = residual(xv, code, __fmul_rn(sbv, s_dec));
-        }
-        // block scale from the 16 lanes' residuals
-        float m = fabsf(rv);
+    int64_t gb, ge;
+    group_range(gr, g, gb, ge);
+    if (row < gb || row >= ge) return;
+    const bool own = g == g0;
+    const float s_enc = own ? s_enc0 : ts[g].s_enc, s_dec = own ? s_dec0 : ts[g].s_dec;
+    const int32_t* sel_g = idx + (int64_t)g * k;
+    const __nv_bfloat16* xr = x + row * ldx;
+    uint8_t* crow = codes + row * ld_codes + K / 2;
+    const int nsb = K / 16;
+    const bool word_sf = (nsb % 4) == 0 && bsplit == 1;
+    uint32_t sfw = 0;
+    for (int b = part; b < k / 16; b += bsplit) {
+        float xv[16];
+        uint32_t sb[16];
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o, 16));
-        const uint32_t sb2 = e4m3(__fmul_rn(__fdiv_rn(m, 6.0f), s_enc));
-        const float sbv2 = e4m3_value(sb2);
-        const float e2 = sb2 == 0 ? 0.0f : __fdiv_rn(s_enc, sbv2);
-        uint32_t c = e2m1x2(__fmul_rn(rv, e2), 0.0f) & 0xfu;   // sb2 == 0: +-0 keeps the sign
-        // pack: byte i/2 = c(i) | c(i+1) << 4, then 8 bytes of the block from lanes 0..7
-        const uint32_t c_hi = __shfl_down_sync(0xffffffffu, c, 1, 16);
-        const uint32_t byte = c | (c_hi << 4);
-        uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            w0 |= __shfl_sync(0xffffffffu, byte, 2 * q, 16) << (8 * q);
-            w1 |= __shfl_sync(0xffffffffu, byte, 8 + 2 * q, 16) << (8 * q);
+        for (int i = 0; i < 16; ++i) {
+            const int j = own ? s_sel[b * 16 + i] : sel_g[b * 16 + i];
+            xv[i] = __bfloat162float(xr[j]);
+            sb[i] = sf[sf_offset(row, j >> 4, sf_cols)];
         }
-        if (active && i == 0) {
-            *reinterpret_cast<uint2*>(codes + row * ld_codes + (K + 16 * b) / 2) = make_uint2(w0, w1);
-            sf[sf_offset(row, K / 16 + b, sf_cols)] = (uint8_t)sb2;
+        float rv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float e_b, d_b;
+            if (own) {
+                e_b = eb_tab[sb[i]];
+                d_b = db_tab[sb[i]];
+            } else {
+                const float sbv = e4m3_value(sb[i]);
+                e_b = sb[i] == 0 ? 0.0f : __fdiv_rn(s_enc, sbv);
+                d_b = __fmul_rn(sbv, s_dec);
+            }
+            const uint32_t code = e2m1x2(__fmul_rn(xv[i], e_b), 0.0f) & 0xfu;  // e_b 0: +-0 keeps the sign
+            rv[i] = residual(xv[i], code, d_b);
+        }
+        const BlockOut o = quantize16(rv, s_enc, s_dec);
+        *reinterpret_cast<uint2*>(crow + 8 * b) = make_uint2(o.code_lo, o.code_hi);
+        if (word_sf) {
+            sfw |= o.sb << (8 * (b & 3));
+            if ((b & 3) == 3) {
+                *reinterpret_cast<uint32_t*>(sf + sf_offset(row, nsb + b - 3, sf_cols)) = sfw;
+                sfw = 0;
+            }
+        } else {
+            sf[sf_offset(row, nsb + b, sf_cols)] = (uint8_t)o.sb;
         }
     }
-    if (active && b == 0)
-        for (int64_t c = (K + k) / 16 + i; c < sf_cols; c += 16) sf[sf_offset(row, c, sf_cols)] = 0;
+    const int64_t c0 = (K + k) / 16;
+    if (word_sf && (c0 & 3)) {
+        *reinterpret_cast<uint32_t*>(sf + sf_offset(row, c0 & ~3ll, sf_cols)) = sfw;  // rest of the group: padding
+        for (int64_t c = (c0 | 3) + 1; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
+    } else if (part == 0) {
+        for (int64_t c = c0; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
+    }
 }
 
 // ------------------------------------------------------------------------ weight tail
@@ -252,25 +289,44 @@ __global__ void __launch_bounds__(256) weight_tail_kernel(uint8_t* __restrict__ 
         for (int64_t c = (K + k) / 16; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
 }
 
-// Same tail from the channel-major copy (nvfp4_channel_major): thread per (group, weight row n),
-// n fastest, so a warp reads each selected channel's codes (16 bytes) and block scales (32
-// bytes) of 32 consecutive rows in one coalesced access.  A thread writes its row's whole tail
-// at once: k/2 code bytes, and the tail scale bytes with the zeroed padding as whole 32-bit
-// words when they start on one (K/16 % 4 == 0).
-__global__ void __launch_bounds__(256) weight_tail_cm_kernel(uint8_t* __restrict__ codes, int64_t ld_codes,
-                                                              uint8_t* __restrict__ sf, int64_t sf_cols, int64_t N,
-                                                              int K, int k, int G, const nvq_tensor_scale* __restrict__ ts,
-                                                              const int32_t* __restrict__ idx, int idx_per_group,
-                                                              const uint8_t* __restrict__ cm_codes,
-                                                              const uint8_t* __restrict__ cm_sf)
+// Same tail from the channel-major copy (nvfp4_channel_major): CTA per (group, 64 weight rows).
+// The CTA first stages, for each of the k selected channels, the 32 code bytes and 64 scale
+// bytes of its rows into shared memory with 16-byte loads (all in flight together); then thread
+// t builds row t's whole tail from there and writes it at once: k/2 code bytes, and the tail
+// scale bytes with the zeroed padding as whole 32-bit words when they start on one
+// (K/16 % 4 == 0).
+constexpr int kWtRows = 64;
+
+__global__ void __launch_bounds__(kWtRows) weight_tail_cm_kernel(uint8_t* __restrict__ codes, int64_t ld_codes,
+                                                                  uint8_t* __restrict__ sf, int64_t sf_cols, int64_t N,
+                                                                  int K, int k, const nvq_tensor_scale* __restrict__ ts,
+                                                                  const int32_t* __restrict__ idx, int idx_per_group,
+                                                                  const uint8_t* __restrict__ cm_codes,
+                                                                  const uint8_t* __restrict__ cm_sf)
 {
-    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= (int64_t)G * N) return;
-    const int64_t n = t % N;
-    const int g = (int)(t / N);
-    const float s_enc = ts[g].s_enc, s_dec = ts[g].s_dec;
-    const int32_t* sel = idx + (idx_per_group ? (int64_t)g * k : 0);
+    extern __shared__ __align__(16) uint8_t wt_smem[];
+    uint8_t* s_codes = wt_smem;                   // [k][32]: rows n0 .. n0+63, two per byte
+    uint8_t* s_sf = wt_smem + (size_t)k * 32;     // [k][64]
+    const int g = blockIdx.y;
+    const int64_t n0 = (int64_t)blockIdx.x * kWtRows;
+    const int t = threadIdx.x;
     const int nsb = K / 16;
+    const int32_t* sel = idx + (idx_per_group ? (int64_t)g * k : 0);
+    // stage: per channel 2 x 16 code bytes + 4 x 16 scale bytes
+    for (int w = t; w < k * 6; w += kWtRows) {
+        const int c = w / 6, part = w % 6;
+        const int j = sel[c];
+        uint4 v;
+        if (part < 2)
+            v = __ldg(reinterpret_cast<const uint4*>(cm_codes + ((int64_t)g * K + j) * (N / 2) + n0 / 2) + part);
+        else
+            v = __ldg(reinterpret_cast<const uint4*>(cm_sf + ((int64_t)g * nsb + (j >> 4)) * N + n0) + (part - 2));
+        if (part < 2) reinterpret_cast<uint4*>(s_codes + c * 32)[part] = v;
+        else reinterpret_cast<uint4*>(s_sf + c * 64)[part - 2] = v;
+    }
+    __syncthreads();
+    const int64_t n = n0 + t;
+    const float s_enc = ts[g].s_enc, s_dec = ts[g].s_dec;
     const int64_t row = (int64_t)g * N + n;
     uint8_t* crow = codes + row * ld_codes + K / 2;
     const bool word_sf = (nsb % 4) == 0;
@@ -279,10 +335,10 @@ __global__ void __launch_bounds__(256) weight_tail_cm_kernel(uint8_t* __restrict
         float wv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const int j = sel[b * 16 + i];
-            const uint32_t c = (cm_codes[((int64_t)g * K + j) * (N / 2) + (n >> 1)] >> ((n & 1) * 4)) & 0xfu;
-            const uint32_t sb = cm_sf[((int64_t)g * nsb + (j >> 4)) * N + n];
-            wv[i] = __fmul_rn(e2m1_value(c), __fmul_rn(e4m3_value(sb), s_dec));
+            const int c = b * 16 + i;
+            const uint32_t code = (s_codes[c * 32 + (t >> 1)] >> ((t & 1) * 4)) & 0xfu;
+            const uint32_t sb = s_sf[c * 64 + t];
+            wv[i] = __fmul_rn(e2m1_value(code), __fmul_rn(e4m3_value(sb), s_dec));
         }
         const BlockOut o = quantize16(wv, s_enc, s_dec);
         *reinterpret_cast<uint2*>(crow + 8 * b) = make_uint2(o.code_lo, o.code_hi);
@@ -400,9 +456,17 @@ extern "C" nvq_status rac_select_quantize(const void* x, int64_t rows, int64_t K
         topk_kernel<<<groups, kTopkThreads, 0, st>>>(reinterpret_cast<const unsigned long long*>(scores), (int)K, k, idx);
         NVQ_LAUNCH_CHECK("topk_kernel");
     }
-    const int64_t threads = rows * (k > 0 ? k / 16 : 1) * 16;
-    act_tail_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), ldx, (int)K,
-                                                                       k, gr, tscale, idx, codes, ld_codes, sf, sf_cols);
+    const int64_t tiles = (rows + kTailRows - 1) / kTailRows;
+    // split a row's tail blocks over threads until there are ~8 CTAs' worth of threads per SM
+    int sms = 148, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int bsplit = 1;
+    const int nbt = k > 0 ? k / 16 : 1;
+    while (bsplit < nbt && bsplit < 8 && tiles * bsplit < (int64_t)sms * 8) bsplit *= 2;
+    if (bsplit > nbt) bsplit = nbt;
+    act_tail_kernel<<<(unsigned)tiles, kTailRows * bsplit, 0, st>>>(static_cast<const __nv_bfloat16*>(x), ldx, (int)K,
+                                                                       k, gr, tscale, idx, codes, ld_codes, sf, sf_cols, bsplit);
     NVQ_LAUNCH_CHECK("act_tail_kernel");
     return NVQ_OK;
 }
@@ -437,6 +501,8 @@ extern "C" nvq_status rac_weight_tail(int32_t groups, int64_t N, int64_t K, int3
     NVQ_CHECK_ARG(idx && b_codes && b_sf && b_tscale, NVQ_ERR_ARG, "rac_weight_tail: null pointer argument");
     NVQ_CHECK_ARG(!cm_codes == !cm_sf, NVQ_ERR_ARG, "rac_weight_tail: give both channel-major arrays or neither");
     NVQ_CHECK_ARG(!cm_codes || N % 64 == 0, NVQ_ERR_SHAPE, "rac_weight_tail: the channel-major path needs N % 64 == 0");
+    NVQ_CHECK_ARG(!cm_codes || (aligned(cm_codes, 16) && aligned(cm_sf, 16)), NVQ_ERR_ALIGN,
+                  "rac_weight_tail: the channel-major arrays must be 16-byte aligned");
     NVQ_CHECK_ARG(groups >= 1 && groups <= 4096 && N >= 1 && (int64_t)groups * N <= (1ll << 24), NVQ_ERR_SHAPE,
                   "rac_weight_tail: groups*N outside [1, 2^24]");
     NVQ_CHECK_ARG(K >= 16 && K <= 8192 && K % 16 == 0, NVQ_ERR_SHAPE, "rac_weight_tail: K must be a multiple of 16 in [16, 8192]");
@@ -447,9 +513,10 @@ extern "C" nvq_status rac_weight_tail(int32_t groups, int64_t N, int64_t K, int3
     set_error("");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (!cm_codes) return weight_tail_impl(b_codes, ldb, b_sf, b_sf_cols, N, (int)K, k, groups, b_tscale, idx, idx_per_group, st);
-    const int64_t total = (int64_t)groups * N;
-    weight_tail_cm_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(b_codes, ldb, b_sf, b_sf_cols, N, (int)K, k, groups,
-                                                                           b_tscale, idx, idx_per_group, cm_codes, cm_sf);
+    const size_t smem = (size_t)k * 96;  // k <= 512: at most 48 KB
+    const dim3 grid((unsigned)(N / kWtRows), (unsigned)groups);
+    weight_tail_cm_kernel<<<grid, kWtRows, smem, st>>>(b_codes, ldb, b_sf, b_sf_cols, N, (int)K, k, b_tscale, idx,
+                                                      idx_per_group, cm_codes, cm_sf);
     NVQ_LAUNCH_CHECK("weight_tail_cm_kernel");
     return NVQ_OK;
 }
