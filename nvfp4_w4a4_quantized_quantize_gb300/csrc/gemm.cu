@@ -33,13 +33,19 @@
 
 namespace nvq {
 
-constexpr int kBM = 128, kBN = 256, kBK = 256;  // kBK in FP4 elements
-constexpr int kStages = 4;
-constexpr int kABytes = kBM * kBK / 2;     // 16384
-constexpr int kBBytes = kBN * kBK / 2;     // 32768
-constexpr int kSFABytes = kBM * kBK / 16;  // 2048: 4 atoms of 512 B
-constexpr int kSFBBytes = kBN * kBK / 16;  // 4096: 2 row blocks x 4 atoms
+constexpr int kBM = 128, kBN = 256, kBK = 256;  // kBK in FP4 elements (128 bytes per row)
+constexpr int kAtoms = kBK / 64;            // K = 64 steps per stage: MMAs, and scale atoms per 128 rows
+constexpr int kStages = 4;                  // 4 x 54 KB (a 128-element K-tile in 8 x 27 KB was slower:
+                                            // twice the per-stage hand-offs)
+constexpr int kRowBytes = kBK / 2;          // bytes of a tile row in shared memory = swizzle span
+constexpr uint32_t kSwizzleLayout = kRowBytes == 128 ? 2u : 4u;  // tcgen05 smem layout: 128B = 2, 64B = 4
+constexpr uint32_t kSBO = 8 * kRowBytes;    // stride between 8-row core-matrix groups
+constexpr int kABytes = kBM * kBK / 2;      // 16384
+constexpr int kBBytes = kBN * kBK / 2;      // 32768
+constexpr int kSFABytes = kBM * kBK / 16;   // 2048: kAtoms atoms of 512 B
+constexpr int kSFBBytes = kBN * kBK / 16;   // 4096: 2 row blocks x kAtoms atoms
 constexpr int kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;  // 55296 (54 x 1024)
+static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned");
 constexpr int kSmemBytes = kStages * kStageBytes + 1024;
 constexpr int kThreads = 448;  // warp 0 TMA, warp 1 MMA, warps 2-5 scale staging, warps 6-13 epilogue
 constexpr int kFirstEpiWarp = 6;
@@ -49,7 +55,7 @@ constexpr int kCluster = 2;  // CTAs sharing one weight tile by multicast
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;                  // 256 fp32 columns
 constexpr uint32_t kSFCol = 256;                 // + stage * 48: SFA 16 columns, SFB 32 columns
-constexpr uint32_t kSFColsPerStage = 48;
+constexpr uint32_t kSFColsPerStage = 12 * kAtoms;  // SFA 4 columns + SFB 8 columns per K = 64
 
 struct GemmArgs {
     Groups gr;              // A row groups
@@ -231,7 +237,14 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float* va,
     }
 }
 
-// 16 / 32 consecutive TMEM columns of this warp's 32 lanes from registers.
+// 8 / 16 / 32 consecutive TMEM columns of this warp's 32 lanes from registers.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v)
 {
     asm volatile(
@@ -461,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 for (int kt = 0; kt < num_kt; ++kt) {
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1, a, abrt, 1)) break;
                     const int kleft = a.ktot - kt * kBK;
-                    const int n_atoms = kleft >= kBK ? 4 : (kleft + 63) / 64;
+                    const int n_atoms = kleft >= kBK ? kAtoms : (kleft + 63) / 64;
                     uint8_t* sA = smem + stage * kStageBytes;
                     uint8_t* sB = sA + kABytes;
                     uint8_t* sSFA = sB + kBBytes;
@@ -470,14 +483,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     // own A tile and scales; this CTA's halves of the weight tile and their scales
                     // into every CTA of the cluster (the peer sends the other half)
                     tma_load_2d(sA, &tmap_a, kt * (kBK / 2), T.lrow0, &full_bar[stage]);
-                    const uint8_t* srcA = a.a_sf + ((int64_t)(T.lrow0 >> 7) * (a.a_sf_cols >> 2) + kt * 4) * 512;
+                    const uint8_t* srcA = a.a_sf + ((int64_t)(T.lrow0 >> 7) * (a.a_sf_cols >> 2) + kt * kAtoms) * 512;
                     bulk_load(sSFA, srcA, 512u * n_atoms, &full_bar[stage]);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         if (h % kCluster != (int)rank) continue;
                         const int64_t brow = h ? brow1 : brow0;
                         tma_load_2d_mc(sB + h * (kBBytes / 2), &tmap_b, kt * (kBK / 2), (int)brow, &full_bar[stage], pol_keep);
-                        const uint8_t* srcB = a.b_sf + ((brow >> 7) * (a.b_sf_cols >> 2) + kt * 4) * 512;
+                        const uint8_t* srcB = a.b_sf + ((brow >> 7) * (a.b_sf_cols >> 2) + kt * kAtoms) * 512;
                         bulk_load_mc(sSFB + h * (kSFBBytes / 2), srcB, 512u * n_atoms, &full_bar[stage]);
                     }
                     ++issued;
@@ -497,8 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         // implies its operand tiles are in shared memory), then up to 4 MMAs and one commit
         // that frees the stage.  Descriptors are precomputed; nothing else is in this loop.
         const uint32_t base = smem_u32(smem);
-        const uint64_t a_desc0 = smem_desc(base, 16, 1024, 2);
-        const uint64_t b_desc0 = smem_desc(base + kABytes, 16, 1024, 2);
+        const uint64_t a_desc0 = smem_desc(base, 16, kSBO, kSwizzleLayout);
+        const uint64_t b_desc0 = smem_desc(base + kABytes, 16, kSBO, kSwizzleLayout);
         constexpr uint64_t kStageStep = kStageBytes >> 4;
         int stage = 0;
         uint32_t phase = 0, acc_phase = 0;
@@ -511,16 +524,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 if (!mbar_wait(&sf_bar[stage], phase, a, abrt, 3)) { ok = false; break; }
                 tc_fence_after();
                 const int kleft = a.ktot - kt * kBK;
-                const int n_mma = kleft >= kBK ? 4 : (kleft + 63) / 64;
+                const int n_mma = kleft >= kBK ? kAtoms : (kleft + 63) / 64;
                 if (lane == 0) {
                     const uint64_t so = (uint64_t)stage * kStageStep;
                     const uint32_t sfa_t = tmem + kSFCol + stage * kSFColsPerStage;
-                    const uint32_t sfb_t = sfa_t + 16;
-                    const uint32_t acc = (kt > 0) ? 1u : 0u;
-                    mma_fp4(tmem + kAccCol, a_desc0 + so, b_desc0 + so, sfa_t, sfb_t, acc);
-                    if (n_mma > 1) mma_fp4(tmem + kAccCol, a_desc0 + so + 2, b_desc0 + so + 2, sfa_t + 4, sfb_t + 8, 1u);
-                    if (n_mma > 2) mma_fp4(tmem + kAccCol, a_desc0 + so + 4, b_desc0 + so + 4, sfa_t + 8, sfb_t + 16, 1u);
-                    if (n_mma > 3) mma_fp4(tmem + kAccCol, a_desc0 + so + 6, b_desc0 + so + 6, sfa_t + 12, sfb_t + 24, 1u);
+                    const uint32_t sfb_t = sfa_t + 4 * kAtoms;
+#pragma unroll
+                    for (int j = 0; j < kAtoms; ++j)  // K = 64 step j: 32 bytes into the tile rows
+                        if (j < n_mma)
+                            mma_fp4(tmem + kAccCol, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, sfa_t + 4 * j, sfb_t + 8 * j,
+                                    (kt > 0 || j > 0) ? 1u : 0u);
                     tc_commit_both(&empty_bar[stage]);  // the stage also holds the peer's weight half
                     issued_any = true;
                 }
@@ -539,9 +552,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         __syncwarp();
     } else if (warp < kFirstEpiWarp) {
         // ---------------- scale staging (warps 2-5, TMEM lane quarter = warp % 4): per K-tile,
-        // lane i loads row i (16 bytes) of each of the stage's 12 scale atoms from shared memory
-        // and stores them to its TMEM lane, SFA atom j at columns 4j, SFB atom j of weight half
-        // h at 16 + 8j + 4h; then fence and arrive on sf_bar for the MMA warp.
+        // lane i loads row i (16 bytes) of each of the stage's 3 * kAtoms scale atoms from shared
+        // memory and stores them to its TMEM lane, SFA atom j at columns 4j, SFB atom j of weight
+        // half h at 4 kAtoms + 8j + 4h; then fence and arrive on sf_bar for the MMA warp.
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
         int stage = 0;
         uint32_t phase = 0;
@@ -550,9 +563,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             for (int kt = 0; kt < num_kt; ++kt) {
                 if (!mbar_wait(&full_bar[stage], phase, a, abrt, 5)) { ok = false; break; }
                 const uint8_t* sf = smem + stage * kStageBytes + kABytes + kBBytes + lane * 16;
-                uint32_t va[16], vb[32];
+                uint32_t va[4 * kAtoms], vb[8 * kAtoms];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < kAtoms; ++j) {
                     const uint4 x = *reinterpret_cast<const uint4*>(sf + j * 512);
                     va[4 * j] = x.x; va[4 * j + 1] = x.y; va[4 * j + 2] = x.z; va[4 * j + 3] = x.w;
 #pragma unroll
@@ -562,8 +575,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     }
                 }
                 const uint32_t sfa_t = tmem + kSFCol + stage * kSFColsPerStage + lane_addr;
-                tmem_st16(sfa_t, va);
-                tmem_st32(sfa_t + 16, vb);
+                if constexpr (kAtoms == 4) {
+                    tmem_st16(sfa_t, va);
+                    tmem_st32(sfa_t + 16, vb);
+                } else {
+                    tmem_st8(sfa_t, va);
+                    tmem_st16(sfa_t + 8, vb);
+                }
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
@@ -677,8 +695,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode()
     return fn;
 }
 
-// 2D byte tensor map over FP4 codes, 128-byte swizzle; box = 128 bytes x box_rows rows
-// (box_rows = 1 for the four-row gathers).
+// 2D byte tensor map over FP4 codes, swizzled as the K-tile's row width (kRowBytes); box =
+// kRowBytes x box_rows rows.
 static nvq_status make_map(CUtensorMap* m, const void* base, int64_t inner_bytes, int64_t rows, int64_t ld,
                            uint32_t box_rows = 128)
 {
@@ -686,10 +704,11 @@ static nvq_status make_map(CUtensorMap* m, const void* base, int64_t inner_bytes
     NVQ_CHECK_ARG(enc, NVQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[2] = {(cuuint64_t)inner_bytes, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)ld};
-    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t box[2] = {(cuuint32_t)kRowBytes, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, kRowBytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     NVQ_CHECK_ARG(r == CUDA_SUCCESS, NVQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return NVQ_OK;
