@@ -163,3 +163,25 @@ def test_moe_layer_small_uniform_topk8(L):
 
 def test_moe_layer_without_rac(L):
     _check_layer(L, T=130, H=256, E=4, topk=2, I=128, k=0, routing="uniform", seed=23)
+
+
+@pytest.mark.parametrize("use_graph", [True, False])
+def test_host_pipeline_matches_direct_forward(L, use_graph):
+    """HostPipeline (inputs copied up, forward, output copied back, neighbouring steps
+    overlapped on three streams) returns exactly the layer's direct forward output."""
+    from nvfp4_w4a4_quantized_quantize_gb300.layers import MoERacLayer
+    from nvfp4_w4a4_quantized_quantize_gb300.pipeline import HostPipeline
+    cfg = wl.MoELayer("t", T=200, H=256, E=8, topk=2, I=128, k=16, seed=31, routing="zipf", n_outliers=3)
+    x_bits, ids, tw, _ = cfg.make_tokens()
+    w13_bits, w2_bits = cfg.make_weights()
+    layer = MoERacLayer(bf16_tensor(w13_bits.reshape(8 * 256, 256)).view(8, 256, 256),
+                        bf16_tensor(w2_bits.reshape(8 * 256, 128)).view(8, 256, 128), 16, 2, 200)
+    ref = torch.empty(200, 256, dtype=torch.bfloat16, device="cuda")
+    layer.forward(bf16_tensor(x_bits), torch.from_numpy(ids).cuda(), torch.from_numpy(tw).cuda(), ref)
+    torch.cuda.synchronize()
+    pipe = HostPipeline(layer, 200, use_graph=use_graph)
+    x_h = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_h = torch.zeros(200, 256, dtype=torch.bfloat16).pin_memory()
+    ms = pipe.run(x_h, torch.from_numpy(ids).pin_memory(), torch.from_numpy(tw).pin_memory(), out_h, 5)
+    assert ms > 0 and L.device_status() == (0, 0)
+    assert torch.equal(out_h.view(torch.int16), ref.cpu().view(torch.int16))
