@@ -18,7 +18,7 @@ namespace nvq {
 
 // Pairs are cut into units of 256 consecutive (token, slot) pairs; one warp owns a unit.
 static constexpr int kUnit = 256;
-static constexpr int kWarpsPerCta = 8;
+static constexpr int kWarpsPerCta = 2;  // 256 CTAs for the 512 units of 131072 pairs: every SM busy
 
 // Per-unit histogram of experts: counts[unit][G].
 __global__ void dispatch_hist_kernel(const int32_t* __restrict__ ids, int64_t n, int G, int32_t* __restrict__ counts)
@@ -137,21 +137,31 @@ __global__ void dispatch_scatter_kernel(const int32_t* __restrict__ ids, const f
     for (int e = lane; e < G; e += 32) base[e] = grp_off[e] + counts[unit * G + e];
     __syncwarp();
     const int64_t p1 = min(p0 + kUnit, n);
-    for (int64_t pb = p0; pb < p1; pb += 32) {
-        const int64_t p = pb + lane;
+    // the unit's expert ids and weights, all loads in flight before the ranking
+    constexpr int kPer = kUnit / 32;
+    int ev[kPer];
+    float wv[kPer];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        const int64_t p = p0 + q * 32 + lane;
+        ev[q] = p < p1 ? ids[p] : 0;
+        wv[q] = (p < p1 && w) ? w[p] : 1.0f;
+    }
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        const int64_t p = p0 + q * 32 + lane;
         const bool valid = p < p1;
         const unsigned act = __ballot_sync(0xffffffffu, valid);
-        int e = 0, rank = 0;
+        const int e = ev[q];
+        int rank = 0;
         unsigned peers = 0;
-        int64_t pos = 0;
         if (valid) {
-            e = ids[p];
             peers = __match_any_sync(act, e);
             rank = __popc(peers & ((1u << lane) - 1u));
-            pos = base[e] + rank;
+            const int64_t pos = base[e] + rank;
             row_src[pos] = (int32_t)p;
             row_of[p] = pos;
-            if (row_w) row_w[pos] = w ? w[p] : 1.0f;
+            if (row_w) row_w[pos] = wv[q];
         }
         __syncwarp();
         if (valid && rank == 0) base[e] += __popc(peers);
