@@ -144,6 +144,13 @@ class MoERacLayer:
         self.scores2 = torch.zeros(E, self.I, dtype=torch.int64, device=dev)
         self.idx2 = torch.zeros(E, max(k, 1), dtype=torch.int32, device=dev)
         self.y = torch.zeros(cap, self.H, dtype=torch.bfloat16, device=dev)
+        # side stream for the work that does not depend on dispatch (token quantization and
+        # selection) or on the gather (the gate/up weight tail); events fork and join it, so
+        # a CUDA graph captured around forward() holds the two branches in parallel
+        self.side = torch.cuda.Stream(device=dev)
+        self.ev_fork = torch.cuda.Event()
+        self.ev_tok = torch.cuda.Event()
+        self.ev_wt = torch.cuda.Event()
 
     def kernel_launches_per_step(self) -> int:
         """Kernels one forward() launches: dispatch 4; tokens: amax + quantize 2, selection and
@@ -162,48 +169,56 @@ class MoERacLayer:
         T = x.shape[0]
         k, E, H, I = self.k, self.E, self.H, self.I
         st = torch.cuda.current_stream() if stream is None else stream
+        side = self.side
 
-        def mark(name, pos):
+        def mark(name, pos, on=None):
             if events is not None:
                 ev = events.setdefault(name, (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
-                ev[pos].record(st)
+                ev[pos].record(st if on is None else on)
 
-        L.moe_dispatch(topk_ids, topk_w, E, self.grp_off, self.grp_rows, self.row_src, self.row_of, self.row_w,
-                       self.ws, stream=stream)
-        # gate/up input: per-token quantization, one tensor scale, one channel set
-        mark("quant_rac_tokens", 0)
+        # fork: token quantization + selection on the side stream, dispatch on the main one
+        self.ev_fork.record(st)
+        side.wait_event(self.ev_fork)
+        mark("quant_rac_tokens", 0, side)
         L.nvfp4_quantize(x, self.a_tok.codes, self.a_tok.sf, self.a_tok.sf_cols, self.a_tok.tscale,
-                         scores=self.scores1 if k else None, zero_pad=(k == 0), stream=stream)
+                         scores=self.scores1 if k else None, zero_pad=(k == 0), stream=side)
         if k:
             L.rac_select_quantize(x, self.a_tok.tscale, self.scores1, k, self.a_tok.codes, self.a_tok.sf,
-                                  self.a_tok.sf_cols, self.idx1, stream=stream)
-        mark("quant_rac_tokens", 1)
-        L.nvfp4_gather_rows(self.a_tok.codes, self.a_tok.sf, self.a_tok.sf_cols, T, self.row_src, self.topk, H + k,
-                            self.a_routed.codes, self.a_routed.sf, stream=stream)
+                                  self.a_tok.sf_cols, self.idx1, stream=side)
+        mark("quant_rac_tokens", 1, side)
+        self.ev_tok.record(side)
+        L.moe_dispatch(topk_ids, topk_w, E, self.grp_off, self.grp_rows, self.row_src, self.row_of, self.row_w,
+                       self.ws, stream=st)
+        st.wait_event(self.ev_tok)
+        # the gate/up weight tail (needs the selection only) beside the gather
         if k:
-            _weight_tail(self.w13, self.w13_cm, E, 2 * I, k, self.idx1, stream=stream)
+            _weight_tail(self.w13, self.w13_cm, E, 2 * I, k, self.idx1, stream=side)
+        self.ev_wt.record(side)
+        L.nvfp4_gather_rows(self.a_tok.codes, self.a_tok.sf, self.a_tok.sf_cols, T, self.row_src, self.topk, H + k,
+                            self.a_routed.codes, self.a_routed.sf, stream=st)
+        st.wait_event(self.ev_wt)  # join
         mark("gemm_gate_up", 0)
         L.w4a4_rac_grouped_gemm(self.a_routed.codes, self.a_routed.sf, self.a_routed.sf_cols, self.a_tok.tscale,
                                 self.w13.codes, self.w13.sf, self.w13.sf_cols, self.w13.tscale, 2 * I, H, k,
                                 None, self.h, groups=E, grp_off=self.grp_off, grp_rows=self.grp_rows,
-                                rows=self.cap, epilogue=L.NVQ_EPI_SWIGLU, out_tscale=self.a2.tscale, stream=stream)
+                                rows=self.cap, epilogue=L.NVQ_EPI_SWIGLU, out_tscale=self.a2.tscale, stream=st)
         mark("gemm_gate_up", 1)
         # down input: per-expert tensor scale (amax of h measured by the gate/up epilogue) and
         # channel set
         L.nvfp4_quantize(self.h, self.a2.codes, self.a2.sf, self.a2.sf_cols, self.a2.tscale,
                          scores=self.scores2 if k else None, grp_off=self.grp_off, grp_rows=self.grp_rows,
-                         groups=E, zero_pad=(k == 0), amax_given=True, stream=stream)
+                         groups=E, zero_pad=(k == 0), amax_given=True, stream=st)
         if k:
             L.rac_select_quantize(self.h, self.a2.tscale, self.scores2, k, self.a2.codes, self.a2.sf,
                                   self.a2.sf_cols, self.idx2, grp_off=self.grp_off, grp_rows=self.grp_rows,
-                                  groups=E, stream=stream)
-            _weight_tail(self.w2, self.w2_cm, E, H, k, self.idx2, idx_per_group=True, stream=stream)
+                                  groups=E, stream=st)
+            _weight_tail(self.w2, self.w2_cm, E, H, k, self.idx2, idx_per_group=True, stream=st)
         mark("gemm_down", 0)
         L.w4a4_rac_grouped_gemm(self.a2.codes, self.a2.sf, self.a2.sf_cols, self.a2.tscale, self.w2.codes,
                                 self.w2.sf, self.w2.sf_cols, self.w2.tscale, H, I, k, None,
                                 self.y, groups=E, grp_off=self.grp_off, grp_rows=self.grp_rows, rows=self.cap,
                                 a_scale_per_group=True, idx_per_group=True, epilogue=L.NVQ_EPI_ROW_SCALE,
-                                row_w=self.row_w, stream=stream)
+                                row_w=self.row_w, stream=st)
         mark("gemm_down", 1)
-        L.moe_combine(self.y, self.row_of, T, self.topk, H, out, stream=stream)
+        L.moe_combine(self.y, self.row_of, T, self.topk, H, out, stream=st)
         return out
