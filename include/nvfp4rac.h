@@ -158,6 +158,28 @@ nvq_status rac_select_quantize(const void* x, int64_t rows, int64_t K, int64_t l
                                int32_t* idx, void* stream);
 
 /*
+ * rac_select -- the selection half of rac_select_quantize (QUADS Eq. (24)): per group, the k
+ * channels with the largest score, ties to the lower channel index, ascending in idx.
+ *   scores    uint64 [groups][K] from nvfp4_quantize.   idx  int32 [groups][k] out.
+ *   16 <= k <= min(K, 512), k % 16 == 0.
+ */
+nvq_status rac_select(const uint64_t* scores, int64_t K, int32_t groups, int32_t k, int32_t* idx,
+                      void* stream);
+
+/*
+ * rac_residual_tail -- the second-pass half of rac_select_quantize (QUADS Eq. (21)): the
+ * residual on the channels in idx (from rac_select, or any ascending set per group) quantized
+ * into columns [K, K + k) of codes and scale columns [K / 16, (K + k) / 16) of sf, the scale
+ * padding beyond zeroed.  Arguments as for rac_select_quantize; idx may be NULL when k == 0.
+ * Split from the selection so that work needing only idx (the weight tail) can run beside it.
+ */
+nvq_status rac_residual_tail(const void* x, int64_t rows, int64_t K, int64_t ldx,
+                             const int64_t* grp_off, const int64_t* grp_rows, int32_t groups,
+                             const nvq_tensor_scale* tscale, const int32_t* idx, int32_t k,
+                             uint8_t* codes, int64_t ld_codes, uint8_t* sf, int64_t sf_cols,
+                             void* stream);
+
+/*
  * weight_qdq -- the trainer-side QDQ_W of QUADS Eq. (12): for each of G weight tensors
  * W_g = w[g] ([N][K] bf16, tensor g at w + g * N * ldw elements) the same quantizer as
  * nvfp4_quantize with one tensor scale per tensor, so that its codes and scales are the

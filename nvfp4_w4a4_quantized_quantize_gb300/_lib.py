@@ -28,6 +28,8 @@ _SIGS = {
     "weight_qdq": ([_P, _I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _I32, _P], C.c_int),
     "w4a4_rac_grouped_gemm": ([_I32, _P, _P, _I64, _P, _I64, _P, _I64, _P, _I32, _P, _I64, _P, _I64, _P, _I64, _I64,
                                _I32, _P, _I32, _I32, _P, _P, _I64, _P, _P], C.c_int),
+    "rac_select": ([_P, _I64, _I32, _I32, _P, _P], C.c_int),
+    "rac_residual_tail": ([_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _I32, _P, _I64, _P, _I64, _P], C.c_int),
     "rac_weight_tail": ([_I32, _I64, _I64, _I32, _P, _I32, _P, _I64, _P, _I64, _P, _P, _P, _P], C.c_int),
     "nvfp4_channel_major": ([_I32, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _P], C.c_int),
     "moe_capacity": ([_I64, _I32, _I32], _I64),
@@ -146,6 +148,19 @@ def weight_qdq(w, groups, N, K, codes, sf, sf_cols_, tscale, w_hat=None, w_hat_d
     _check("weight_qdq", LIB.weight_qdq(
         _ptr(w), groups, N, K, w.stride(-2), _ptr(codes), codes.stride(0), _ptr(sf), sf_cols_, _ptr(tscale),
         _ptr(w_hat), w_hat_dtype, _stream(stream)))
+
+
+def rac_select(scores, K, k, idx, groups=1, stream=None):
+    _check("rac_select", LIB.rac_select(_ptr(scores), K, groups, k, _ptr(idx), _stream(stream)))
+
+
+def rac_residual_tail(x, tscale, idx, k, codes, sf, sf_cols_, grp_off=None, grp_rows=None, groups=1, rows=None, K=None,
+                      stream=None):
+    rows = x.shape[0] if rows is None else rows
+    K = x.shape[1] if K is None else K
+    _check("rac_residual_tail", LIB.rac_residual_tail(
+        _ptr(x), rows, K, x.stride(0), _ptr(grp_off), _ptr(grp_rows), groups, _ptr(tscale), _ptr(idx), k,
+        _ptr(codes), codes.stride(0), _ptr(sf), sf_cols_, _stream(stream)))
 
 
 def w4a4_rac_grouped_gemm(a_codes, a_sf, a_sf_cols, a_tscale, b_codes, b_sf, b_sf_cols, b_tscale, N, K, k, idx,

@@ -432,30 +432,37 @@ nvq_status weight_tail_impl(uint8_t* codes, int64_t ld_codes, uint8_t* sf, int64
 
 using namespace nvq;
 
-extern "C" nvq_status rac_select_quantize(const void* x, int64_t rows, int64_t K, int64_t ldx, const int64_t* grp_off,
-                                          const int64_t* grp_rows, int32_t groups, const nvq_tensor_scale* tscale,
-                                          const uint64_t* scores, int32_t k, uint8_t* codes, int64_t ld_codes,
-                                          uint8_t* sf, int64_t sf_cols, int32_t* idx, void* stream)
+static nvq_status check_rac_args(const char* fn, const void* x, int64_t rows, int64_t K, int64_t ldx,
+                                 const int64_t* grp_off, int32_t groups, const nvq_tensor_scale* tscale, int32_t k,
+                                 const uint8_t* codes, int64_t ld_codes, const uint8_t* sf, int64_t sf_cols)
 {
-    NVQ_CHECK_ARG(x && codes && sf && tscale, NVQ_ERR_ARG, "rac_select_quantize: null pointer argument");
-    NVQ_CHECK_ARG(k == 0 || (scores && idx), NVQ_ERR_ARG, "rac_select_quantize: scores and idx are required when k > 0");
-    NVQ_CHECK_ARG(rows >= 1 && rows <= (1ll << 24), NVQ_ERR_SHAPE, "rac_select_quantize: rows outside [1, 2^24]");
-    NVQ_CHECK_ARG(K >= 16 && K <= 8192 && K % 16 == 0, NVQ_ERR_SHAPE, "rac_select_quantize: K must be a multiple of 16 in [16, 8192]");
+    NVQ_CHECK_ARG(x && codes && sf && tscale, NVQ_ERR_ARG, "%s: null pointer argument", fn);
+    NVQ_CHECK_ARG(rows >= 1 && rows <= (1ll << 24), NVQ_ERR_SHAPE, "%s: rows outside [1, 2^24]", fn);
+    NVQ_CHECK_ARG(K >= 16 && K <= 8192 && K % 16 == 0, NVQ_ERR_SHAPE, "%s: K must be a multiple of 16 in [16, 8192]", fn);
     NVQ_CHECK_ARG(k >= 0 && k <= K && k % 16 == 0 && k <= 512, NVQ_ERR_SHAPE,
-                  "rac_select_quantize: k=%d must be a multiple of 16 in [0, min(K, 512)]", k);
-    NVQ_CHECK_ARG(groups >= 1 && groups <= 4096, NVQ_ERR_SHAPE, "rac_select_quantize: groups outside [1, 4096]");
-    NVQ_CHECK_ARG(grp_off || groups == 1 || rows % groups == 0, NVQ_ERR_SHAPE, "rac_select_quantize: rows not divisible by groups");
-    NVQ_CHECK_ARG(ldx >= K && ldx % 8 == 0, NVQ_ERR_ALIGN, "rac_select_quantize: ldx must be >= K and a multiple of 8");
-    NVQ_CHECK_ARG(ld_codes >= (K + k) / 2 && ld_codes % 16 == 0, NVQ_ERR_ALIGN, "rac_select_quantize: ld_codes must be >= (K+k)/2 and a multiple of 16");
-    NVQ_CHECK_ARG(sf_cols >= (K + k) / 16 && sf_cols % 4 == 0, NVQ_ERR_SHAPE, "rac_select_quantize: sf_cols must be >= (K+k)/16 and a multiple of 4");
-    NVQ_CHECK_ARG(aligned(codes, 16), NVQ_ERR_ALIGN, "rac_select_quantize: codes must be 16-byte aligned");
-    set_error("");
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    Groups gr{grp_off, grp_rows, groups, rows};
-    if (k > 0) {
-        topk_kernel<<<groups, kTopkThreads, 0, st>>>(reinterpret_cast<const unsigned long long*>(scores), (int)K, k, idx);
-        NVQ_LAUNCH_CHECK("topk_kernel");
-    }
+                  "%s: k=%d must be a multiple of 16 in [0, min(K, 512)]", fn, k);
+    NVQ_CHECK_ARG(groups >= 1 && groups <= 4096, NVQ_ERR_SHAPE, "%s: groups outside [1, 4096]", fn);
+    NVQ_CHECK_ARG(grp_off || groups == 1 || rows % groups == 0, NVQ_ERR_SHAPE, "%s: rows not divisible by groups", fn);
+    NVQ_CHECK_ARG(ldx >= K && ldx % 8 == 0, NVQ_ERR_ALIGN, "%s: ldx must be >= K and a multiple of 8", fn);
+    NVQ_CHECK_ARG(ld_codes >= (K + k) / 2 && ld_codes % 16 == 0, NVQ_ERR_ALIGN,
+                  "%s: ld_codes must be >= (K+k)/2 and a multiple of 16", fn);
+    NVQ_CHECK_ARG(sf_cols >= (K + k) / 16 && sf_cols % 4 == 0, NVQ_ERR_SHAPE,
+                  "%s: sf_cols must be >= (K+k)/16 and a multiple of 4", fn);
+    NVQ_CHECK_ARG(aligned(codes, 16), NVQ_ERR_ALIGN, "%s: codes must be 16-byte aligned", fn);
+    return NVQ_OK;
+}
+
+static nvq_status launch_topk(const uint64_t* scores, int64_t K, int32_t groups, int32_t k, int32_t* idx, cudaStream_t st)
+{
+    topk_kernel<<<groups, kTopkThreads, 0, st>>>(reinterpret_cast<const unsigned long long*>(scores), (int)K, k, idx);
+    NVQ_LAUNCH_CHECK("topk_kernel");
+    return NVQ_OK;
+}
+
+static nvq_status launch_act_tail(const void* x, int64_t rows, int64_t K, int64_t ldx, Groups gr,
+                                  const nvq_tensor_scale* tscale, const int32_t* idx, int32_t k, uint8_t* codes,
+                                  int64_t ld_codes, uint8_t* sf, int64_t sf_cols, cudaStream_t st)
+{
     const int64_t tiles = (rows + kTailRows - 1) / kTailRows;
     // split a row's tail blocks over threads until there are ~8 CTAs' worth of threads per SM
     int sms = 148, dev = 0;
@@ -466,9 +473,47 @@ extern "C" nvq_status rac_select_quantize(const void* x, int64_t rows, int64_t K
     while (bsplit < nbt && bsplit < 8 && tiles * bsplit < (int64_t)sms * 8) bsplit *= 2;
     if (bsplit > nbt) bsplit = nbt;
     act_tail_kernel<<<(unsigned)tiles, kTailRows * bsplit, 0, st>>>(static_cast<const __nv_bfloat16*>(x), ldx, (int)K,
-                                                                       k, gr, tscale, idx, codes, ld_codes, sf, sf_cols, bsplit);
+                                                                   k, gr, tscale, idx, codes, ld_codes, sf, sf_cols, bsplit);
     NVQ_LAUNCH_CHECK("act_tail_kernel");
     return NVQ_OK;
+}
+
+extern "C" nvq_status rac_select_quantize(const void* x, int64_t rows, int64_t K, int64_t ldx, const int64_t* grp_off,
+                                          const int64_t* grp_rows, int32_t groups, const nvq_tensor_scale* tscale,
+                                          const uint64_t* scores, int32_t k, uint8_t* codes, int64_t ld_codes,
+                                          uint8_t* sf, int64_t sf_cols, int32_t* idx, void* stream)
+{
+    nvq_status s = check_rac_args("rac_select_quantize", x, rows, K, ldx, grp_off, groups, tscale, k, codes, ld_codes, sf, sf_cols);
+    if (s != NVQ_OK) return s;
+    NVQ_CHECK_ARG(k == 0 || (scores && idx), NVQ_ERR_ARG, "rac_select_quantize: scores and idx are required when k > 0");
+    set_error("");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (k > 0 && (s = launch_topk(scores, K, groups, k, idx, st)) != NVQ_OK) return s;
+    return launch_act_tail(x, rows, K, ldx, Groups{grp_off, grp_rows, groups, rows}, tscale, idx, k, codes, ld_codes, sf,
+                           sf_cols, st);
+}
+
+extern "C" nvq_status rac_select(const uint64_t* scores, int64_t K, int32_t groups, int32_t k, int32_t* idx, void* stream)
+{
+    NVQ_CHECK_ARG(scores && idx, NVQ_ERR_ARG, "rac_select: null pointer argument");
+    NVQ_CHECK_ARG(K >= 16 && K <= 8192 && K % 16 == 0, NVQ_ERR_SHAPE, "rac_select: K must be a multiple of 16 in [16, 8192]");
+    NVQ_CHECK_ARG(k >= 16 && k <= K && k % 16 == 0 && k <= 512, NVQ_ERR_SHAPE, "rac_select: bad k=%d", k);
+    NVQ_CHECK_ARG(groups >= 1 && groups <= 4096, NVQ_ERR_SHAPE, "rac_select: groups outside [1, 4096]");
+    set_error("");
+    return launch_topk(scores, K, groups, k, idx, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" nvq_status rac_residual_tail(const void* x, int64_t rows, int64_t K, int64_t ldx, const int64_t* grp_off,
+                                        const int64_t* grp_rows, int32_t groups, const nvq_tensor_scale* tscale,
+                                        const int32_t* idx, int32_t k, uint8_t* codes, int64_t ld_codes, uint8_t* sf,
+                                        int64_t sf_cols, void* stream)
+{
+    nvq_status s = check_rac_args("rac_residual_tail", x, rows, K, ldx, grp_off, groups, tscale, k, codes, ld_codes, sf, sf_cols);
+    if (s != NVQ_OK) return s;
+    NVQ_CHECK_ARG(k == 0 || idx, NVQ_ERR_ARG, "rac_residual_tail: idx is required when k > 0");
+    set_error("");
+    return launch_act_tail(x, rows, K, ldx, Groups{grp_off, grp_rows, groups, rows}, tscale, idx, k, codes, ld_codes, sf,
+                           sf_cols, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" nvq_status nvfp4_channel_major(int32_t groups, int64_t N, int64_t K, const uint8_t* b_codes, int64_t ldb,

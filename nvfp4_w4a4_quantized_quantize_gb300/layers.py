@@ -151,6 +151,8 @@ class MoERacLayer:
         self.ev_fork = torch.cuda.Event()
         self.ev_tok = torch.cuda.Event()
         self.ev_wt = torch.cuda.Event()
+        self.ev_sel2 = torch.cuda.Event()
+        self.ev_wt2 = torch.cuda.Event()
 
     def kernel_launches_per_step(self) -> int:
         """Kernels one forward() launches: dispatch 4; tokens: amax + quantize 2, selection and
@@ -209,10 +211,15 @@ class MoERacLayer:
                          scores=self.scores2 if k else None, grp_off=self.grp_off, grp_rows=self.grp_rows,
                          groups=E, zero_pad=(k == 0), amax_given=True, stream=st)
         if k:
-            L.rac_select_quantize(self.h, self.a2.tscale, self.scores2, k, self.a2.codes, self.a2.sf,
-                                  self.a2.sf_cols, self.idx2, grp_off=self.grp_off, grp_rows=self.grp_rows,
-                                  groups=E, stream=st)
-            _weight_tail(self.w2, self.w2_cm, E, H, k, self.idx2, idx_per_group=True, stream=st)
+            # selection, then the down weight tail (needs idx2 only) beside the residual tail of h
+            L.rac_select(self.scores2, I, k, self.idx2, groups=E, stream=st)
+            self.ev_sel2.record(st)
+            side.wait_event(self.ev_sel2)
+            _weight_tail(self.w2, self.w2_cm, E, H, k, self.idx2, idx_per_group=True, stream=side)
+            self.ev_wt2.record(side)
+            L.rac_residual_tail(self.h, self.a2.tscale, self.idx2, k, self.a2.codes, self.a2.sf, self.a2.sf_cols,
+                                grp_off=self.grp_off, grp_rows=self.grp_rows, groups=E, stream=st)
+            st.wait_event(self.ev_wt2)
         mark("gemm_down", 0)
         L.w4a4_rac_grouped_gemm(self.a2.codes, self.a2.sf, self.a2.sf_cols, self.a2.tscale, self.w2.codes,
                                 self.w2.sf, self.w2.sf_cols, self.w2.tscale, H, I, k, None,

@@ -305,3 +305,31 @@ def test_quantize_with_given_amax_equals_measured(L):
     assert torch.equal(ts.view(torch.int32), a["ts"].view(torch.int32))
     assert np.array_equal(codes.cpu().numpy(), a["codes"]) and torch.equal(sf, a["sf"])
     assert np.array_equal(scores.cpu().numpy().view(np.uint64), a["scores"])
+
+
+def test_select_and_residual_tail_split_equals_combined(L):
+    """rac_select followed by rac_residual_tail writes exactly what rac_select_quantize writes."""
+    counts = [300, 0, 129]
+    off = [0, 384, 384, 640]
+    K, k = 768, 32
+    x = np.zeros((640, K), np.uint16)
+    for g, c in enumerate(counts):
+        if c:
+            xg, _ = wl.activations(c, K, seed=60 + g, n_outliers=8, outlier_gain=15.0)
+            x[off[g]:off[g] + c] = xg
+    a = _gpu_quant(L, x, k=k, groups=3, grp_off=off, grp_rows=counts)
+    xt = bf16_tensor(x)
+    go = torch.tensor(off, dtype=torch.int64, device="cuda")
+    gr = torch.tensor(counts, dtype=torch.int64, device="cuda")
+    sf_cols = a["sf_cols"]
+    codes = torch.full((640, a["codes"].shape[1]), 0xAB, dtype=torch.uint8, device="cuda")
+    sf = torch.full_like(a["sf"], 0xCD)
+    ts = torch.zeros(3, 4, dtype=torch.float32, device="cuda")
+    scores = torch.zeros(3, K, dtype=torch.int64, device="cuda")
+    L.nvfp4_quantize(xt, codes, sf, sf_cols, ts, scores=scores, grp_off=go, grp_rows=gr, groups=3)
+    idx = torch.zeros(3, k, dtype=torch.int32, device="cuda")
+    L.rac_select(scores, K, k, idx, groups=3)
+    L.rac_residual_tail(xt, ts, idx, k, codes, sf, sf_cols, grp_off=go, grp_rows=gr, groups=3)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy(), a["idx"])
+    assert np.array_equal(codes.cpu().numpy(), a["codes"]) and torch.equal(sf, a["sf"])
