@@ -7,10 +7,11 @@
 //                        8 in flight per thread, one atomicMax per (CTA, group run);
 //   quant_score_kernel   codes + blocked E4M3 scales + residual + integer channel score (+ the
 //                        dequantized values for the trainer-side QDQ).  One CTA of 16 warps per
-//                        SM: one lane streams the CTA's band of rows into an 8-stage shared
-//                        memory ring with cp.async.bulk (up to 96 KB in flight per SM,
-//                        independent of register pressure), every thread quantizes one
-//                        16-element block per row from shared memory.  The CTA re-reads the
+//                        SM: one lane streams the CTA's band of rows into a 5-stage shared
+//                        memory ring of up to 32 KB stages with cp.async.bulk (up to 96 KB in
+//                        flight per SM, independent of register pressure), every thread
+//                        quantizes one 16-element block per row from shared memory, two or
+//                        more rows per stage (fewer hand-offs per element).  The CTA re-reads the
 //                        rows amax_kernel's CTAs just streamed, so most of that second read is
 //                        served by L2.
 #include <cuda_bf16.h>
@@ -88,8 +89,8 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const __nv_bfloat16*
 }
 
 // ------------------------------------------------------------------------ quantize + score
-static constexpr int kQStages = 8;
-static constexpr int kQStageBytes = 16384;
+static constexpr int kQStages = 5;
+static constexpr int kQStageBytes = 32768;  // capacity; a stage holds whole groups of rows_per_iter rows
 static constexpr int kQCompute = 512;  // 16 warps: one thread per 16-element block up to K = 8192
 static constexpr int kQThreads = kQCompute;
 static constexpr int kQAhead = kQStages - 2;  // stages the loads run ahead of the compute
@@ -230,8 +231,11 @@ __device__ __forceinline__ bool cursor_issue(const QuantArgs& qa, LoadCursor& c,
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa32(&full_bar[s])),
                  "r"((uint32_t)(nr * row_bytes))
                  : "memory");
-    for (int j = 0; j < nr; ++j)
-        q_bulk_row(ring + s * kQStageBytes + j * row_bytes, qa.x + (c.r + j) * qa.ldx, row_bytes, &full_bar[s]);
+    if (qa.ldx * 2 == row_bytes)  // contiguous rows: the whole stage in one copy
+        q_bulk_row(ring + s * kQStageBytes, qa.x + c.r * qa.ldx, (uint32_t)(nr * row_bytes), &full_bar[s]);
+    else
+        for (int j = 0; j < nr; ++j)
+            q_bulk_row(ring + s * kQStageBytes + j * row_bytes, qa.x + (c.r + j) * qa.ldx, row_bytes, &full_bar[s]);
     ++c.it;
     c.r += R;
     if (c.r >= c.b) {
@@ -259,7 +263,10 @@ __global__ void __launch_bounds__(kQThreads, 1) quant_score_kernel(const QuantAr
     const int K = qa.K;
     const int nb = K / 16;
     const int row_bytes = 2 * K;
-    const int R = max(1, kQStageBytes / row_bytes);  // rows per stage
+    // rows per stage: whole groups of the rows_per_iter rows the threads take side by side, as
+    // many as fit, so every thread handles the same number of rows per stage
+    const int rpi = (BPT == 1) ? (kQCompute / nb) : 1;
+    const int R = rpi * max(1, kQStageBytes / (rpi * row_bytes));
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     unsigned long long* red_scores = reinterpret_cast<unsigned long long*>(ring + kQStages * kQStageBytes);
