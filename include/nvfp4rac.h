@@ -322,15 +322,17 @@ nvq_status moe_dispatch_static_scratch(const int32_t* topk_ids, const float* top
                                        void* stream);
 
 /*
- * nvfp4_gather_rows -- copies quantized rows (codes and blocked scales of K_tot columns) into
- * the routed layout: out row r = source row row_src[r] / topk, padding rows (row_src < 0) get
- * zero codes and zero scales.  out_sf uses the same sf_cols as sf.  With out_codes NULL only
- * the scales are copied.
+ * nvfp4_gather_rows -- copies quantized rows (codes of columns [col0, ktot) and the blocked
+ * scale atoms covering them) into the routed layout: out row r = source row row_src[r] / topk,
+ * padding rows (row_src < 0) get zero codes and zero scales.  out_sf uses the same sf_cols as
+ * sf.  With out_codes NULL only the scales are copied.  col0 % 64 == 0 (a scale atom holds 64
+ * columns); two calls with [0, K) and [K, K + k) copy the main columns and the RAC tail
+ * separately, so the first can run before the tail exists.
  */
 nvq_status nvfp4_gather_rows(const uint8_t* codes, int64_t ld_codes, const uint8_t* sf,
                              int64_t sf_cols, int64_t src_rows, const int32_t* row_src,
-                             int32_t topk, int64_t capacity, int64_t ktot, uint8_t* out_codes,
-                             int64_t ld_out, uint8_t* out_sf, void* stream);
+                             int32_t topk, int64_t capacity, int64_t ktot, int64_t col0,
+                             uint8_t* out_codes, int64_t ld_out, uint8_t* out_sf, void* stream);
 
 /*
  * moe_combine -- out[t, :] = bf16( sum over slots s = 0..topk-1, in slot order, in fp32, of

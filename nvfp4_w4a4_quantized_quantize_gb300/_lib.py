@@ -36,7 +36,7 @@ _SIGS = {
     "moe_dispatch_workspace_size": ([_I64, _I32, _I32], C.c_size_t),
     "moe_dispatch": ([_P, _P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _I64, _P, C.c_size_t, _P], C.c_int),
     "moe_dispatch_static_scratch": ([_P, _P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _I64, _P], C.c_int),
-    "nvfp4_gather_rows": ([_P, _I64, _P, _I64, _I64, _P, _I32, _I64, _I64, _P, _I64, _P, _P], C.c_int),
+    "nvfp4_gather_rows": ([_P, _I64, _P, _I64, _I64, _P, _I32, _I64, _I64, _I64, _P, _I64, _P, _P], C.c_int),
     "moe_combine": ([_P, _I64, _P, _I64, _I32, _I64, _P, _I64, _P], C.c_int),
 }
 
@@ -205,9 +205,9 @@ def moe_dispatch_static_scratch(topk_ids, topk_w, groups, grp_off, grp_rows, row
         _ptr(row_w), row_src.numel(), _stream(stream)))
 
 
-def nvfp4_gather_rows(codes, sf, sf_cols_, src_rows, row_src, topk, ktot, out_codes, out_sf, stream=None):
+def nvfp4_gather_rows(codes, sf, sf_cols_, src_rows, row_src, topk, ktot, out_codes, out_sf, col0=0, stream=None):
     _check("nvfp4_gather_rows", LIB.nvfp4_gather_rows(
-        _ptr(codes), codes.stride(0), _ptr(sf), sf_cols_, src_rows, _ptr(row_src), topk, row_src.numel(), ktot,
+        _ptr(codes), codes.stride(0), _ptr(sf), sf_cols_, src_rows, _ptr(row_src), topk, row_src.numel(), ktot, col0,
         _ptr(out_codes), out_codes.stride(0) if out_codes is not None else 0, _ptr(out_sf), _stream(stream)))
 
 

@@ -175,7 +175,7 @@ __global__ void dispatch_scatter_kernel(const int32_t* __restrict__ ids, const f
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restrict__ codes, int64_t ld_codes,
                                                           const uint8_t* __restrict__ sf, int64_t sf_cols,
                                                           const int32_t* __restrict__ row_src, int topk, int64_t ktot,
-                                                          uint8_t* __restrict__ out_codes, int64_t ld_out,
+                                                          int64_t col0, uint8_t* __restrict__ out_codes, int64_t ld_out,
                                                           uint8_t* __restrict__ out_sf)
 {
     __shared__ int src[128];
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
         const int nvec = (int)(ktot / 32);  // 16-byte vectors of codes
         const bool tail8 = (ktot % 32) != 0;
         for (int r4 = warp * 4; r4 < 128; r4 += 32) {
-            for (int v0 = 0; v0 < nvec; v0 += 32) {
+            for (int v0 = (int)(col0 / 32); v0 < nvec; v0 += 32) {
                 const int v = v0 + lane;
                 uint4 val[4];
 #pragma unroll
@@ -213,9 +213,9 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
     }
     // scales: four words per thread at a time, loads before stores
     const int natoms = (int)(sf_cols / 4);
-    const int nwords = natoms * 128;
+    const int nwords = (int)((ktot + 63) / 64) * 128;  // atoms covering columns [col0, ktot)
     uint32_t* outw = reinterpret_cast<uint32_t*>(out_sf + blockIdx.x * (int64_t)natoms * 512);
-    for (int w0 = tid; w0 < nwords; w0 += 4 * 256) {
+    for (int w0 = (int)(col0 / 64) * 128 + tid; w0 < nwords; w0 += 4 * 256) {
         uint32_t val[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -311,20 +311,23 @@ extern "C" nvq_status moe_dispatch(const int32_t* topk_ids, const float* topk_w,
 
 extern "C" nvq_status nvfp4_gather_rows(const uint8_t* codes, int64_t ld_codes, const uint8_t* sf, int64_t sf_cols,
                                         int64_t src_rows, const int32_t* row_src, int32_t topk, int64_t capacity,
-                                        int64_t ktot, uint8_t* out_codes, int64_t ld_out, uint8_t* out_sf, void* stream)
+                                        int64_t ktot, int64_t col0, uint8_t* out_codes, int64_t ld_out, uint8_t* out_sf,
+                                        void* stream)
 {
     NVQ_CHECK_ARG(codes && sf && row_src && out_sf, NVQ_ERR_ARG, "nvfp4_gather_rows: null pointer argument");
     NVQ_CHECK_ARG(ktot >= 16 && ktot % 16 == 0 && sf_cols >= ktot / 16 && sf_cols % 4 == 0, NVQ_ERR_SHAPE,
                   "nvfp4_gather_rows: bad ktot / sf_cols");
     NVQ_CHECK_ARG(capacity >= 1 && capacity % 128 == 0 && src_rows >= 1 && topk >= 1, NVQ_ERR_SHAPE,
                   "nvfp4_gather_rows: capacity must be a positive multiple of 128");
+    NVQ_CHECK_ARG(col0 >= 0 && col0 % 64 == 0 && col0 < ktot, NVQ_ERR_SHAPE,
+                  "nvfp4_gather_rows: col0 must be a multiple of 64 below ktot");
     NVQ_CHECK_ARG(ld_codes % 16 == 0 && ld_codes >= ktot / 2 && aligned(codes, 16) && aligned(sf, 4) && aligned(out_sf, 4) &&
                       (!out_codes || (ld_out % 16 == 0 && ld_out >= ktot / 2 && aligned(out_codes, 16))),
                   NVQ_ERR_ALIGN, "nvfp4_gather_rows: codes need 16-byte aligned rows");
     set_error("");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     gather_rows_kernel<<<(unsigned)(capacity / 128), 256, 0, st>>>(codes, ld_codes, sf, sf_cols, row_src, topk, ktot,
-                                                                   out_codes, ld_out, out_sf);
+                                                                   col0, out_codes, ld_out, out_sf);
     NVQ_LAUNCH_CHECK("gather_rows_kernel");
     return NVQ_OK;
 }
