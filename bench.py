@@ -310,6 +310,9 @@ def run_ours(args, world, rank, local):
 
     # ---- activation quantizer + RAC on the 8192 x 4096 Student-t workload (HBM-bound)
     act = act_quant_bench(args, L, wl, dev, flush, peaks) if rank == 0 else None
+    # ---- baseline rows: the same layer without RAC (k = 0), and the expert GEMMs in bf16
+    base = baseline_rows(args, layer, x, ids_d, tw_d, w13_bits, w2_bits, cfg, dev, flush, ms_per_step,
+                         t_gu, t_dn) if rank == 0 else None
 
     result = {
         "metric": METRIC,
@@ -341,7 +344,82 @@ def run_ours(args, world, rank, local):
     }
     if act:
         result["act_quant_rac"] = act
+    if base:
+        result["baselines"] = base
     return result, (x_bits, ids, tw, w13_bits, w2_bits, cfg)
+
+
+def _time_replays(fn, flush, steps, warmup):
+    """Median milliseconds of a CUDA-graph replay of fn (L2 flushed before every replay)."""
+    import torch
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            fn()
+    torch.cuda.current_stream().wait_stream(cap)
+    times = []
+    for i in range(warmup + steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        b.synchronize()
+        if i >= warmup:
+            times.append(a.elapsed_time(b))
+    return statistics.median(times)
+
+
+def baseline_rows(args, layer, x, ids_d, tw_d, w13_bits, w2_bits, cfg, dev, flush, ms_rac, t_gu, t_dn):
+    """The comparison rows of the measurement plan: the same layer with k = 0 (W4A4 without RAC;
+    RAC cost = (t_RAC - t_noRAC) / t_noRAC), and the two expert GEMMs with SwiGLU in bf16 through
+    cuBLAS (a per-expert loop over this batch's routed rows, captured in a CUDA graph)."""
+    import torch
+    from nvfp4_w4a4_quantized_quantize_gb300.layers import MoERacLayer
+    E, H, I, T, topk = cfg.E, cfg.H, cfg.I, cfg.T, cfg.topk
+    steps = max(5, min(args.steps, 20))
+    w13 = _bf16(w13_bits.reshape(E * 2 * I, H), dev).view(E, 2 * I, H)
+    w2 = _bf16(w2_bits.reshape(E * H, I), dev).view(E, H, I)
+    layer0 = MoERacLayer(w13, w2, 0, topk, T)
+    out0 = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    ms0 = _time_replays(lambda: layer0.forward(x, ids_d, tw_d, out0), flush, steps, 3)
+    del layer0, out0
+    # bf16 expert GEMMs on the routed rows of this batch (the rows gathered outside the timing)
+    off = layer.grp_off.cpu().tolist()
+    cnt = layer.grp_rows.cpu().tolist()
+    src = layer.row_src.long()
+    xs, ys = [], []
+    for e in range(E):
+        r = src[off[e]:off[e] + cnt[e]]
+        xs.append(x[r // topk].contiguous() if cnt[e] else None)
+        ys.append(torch.empty(cnt[e], H, dtype=torch.bfloat16, device=dev) if cnt[e] else None)
+
+    def bf16_gemms():
+        for e in range(E):
+            if xs[e] is not None:
+                g = xs[e] @ w13[e].t()
+                h = torch.nn.functional.silu(g[:, :I]) * g[:, I:]
+                torch.matmul(h, w2[e].t(), out=ys[e])
+
+    ms_bf = _time_replays(bf16_gemms, flush, steps, 3)
+    rows = T * topk
+    flop_k0 = 2.0 * rows * (2 * I) * H + 2.0 * rows * H * I
+    del w13, w2, xs, ys
+    torch.cuda.empty_cache()
+    return {
+        "w4a4_no_rac_layer": {"ms_per_step": round(ms0, 4), "tokens_per_s": round(T / (ms0 * 1e-3), 1),
+                              "rac_cost": round((ms_rac - ms0) / ms0, 4)},
+        "bf16_expert_gemms": {"ms": round(ms_bf, 4), "tflops": round(flop_k0 / (ms_bf * 1e-3) / 1e12, 1),
+                              "impl": "cuBLAS per-expert loop (gate/up, SwiGLU, down) in a CUDA graph"},
+        "w4a4_rac_expert_gemms": {"ms": round(t_gu + t_dn, 4),
+                                  "useful_tflops": round(flop_k0 / ((t_gu + t_dn) * 1e-3) / 1e12, 1),
+                                  "speedup_vs_bf16": round(ms_bf / (t_gu + t_dn), 3)},
+    }
 
 
 def act_quant_bench(args, L, wl, dev, flush, peaks):
