@@ -313,6 +313,7 @@ def run_ours(args, world, rank, local):
     # ---- baseline rows: the same layer without RAC (k = 0), and the expert GEMMs in bf16
     base = baseline_rows(args, layer, x, ids_d, tw_d, w13_bits, w2_bits, cfg, dev, flush, ms_per_step,
                          t_gu, t_dn) if rank == 0 else None
+    trainer = trainer_rows(args, L, dev, flush, peaks) if rank == 0 else None
 
     result = {
         "metric": METRIC,
@@ -346,6 +347,8 @@ def run_ours(args, world, rank, local):
         result["act_quant_rac"] = act
     if base:
         result["baselines"] = base
+    if trainer:
+        result["trainer_side"] = trainer
     return result, (x_bits, ids, tw, w13_bits, w2_bits, cfg)
 
 
@@ -420,6 +423,70 @@ def baseline_rows(args, layer, x, ids_d, tw_d, w13_bits, w2_bits, cfg, dev, flus
                                   "useful_tflops": round(flop_k0 / ((t_gu + t_dn) * 1e-3) / 1e12, 1),
                                   "speedup_vs_bf16": round(ms_bf / (t_gu + t_dn), 3)},
     }
+
+
+def trainer_rows(args, L, dev, flush, peaks):
+    """Trainer-side rows: weight_qdq (QDQ_W of Eq. (12)) over all expert weights of the decode
+    workload shape (W13 [128, 3072, 4096] + W2 [128, 4096, 1536], 2.42 G elements, with the bf16
+    W-hat), against the HBM roofline; and a W4A16 QAT linear layer (forward + backward at
+    M = 4096, K = 4096, N = 14336) against the same layer in plain bf16."""
+    import torch
+    from nvfp4_w4a4_quantized_quantize_gb300.layers import Operand
+    from nvfp4_w4a4_quantized_quantize_gb300.qat import QATLinear
+    gen = torch.Generator(device=dev).manual_seed(5)
+    res = {}
+    total_ms, elems = 0.0, 0
+    for (G, N, K) in ((128, 3072, 4096), (128, 4096, 1536)):
+        w = (torch.randn(G, N, K, device=dev, generator=gen) * 0.02).bfloat16()
+        op = Operand.empty(G * N, K, 0, G, device=dev)
+        w_hat = torch.empty(G, N, K, dtype=torch.bfloat16, device=dev)
+
+        def qdq():
+            L.weight_qdq(w, G, N, K, op.codes, op.sf, op.sf_cols, op.tscale, w_hat=w_hat, w_hat_dtype=L.NVQ_BF16)
+        total_ms += _time_replays(qdq, flush, 5, 2)
+        elems += G * N * K
+        del w, op, w_hat
+        torch.cuda.empty_cache()
+    alg = elems * (2 + 0.5625 + 2)
+    res["weight_qdq"] = {"workload": "W13 [128,3072,4096] + W2 [128,4096,1536], bf16 W-hat", "elements": elems,
+                         "ms": round(total_ms, 4), "algorithmic_bytes": int(alg),
+                         "gbs": round(alg / (total_ms * 1e-3) / 1e9, 1),
+                         "frac_of_measured_hbm": round(alg / (total_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+    torch.manual_seed(6)
+    M, K, N = 4096, 4096, 14336
+    x = torch.randn(M, K, device=dev).bfloat16().requires_grad_(True)
+    lin = QATLinear(K, N, device=dev)
+    gy = torch.randn(M, N, device=dev).bfloat16()
+    w_plain = lin.weight.detach().clone().requires_grad_(True)
+
+    def step_qat():
+        y = lin(x)
+        y.backward(gy)
+
+    def step_bf16():
+        y = x @ w_plain.t()
+        y.backward(gy)
+
+    ts = {}
+    for name, fn in (("qat", step_qat), ("bf16", step_bf16)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(10):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        ts[name] = statistics.median(times)
+    res["qat_linear_4096x4096x14336"] = {"ms_fwd_bwd": round(ts["qat"], 4), "bf16_ms_fwd_bwd": round(ts["bf16"], 4),
+                                         "qdq_overhead": round((ts["qat"] - ts["bf16"]) / ts["bf16"], 4)}
+    del x, lin, gy, w_plain
+    torch.cuda.empty_cache()
+    return res
 
 
 def act_quant_bench(args, L, wl, dev, flush, peaks):
