@@ -147,7 +147,7 @@ nvq_status nvfp4_quantize(const void* x, int64_t rows, int64_t K, int64_t ldx,
  *
  *   x, rows, K, ldx, grp_*, groups   as for nvfp4_quantize (the same call's inputs).
  *   tscale    [groups] from nvfp4_quantize.   scores  uint64 [groups][K] from nvfp4_quantize.
- *   k         0 <= k <= K, k % 16 == 0, k <= 512.  k = 0 only zeroes the scale padding.
+ *   k         0 <= k <= K, k % 16 == 0.  k = 0 only zeroes the scale padding.
  *   codes, sf the buffers nvfp4_quantize wrote; ld_codes >= (K + k) / 2; sf_cols >= (K + k) / 16.
  *   idx       int32 [groups][k] out (may be NULL when k == 0).
  */
@@ -161,7 +161,7 @@ nvq_status rac_select_quantize(const void* x, int64_t rows, int64_t K, int64_t l
  * rac_select -- the selection half of rac_select_quantize (QUADS Eq. (24)): per group, the k
  * channels with the largest score, ties to the lower channel index, ascending in idx.
  *   scores    uint64 [groups][K] from nvfp4_quantize.   idx  int32 [groups][k] out.
- *   16 <= k <= min(K, 512), k % 16 == 0.
+ *   16 <= k <= K, k % 16 == 0.
  */
 nvq_status rac_select(const uint64_t* scores, int64_t K, int32_t groups, int32_t k, int32_t* idx,
                       void* stream);
@@ -241,7 +241,7 @@ nvq_status w4a4_rac_grouped_gemm(int32_t groups, const int64_t* grp_off, const i
  * gathered channels) with the weight tensor's own S_enc, written into columns [K, K + k) of
  * b_codes and scale columns [K / 16, (K + k) / 16) of b_sf; scale columns beyond are zeroed.
  *   b_codes, ldb, b_sf, b_sf_cols, b_tscale   weight_qdq output for groups x N rows.
- *   idx       int32 [groups][k] if idx_per_group else [k].  1 <= k <= min(K, 512), k % 16 == 0.
+ *   idx       int32 [groups][k] if idx_per_group else [k].  16 <= k <= K, k % 16 == 0.
  *   cm_codes, cm_sf   NULL, or the nvfp4_channel_major copy of the same weights (both or
  *             neither; N % 64 == 0).  With the copy the selected channels are read in
  *             coalesced runs (about 1.5 N bytes per selected channel instead of scattered

@@ -742,7 +742,7 @@ extern "C" nvq_status w4a4_rac_grouped_gemm(int32_t groups, const int64_t* grp_o
     NVQ_CHECK_ARG(N >= kBN && N % kBN == 0 && (int64_t)groups * N <= (1ll << 24), NVQ_ERR_SHAPE,
                   "w4a4_rac_grouped_gemm: N=%lld must be a positive multiple of %d", (long long)N, kBN);
     NVQ_CHECK_ARG(K >= 16 && K <= 8192 && K % 16 == 0, NVQ_ERR_SHAPE, "w4a4_rac_grouped_gemm: K must be a multiple of 16 in [16, 8192]");
-    NVQ_CHECK_ARG(k >= 0 && k <= K && k % 16 == 0 && k <= 512, NVQ_ERR_SHAPE, "w4a4_rac_grouped_gemm: bad k=%d", k);
+    NVQ_CHECK_ARG(k >= 0 && k <= K && k % 16 == 0, NVQ_ERR_SHAPE, "w4a4_rac_grouped_gemm: k=%d must be a multiple of 16 in [0, K]", k);
     const int64_t ktot = K + k;
     NVQ_CHECK_ARG(lda % 16 == 0 && ldb % 16 == 0 && lda >= ktot / 2 && ldb >= ktot / 2, NVQ_ERR_ALIGN,
                   "w4a4_rac_grouped_gemm: lda/ldb must be multiples of 16 covering (K+k)/2 bytes");

@@ -191,7 +191,9 @@ __global__ void __launch_bounds__(512) act_tail_kernel(const __nv_bfloat16* __re
         eb_tab[e] = (e == 0 || e == 127) ? 0.0f : __fdiv_rn(s_enc0, sbv);
         db_tab[e] = (e == 127) ? 0.0f : __fmul_rn(sbv, s_dec0);
     }
-    for (int c = tid; c < k; c += blockDim.x) s_sel[c] = idx[(int64_t)g0 * k + c];
+    const bool sel_smem = k <= 512;  // larger channel sets are read from global memory
+    if (sel_smem)
+        for (int c = tid; c < k; c += blockDim.x) s_sel[c] = idx[(int64_t)g0 * k + c];
     __syncthreads();
 
     const int64_t row = tile_row + t;
@@ -217,7 +219,7 @@ __global__ void __launch_bounds__(512) act_tail_kernel(const __nv_bfloat16* __re
         uint32_t sb[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const int j = own ? s_sel[b * 16 + i] : sel_g[b * 16 + i];
+            const int j = (own && sel_smem) ? s_sel[b * 16 + i] : sel_g[b * 16 + i];
             xv[i] = __bfloat162float(xr[j]);
             sb[i] = sf[sf_offset(row, j >> 4, sf_cols)];
         }
@@ -296,6 +298,7 @@ __global__ void __launch_bounds__(256) weight_tail_kernel(uint8_t* __restrict__ 
 // scale bytes with the zeroed padding as whole 32-bit words when they start on one
 // (K/16 % 4 == 0).
 constexpr int kWtRows = 64;
+constexpr int kWtChunk = 256;  // selected channels staged per pass (24 KB of shared memory)
 
 __global__ void __launch_bounds__(kWtRows) weight_tail_cm_kernel(uint8_t* __restrict__ codes, int64_t ld_codes,
                                                                   uint8_t* __restrict__ sf, int64_t sf_cols, int64_t N,
@@ -305,60 +308,65 @@ __global__ void __launch_bounds__(kWtRows) weight_tail_cm_kernel(uint8_t* __rest
                                                                   const uint8_t* __restrict__ cm_sf)
 {
     extern __shared__ __align__(16) uint8_t wt_smem[];
-    uint8_t* s_codes = wt_smem;                   // [k][32]: rows n0 .. n0+63, two per byte
-    uint8_t* s_sf = wt_smem + (size_t)k * 32;     // [k][64]
+    const int kc = k < kWtChunk ? k : kWtChunk;   // channels staged at a time
+    uint8_t* s_codes = wt_smem;                    // [kc][32]: rows n0 .. n0+63, two per byte
+    uint8_t* s_sf = wt_smem + (size_t)kc * 32;     // [kc][64]
     const int g = blockIdx.y;
     const int64_t n0 = (int64_t)blockIdx.x * kWtRows;
     const int t = threadIdx.x;
     const int nsb = K / 16;
     const int32_t* sel = idx + (idx_per_group ? (int64_t)g * k : 0);
-    // stage: per channel 2 x 16 code bytes + 4 x 16 scale bytes
-    for (int w = t; w < k * 6; w += kWtRows) {
-        const int c = w / 6, part = w % 6;
-        const int j = sel[c];
-        uint4 v;
-        if (part < 2)
-            v = __ldg(reinterpret_cast<const uint4*>(cm_codes + ((int64_t)g * K + j) * (N / 2) + n0 / 2) + part);
-        else
-            v = __ldg(reinterpret_cast<const uint4*>(cm_sf + ((int64_t)g * nsb + (j >> 4)) * N + n0) + (part - 2));
-        if (part < 2) reinterpret_cast<uint4*>(s_codes + c * 32)[part] = v;
-        else reinterpret_cast<uint4*>(s_sf + c * 64)[part - 2] = v;
-    }
-    __syncthreads();
     const int64_t n = n0 + t;
     const float s_enc = ts[g].s_enc, s_dec = ts[g].s_dec;
     const int64_t row = (int64_t)g * N + n;
     uint8_t* crow = codes + row * ld_codes + K / 2;
     const bool word_sf = (nsb % 4) == 0;
     uint32_t sfw = 0;  // tail scale bytes of the current 4-column group
-    for (int b = 0; b < k / 16; ++b) {
-        float wv[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int c = b * 16 + i;
-            const uint32_t code = (s_codes[c * 32 + (t >> 1)] >> ((t & 1) * 4)) & 0xfu;
-            const uint32_t sb = s_sf[c * 64 + t];
-            wv[i] = __fmul_rn(e2m1_value(code), __fmul_rn(e4m3_value(sb), s_dec));
+    for (int c0 = 0; c0 < k; c0 += kc) {
+        const int cnt = k - c0 < kc ? k - c0 : kc;  // channels of this chunk (a multiple of 16)
+        __syncthreads();  // the previous chunk's reads are done
+        // stage: per channel 2 x 16 code bytes + 4 x 16 scale bytes
+        for (int w = t; w < cnt * 6; w += kWtRows) {
+            const int c = w / 6, part = w % 6;
+            const int j = sel[c0 + c];
+            uint4 v;
+            if (part < 2)
+                v = __ldg(reinterpret_cast<const uint4*>(cm_codes + ((int64_t)g * K + j) * (N / 2) + n0 / 2) + part);
+            else
+                v = __ldg(reinterpret_cast<const uint4*>(cm_sf + ((int64_t)g * nsb + (j >> 4)) * N + n0) + (part - 2));
+            if (part < 2) reinterpret_cast<uint4*>(s_codes + c * 32)[part] = v;
+            else reinterpret_cast<uint4*>(s_sf + c * 64)[part - 2] = v;
         }
-        const BlockOut o = quantize16(wv, s_enc, s_dec);
-        *reinterpret_cast<uint2*>(crow + 8 * b) = make_uint2(o.code_lo, o.code_hi);
-        if (word_sf) {
-            sfw |= o.sb << (8 * (b & 3));
-            if ((b & 3) == 3) {
-                *reinterpret_cast<uint32_t*>(sf + sf_offset(row, nsb + b - 3, sf_cols)) = sfw;
-                sfw = 0;
+        __syncthreads();
+        for (int b = c0 / 16; b < (c0 + cnt) / 16; ++b) {
+            float wv[16];
+    #pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int c = b * 16 + i - c0;
+                const uint32_t code = (s_codes[c * 32 + (t >> 1)] >> ((t & 1) * 4)) & 0xfu;
+                const uint32_t sb = s_sf[c * 64 + t];
+                wv[i] = __fmul_rn(e2m1_value(code), __fmul_rn(e4m3_value(sb), s_dec));
             }
-        } else {
-            sf[sf_offset(row, nsb + b, sf_cols)] = (uint8_t)o.sb;
+            const BlockOut o = quantize16(wv, s_enc, s_dec);
+            *reinterpret_cast<uint2*>(crow + 8 * b) = make_uint2(o.code_lo, o.code_hi);
+            if (word_sf) {
+                sfw |= o.sb << (8 * (b & 3));
+                if ((b & 3) == 3) {
+                    *reinterpret_cast<uint32_t*>(sf + sf_offset(row, nsb + b - 3, sf_cols)) = sfw;
+                    sfw = 0;
+                }
+            } else {
+                sf[sf_offset(row, nsb + b, sf_cols)] = (uint8_t)o.sb;
+            }
         }
     }
-    const int64_t c0 = (K + k) / 16;
-    if (word_sf && (c0 & 3)) {
+    const int64_t cend = (K + k) / 16;
+    if (word_sf && (cend & 3)) {
         // the last partial group: its remaining bytes are padding (zero)
-        *reinterpret_cast<uint32_t*>(sf + sf_offset(row, c0 & ~3ll, sf_cols)) = sfw;
-        for (int64_t c = (c0 | 3) + 1; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
+        *reinterpret_cast<uint32_t*>(sf + sf_offset(row, cend & ~3ll, sf_cols)) = sfw;
+        for (int64_t c = (cend | 3) + 1; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
     } else {
-        for (int64_t c = c0; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
+        for (int64_t c = cend; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
     }
 }
 
@@ -439,8 +447,7 @@ static nvq_status check_rac_args(const char* fn, const void* x, int64_t rows, in
     NVQ_CHECK_ARG(x && codes && sf && tscale, NVQ_ERR_ARG, "%s: null pointer argument", fn);
     NVQ_CHECK_ARG(rows >= 1 && rows <= (1ll << 24), NVQ_ERR_SHAPE, "%s: rows outside [1, 2^24]", fn);
     NVQ_CHECK_ARG(K >= 16 && K <= 8192 && K % 16 == 0, NVQ_ERR_SHAPE, "%s: K must be a multiple of 16 in [16, 8192]", fn);
-    NVQ_CHECK_ARG(k >= 0 && k <= K && k % 16 == 0 && k <= 512, NVQ_ERR_SHAPE,
-                  "%s: k=%d must be a multiple of 16 in [0, min(K, 512)]", fn, k);
+    NVQ_CHECK_ARG(k >= 0 && k <= K && k % 16 == 0, NVQ_ERR_SHAPE, "%s: k=%d must be a multiple of 16 in [0, K]", fn, k);
     NVQ_CHECK_ARG(groups >= 1 && groups <= 4096, NVQ_ERR_SHAPE, "%s: groups outside [1, 4096]", fn);
     NVQ_CHECK_ARG(grp_off || groups == 1 || rows % groups == 0, NVQ_ERR_SHAPE, "%s: rows not divisible by groups", fn);
     NVQ_CHECK_ARG(ldx >= K && ldx % 8 == 0, NVQ_ERR_ALIGN, "%s: ldx must be >= K and a multiple of 8", fn);
@@ -497,7 +504,7 @@ extern "C" nvq_status rac_select(const uint64_t* scores, int64_t K, int32_t grou
 {
     NVQ_CHECK_ARG(scores && idx, NVQ_ERR_ARG, "rac_select: null pointer argument");
     NVQ_CHECK_ARG(K >= 16 && K <= 8192 && K % 16 == 0, NVQ_ERR_SHAPE, "rac_select: K must be a multiple of 16 in [16, 8192]");
-    NVQ_CHECK_ARG(k >= 16 && k <= K && k % 16 == 0 && k <= 512, NVQ_ERR_SHAPE, "rac_select: bad k=%d", k);
+    NVQ_CHECK_ARG(k >= 16 && k <= K && k % 16 == 0, NVQ_ERR_SHAPE, "rac_select: k=%d must be a multiple of 16 in [16, K]", k);
     NVQ_CHECK_ARG(groups >= 1 && groups <= 4096, NVQ_ERR_SHAPE, "rac_select: groups outside [1, 4096]");
     set_error("");
     return launch_topk(scores, K, groups, k, idx, static_cast<cudaStream_t>(stream));
@@ -551,14 +558,14 @@ extern "C" nvq_status rac_weight_tail(int32_t groups, int64_t N, int64_t K, int3
     NVQ_CHECK_ARG(groups >= 1 && groups <= 4096 && N >= 1 && (int64_t)groups * N <= (1ll << 24), NVQ_ERR_SHAPE,
                   "rac_weight_tail: groups*N outside [1, 2^24]");
     NVQ_CHECK_ARG(K >= 16 && K <= 8192 && K % 16 == 0, NVQ_ERR_SHAPE, "rac_weight_tail: K must be a multiple of 16 in [16, 8192]");
-    NVQ_CHECK_ARG(k >= 16 && k <= K && k % 16 == 0 && k <= 512, NVQ_ERR_SHAPE, "rac_weight_tail: bad k=%d", k);
+    NVQ_CHECK_ARG(k >= 16 && k <= K && k % 16 == 0, NVQ_ERR_SHAPE, "rac_weight_tail: k=%d must be a multiple of 16 in [16, K]", k);
     NVQ_CHECK_ARG(ldb % 16 == 0 && ldb >= (K + k) / 2 && aligned(b_codes, 16), NVQ_ERR_ALIGN,
                   "rac_weight_tail: ldb must be a multiple of 16 covering (K+k)/2 bytes");
     NVQ_CHECK_ARG(b_sf_cols % 4 == 0 && b_sf_cols >= (K + k) / 16, NVQ_ERR_SHAPE, "rac_weight_tail: b_sf_cols too small");
     set_error("");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (!cm_codes) return weight_tail_impl(b_codes, ldb, b_sf, b_sf_cols, N, (int)K, k, groups, b_tscale, idx, idx_per_group, st);
-    const size_t smem = (size_t)k * 96;  // k <= 512: at most 48 KB
+    const size_t smem = (size_t)(k < kWtChunk ? k : kWtChunk) * 96;
     const dim3 grid((unsigned)(N / kWtRows), (unsigned)groups);
     weight_tail_cm_kernel<<<grid, kWtRows, smem, st>>>(b_codes, ldb, b_sf, b_sf_cols, N, (int)K, k, b_tscale, idx,
                                                       idx_per_group, cm_codes, cm_sf);

@@ -145,7 +145,8 @@ def test_gemm_small_linear_layer(L):
 
 
 @pytest.mark.parametrize("M,N,K,k", [(1, 256, 256, 0), (200, 512, 448, 64), (130, 256, 320, 16),
-                                     (256, 512, 4096, 64), (77, 768, 1536, 48)])
+                                     (256, 512, 4096, 64), (77, 768, 1536, 48),
+                                     (130, 256, 256, 256), (200, 512, 1024, 512)])
 def test_gemm_dense_shapes(L, M, N, K, k):
     _run_case(L, [M], N, K, k, dense=True, seed=M + K)
 

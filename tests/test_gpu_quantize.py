@@ -117,7 +117,8 @@ def test_quantize_extreme_scales(L):
 
 
 @pytest.mark.parametrize("M,K,k", [(64, 256, 16), (200, 512, 64), (96, 768, 32), (50, 256, 256), (17, 4096, 64),
-                                   (31, 6144, 128)])
+                                   (31, 6144, 128), (130, 768, 384), (40, 2048, 1024), (9, 4096, 4096),
+                                   (64, 1024, 1024)])
 def test_rac_select_and_tail_dense(L, M, K, k):
     x, _ = wl.activations(M, K, seed=7 * M + K, n_outliers=max(2, K // 64), outlier_gain=16.0)
     g = _gpu_quant(L, x, k=k)
@@ -237,7 +238,9 @@ def test_argument_errors_are_reported_before_launch(L):
 
 
 @pytest.mark.parametrize("G,N,K,k,per_group", [(3, 384, 272, 32, True), (1, 256, 2048, 64, False),
-                                               (2, 128, 16, 16, True), (4, 128, 1536, 48, True)])
+                                               (2, 128, 16, 16, True), (4, 128, 1536, 48, True),
+                                               (1, 128, 768, 400, False), (2, 128, 1536, 768, True),
+                                               (1, 256, 256, 256, False)])
 def test_weight_tail_channel_major_path(L, G, N, K, k, per_group):
     """nvfp4_channel_major holds every code and scale of the weights at its channel-major place,
     and rac_weight_tail from that copy writes the same bytes as the row-major path and the oracle
