@@ -180,6 +180,27 @@ nvq_status rac_residual_tail(const void* x, int64_t rows, int64_t K, int64_t ldx
                              void* stream);
 
 /*
+ * rac_reconstruct -- the compensated activation X~ of QUADS Eq. (21) read back from an activation
+ * operand (codes, sf and tscale as written by nvfp4_quantize + rac_select_quantize): for row r of
+ * group g, out[r][j] = fl(DQ_main[r][j] + DQ_tail[r][p]) where j = idx[g * k + p], and
+ * out[r][j] = DQ_main[r][j] for channels outside the group's set; DQ(code) = fl(V * fl(sb *
+ * S_dec_g)).  An evaluation entry (the activation error ||X~ - X|| of a k), not a step of the
+ * layer: two kernel launches on `stream`.
+ *   codes     [rows][ld_codes] with the main columns [0, K) and the tail [K, K + k);
+ *             8-byte aligned rows.   sf: blocked scales, sf_cols >= (K + k) / 16.
+ *   tscale    [groups] (device).   idx: int32 [groups][k], distinct channels per group (NULL when
+ *             k == 0).   grp_off / grp_rows: as for rac_select_quantize (NULL: equal groups).
+ *   out       fp32 [rows][ldo], ldo >= K, 16-byte aligned rows; rows outside every group's
+ *             range are not written.
+ *   Errors: NVQ_ERR_ARG (null pointer), NVQ_ERR_SHAPE (K or k not multiples of 16, k > K, short
+ *   leading dimensions), NVQ_ERR_ALIGN, NVQ_ERR_CUDA.
+ */
+nvq_status rac_reconstruct(const uint8_t* codes, int64_t ld_codes, const uint8_t* sf, int64_t sf_cols,
+                           const nvq_tensor_scale* tscale, int64_t rows, int64_t K, int32_t k,
+                           const int32_t* idx, const int64_t* grp_off, const int64_t* grp_rows,
+                           int32_t groups, float* out, int64_t ldo, void* stream);
+
+/*
  * weight_qdq -- the trainer-side QDQ_W of QUADS Eq. (12): for each of G weight tensors
  * W_g = w[g] ([N][K] bf16, tensor g at w + g * N * ldw elements) the same quantizer as
  * nvfp4_quantize with one tensor scale per tensor, so that its codes and scales are the

@@ -30,6 +30,7 @@ _SIGS = {
                                _I32, _P, _I32, _I32, _P, _P, _I64, _P, _P], C.c_int),
     "rac_select": ([_P, _I64, _I32, _I32, _P, _P], C.c_int),
     "rac_residual_tail": ([_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _I32, _P, _I64, _P, _I64, _P], C.c_int),
+    "rac_reconstruct": ([_P, _I64, _P, _I64, _P, _I64, _I64, _I32, _P, _P, _P, _I32, _P, _I64, _P], C.c_int),
     "rac_weight_tail": ([_I32, _I64, _I64, _I32, _P, _I32, _P, _I64, _P, _I64, _P, _P, _P, _P], C.c_int),
     "nvfp4_channel_major": ([_I32, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _P], C.c_int),
     "moe_capacity": ([_I64, _I32, _I32], _I64),
@@ -161,6 +162,14 @@ def rac_residual_tail(x, tscale, idx, k, codes, sf, sf_cols_, grp_off=None, grp_
     _check("rac_residual_tail", LIB.rac_residual_tail(
         _ptr(x), rows, K, x.stride(0), _ptr(grp_off), _ptr(grp_rows), groups, _ptr(tscale), _ptr(idx), k,
         _ptr(codes), codes.stride(0), _ptr(sf), sf_cols_, _stream(stream)))
+
+
+def rac_reconstruct(codes, sf, sf_cols_, tscale, K, k, idx, out, rows=None, grp_off=None, grp_rows=None, groups=1,
+                    stream=None):
+    rows = codes.shape[0] if rows is None else rows
+    _check("rac_reconstruct", LIB.rac_reconstruct(
+        _ptr(codes), codes.stride(0), _ptr(sf), sf_cols_, _ptr(tscale), rows, K, k, _ptr(idx), _ptr(grp_off),
+        _ptr(grp_rows), groups, _ptr(out), out.stride(0), _stream(stream)))
 
 
 def w4a4_rac_grouped_gemm(a_codes, a_sf, a_sf_cols, a_tscale, b_codes, b_sf, b_sf_cols, b_tscale, N, K, k, idx,

@@ -302,6 +302,18 @@ class RacQuant:
     tail_scales: np.ndarray  # [M, k/16]
 
 
+def rac_reconstruct(q: RacQuant) -> np.ndarray:
+    """The compensated activation of QUADS Eq. (21), X-tilde = DQ(Q(X)) + DQ(Q(R)) on the selected
+    channels and DQ(Q(X)) elsewhere, as binary32: each dequantized value is fl(V * fl(sb * S_dec))
+    (the `dequantize` above) and the two are summed with one binary32 addition (numpy float32
+    arithmetic rounds to nearest-even)."""
+    out = dequantize(q.codes, q.scales, q.ts.s_dec)
+    if q.idx.size:
+        tail = dequantize(q.tail_codes, q.tail_scales, q.ts.s_dec)
+        out[:, q.idx] = out[:, q.idx] + tail
+    return out
+
+
 def rac_quantize(x: np.ndarray, k: int) -> RacQuant:
     """Steps of QUADS §3.3 in the paper's order: Q_A(X), residual, score, TopK, second pass."""
     ts = tensor_scale(x)

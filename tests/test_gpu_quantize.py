@@ -40,7 +40,7 @@ def _gpu_quant(L, x_bits, k=0, groups=1, grp_off=None, grp_rows=None, ktail=None
     torch.cuda.synchronize()
     assert L.device_status() == (0, 0)
     return dict(codes=codes.cpu().numpy(), sf=sf, sf_cols=sf_cols, ts=ts, scores=scores.cpu().numpy().view(np.uint64),
-                idx=idx.cpu().numpy())
+                idx=idx.cpu().numpy(), codes_d=codes, idx_d=idx, go=go, gr=gr)
 
 
 def _check_rows(L, x_bits, g, rows, k, K, ref_k=None):
@@ -336,3 +336,38 @@ def test_select_and_residual_tail_split_equals_combined(L):
     torch.cuda.synchronize()
     assert np.array_equal(idx.cpu().numpy(), a["idx"])
     assert np.array_equal(codes.cpu().numpy(), a["codes"]) and torch.equal(sf, a["sf"])
+
+
+@pytest.mark.parametrize("M,K,k", [(64, 256, 16), (130, 768, 0), (200, 1024, 128), (9, 512, 512), (257, 4096, 1024)])
+def test_rac_reconstruct_dense(L, M, K, k):
+    """X~ of Eq. (21) read back from the GPU operand equals the oracle's binary32 X~ bit for bit."""
+    x, _ = wl.activations(M, K, seed=3 * M + k, n_outliers=max(1, K // 64), outlier_gain=20.0)
+    g = _gpu_quant(L, x, k=k)
+    out = torch.full((M, K), float("nan"), dtype=torch.float32, device="cuda")
+    L.rac_reconstruct(g["codes_d"], g["sf"], g["sf_cols"], g["ts"], K, k, g["idx_d"] if k else None, out)
+    torch.cuda.synchronize()
+    ref = oracle.rac_reconstruct(oracle.rac_quantize(x, k))
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def test_rac_reconstruct_grouped_with_gaps(L):
+    """Per-group tensor scales and channel sets, padding rows between groups left unwritten."""
+    G, K, k = 4, 512, 64
+    counts = [3, 0, 200, 129]
+    off = [0]
+    for c in counts:
+        off.append(off[-1] + (c + 127) // 128 * 128)
+    rows = off[-1]
+    x, _ = wl.activations(rows, K, seed=8, n_outliers=6, outlier_gain=12.0)
+    g = _gpu_quant(L, x, k=k, groups=G, grp_off=off, grp_rows=counts)
+    out = torch.full((rows, K), -1.0, dtype=torch.float32, device="cuda")
+    L.rac_reconstruct(g["codes_d"], g["sf"], g["sf_cols"], g["ts"], K, k, g["idx_d"], out, grp_off=g["go"],
+                      grp_rows=g["gr"], groups=G)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    for gi in range(G):
+        a, c = off[gi], counts[gi]
+        if c:
+            ref = oracle.rac_reconstruct(oracle.rac_quantize(x[a:a + c], k))
+            assert np.array_equal(o[a:a + c].view(np.uint32), ref.view(np.uint32))
+        assert np.all(o[a + c:off[gi + 1]] == -1.0)

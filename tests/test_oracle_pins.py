@@ -245,11 +245,32 @@ def test_topk_against_brute_force_sort():
 
 
 def _reconstruct(x, q: "oracle.RacQuant"):
-    dq = oracle.dequantize(q.codes, q.scales, q.ts.s_dec).astype(np.float64)
-    if q.idx.size:
-        dt = oracle.dequantize(q.tail_codes, q.tail_scales, q.ts.s_dec).astype(np.float64)
-        dq[:, q.idx] += dt
-    return dq
+    return oracle.rac_reconstruct(q).astype(np.float64)
+
+
+def test_rac_reconstruct_properties():
+    """X-tilde (Eq. (21)): k = 0 is plain DQ(Q(X)); channels outside S keep DQ(Q(X)) bit for
+    bit; on S every element is at least as close to X as DQ(Q(X)) (E2M1 rounding is to the
+    nearest grid value and 0 is on the grid, so |R - DQ(Q(R))| <= |R|), up to the half ulp of
+    the binary32 sum; and that sum is the correctly rounded fp64 sum of the two parts."""
+    x = _rand_x(48, 384, 34, outliers=6)
+    xf = wl.bf16_bits_to_f32(x).astype(np.float64)
+    q0 = oracle.rac_quantize(x, 0)
+    dq = oracle.dequantize(q0.codes, q0.scales, q0.ts.s_dec)
+    assert np.array_equal(oracle.rac_reconstruct(q0).view(np.uint32), dq.view(np.uint32))
+    for k in (16, 96, 384):
+        q = oracle.rac_quantize(x, k)
+        xt = oracle.rac_reconstruct(q)
+        rest = np.setdiff1d(np.arange(384), q.idx)
+        assert np.array_equal(xt[:, rest].view(np.uint32), dq[:, rest].view(np.uint32))
+        sel = xt[:, q.idx].astype(np.float64)
+        half_ulp = np.spacing(np.abs(xt[:, q.idx])).astype(np.float64) / 2
+        assert np.all(np.abs(xf[:, q.idx] - sel) <= np.abs(xf[:, q.idx] - dq[:, q.idx]) + half_ulp)
+        tail = oracle.dequantize(q.tail_codes, q.tail_scales, q.ts.s_dec).astype(np.float64)
+        exact = dq[:, q.idx].astype(np.float64) + tail
+        assert np.array_equal(sel.astype(np.float32), exact.astype(np.float32))
+        # the compensation is not a no-op: some selected element moved
+        assert np.any(xt[:, q.idx] != dq[:, q.idx])
 
 
 def test_rac_reduces_activation_error_eq22_and_monotone_in_k():
