@@ -96,6 +96,16 @@ nvq_status nvq_device_status(void* stream, int32_t* status, int32_t* where);
  * Applies to launches made after the call on the current device. */
 nvq_status nvq_set_wait_limit(uint64_t cycles);
 
+/* How rac_select_quantize, rac_residual_tail and rac_weight_tail build the tail columns; every
+ * path writes the same bytes.  NVQ_TAIL_GATHER loads the selected channels one by one (the
+ * least traffic when k is a small share of K); NVQ_TAIL_ROWS reads whole rows with 16-byte
+ * loads, expands them in shared memory and gathers from there (fewer instructions per tail
+ * element when k is a large share); NVQ_TAIL_AUTO (the default) takes the row path when
+ * k >= K / 4, and for a weight tail given the channel-major copy when k > K / 2.  A process-wide setting for launches made after the call; NVQ_ERR_ARG for an
+ * unknown value.  Not part of the paper's method: a choice between two schedules of Eq. (21). */
+enum nvq_tail_path { NVQ_TAIL_AUTO = 0, NVQ_TAIL_GATHER = 1, NVQ_TAIL_ROWS = 2 };
+nvq_status nvq_set_tail_path(int32_t path);
+
 /* Measured NVFP4 tensor-core rate of the current GPU (a roofline reference; not part of the
  * paper's method): back-to-back tcgen05 M128 N256 K64 mxf4nvf4 MMAs with FP32 accumulation in
  * TMEM on every SM, no memory traffic, mmas_per_sm per SM (16 .. 2^20).  with_cp != 0 adds the

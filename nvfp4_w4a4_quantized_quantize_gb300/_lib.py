@@ -19,6 +19,7 @@ _SIGS = {
     "nvq_last_error": ([], C.c_char_p),
     "nvq_device_status": ([_P, _P, _P], C.c_int),
     "nvq_set_wait_limit": ([_U64], C.c_int),
+    "nvq_set_tail_path": ([_I32], C.c_int),
     "nvq_fp4_mma_rate": ([_I32, _I32, _P, _P], C.c_int),
     "nvq_sf_cols": ([_I64], _I64),
     "nvq_sf_bytes": ([_I64, _I64], _I64),
@@ -111,6 +112,13 @@ def moe_dispatch_workspace_size(tokens: int, topk: int, groups: int) -> int:
 
 def set_wait_limit(cycles: int):
     _check("nvq_set_wait_limit", LIB.nvq_set_wait_limit(cycles))
+
+
+NVQ_TAIL_AUTO, NVQ_TAIL_GATHER, NVQ_TAIL_ROWS = 0, 1, 2
+
+
+def set_tail_path(path: int):
+    _check("nvq_set_tail_path", LIB.nvq_set_tail_path(path))
 
 
 def device_status(stream=None):

@@ -36,6 +36,10 @@ static unsigned long long g_wait_limit = 1ull << 32;
 
 unsigned long long wait_limit() { return g_wait_limit; }
 
+static int g_tail_path = NVQ_TAIL_AUTO;
+
+int tail_path() { return g_tail_path; }
+
 }  // namespace nvq
 
 using namespace nvq;
@@ -46,6 +50,15 @@ extern "C" nvq_status nvq_set_wait_limit(uint64_t cycles)
 {
     NVQ_CHECK_ARG(cycles >= 1000, NVQ_ERR_ARG, "nvq_set_wait_limit: limit below 1000 cycles");
     g_wait_limit = cycles;
+    set_error("");
+    return NVQ_OK;
+}
+
+extern "C" nvq_status nvq_set_tail_path(int32_t path)
+{
+    NVQ_CHECK_ARG(path == NVQ_TAIL_AUTO || path == NVQ_TAIL_GATHER || path == NVQ_TAIL_ROWS, NVQ_ERR_ARG,
+                  "nvq_set_tail_path: unknown path %d", path);
+    g_tail_path = path;
     set_error("");
     return NVQ_OK;
 }

@@ -28,6 +28,7 @@ struct DeviceStatus {
 };
 DeviceStatus* device_status_ptr();   // address of the current device's status word
 unsigned long long wait_limit();      // cycles
+int tail_path();                      // nvq_tail_path set by nvq_set_tail_path
 
 #define NVQ_CHECK_ARG(cond, code, ...)          \
     do {                                        \

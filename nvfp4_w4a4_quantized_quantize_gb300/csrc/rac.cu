@@ -291,12 +291,13 @@ __global__ void __launch_bounds__(256) weight_tail_kernel(uint8_t* __restrict__ 
         for (int64_t c = (K + k) / 16; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
 }
 
-// Same tail from the channel-major copy (nvfp4_channel_major): CTA per (group, 64 weight rows).
-// The CTA first stages, for each of the k selected channels, the 32 code bytes and 64 scale
-// bytes of its rows into shared memory with 16-byte loads (all in flight together); then thread
-// t builds row t's whole tail from there and writes it at once: k/2 code bytes, and the tail
-// scale bytes with the zeroed padding as whole 32-bit words when they start on one
-// (K/16 % 4 == 0).
+// Same tail from the channel-major copy (nvfp4_channel_major): CTA per (group, 64 weight rows,
+// chunk of up to 256 selected channels).  The CTA first stages, for each channel of its chunk,
+// the 32 code bytes and 64 scale bytes of its rows into shared memory with 16-byte loads (all in
+// flight together); then thread t builds row t's tail blocks of the chunk from there: 8 code
+// bytes per block, and the tail scale bytes as whole 32-bit words when they start on one
+// (K/16 % 4 == 0; every chunk but the last holds 16 blocks).  The CTA of the last chunk also
+// zeroes the scale padding.
 constexpr int kWtRows = 64;
 constexpr int kWtChunk = 256;  // selected channels staged per pass (24 KB of shared memory)
 
@@ -311,6 +312,7 @@ __global__ void __launch_bounds__(kWtRows) weight_tail_cm_kernel(uint8_t* __rest
     const int kc = k < kWtChunk ? k : kWtChunk;   // channels staged at a time
     uint8_t* s_codes = wt_smem;                    // [kc][32]: rows n0 .. n0+63, two per byte
     uint8_t* s_sf = wt_smem + (size_t)kc * 32;     // [kc][64]
+    const int c0 = blockIdx.z * kWtChunk;
     const int g = blockIdx.y;
     const int64_t n0 = (int64_t)blockIdx.x * kWtRows;
     const int t = threadIdx.x;
@@ -322,9 +324,8 @@ __global__ void __launch_bounds__(kWtRows) weight_tail_cm_kernel(uint8_t* __rest
     uint8_t* crow = codes + row * ld_codes + K / 2;
     const bool word_sf = (nsb % 4) == 0;
     uint32_t sfw = 0;  // tail scale bytes of the current 4-column group
-    for (int c0 = 0; c0 < k; c0 += kc) {
+    {
         const int cnt = k - c0 < kc ? k - c0 : kc;  // channels of this chunk (a multiple of 16)
-        __syncthreads();  // the previous chunk's reads are done
         // stage: per channel 2 x 16 code bytes + 4 x 16 scale bytes
         for (int w = t; w < cnt * 6; w += kWtRows) {
             const int c = w / 6, part = w % 6;
@@ -340,7 +341,7 @@ __global__ void __launch_bounds__(kWtRows) weight_tail_cm_kernel(uint8_t* __rest
         __syncthreads();
         for (int b = c0 / 16; b < (c0 + cnt) / 16; ++b) {
             float wv[16];
-    #pragma unroll
+#pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int c = b * 16 + i - c0;
                 const uint32_t code = (s_codes[c * 32 + (t >> 1)] >> ((t & 1) * 4)) & 0xfu;
@@ -360,6 +361,7 @@ __global__ void __launch_bounds__(kWtRows) weight_tail_cm_kernel(uint8_t* __rest
             }
         }
     }
+    if (c0 + kWtChunk < k) return;  // not the last chunk
     const int64_t cend = (K + k) / 16;
     if (word_sf && (cend & 3)) {
         // the last partial group: its remaining bytes are padding (zero)
@@ -424,6 +426,138 @@ __global__ void __launch_bounds__(256) channel_major_sf_kernel(const uint8_t* __
     cm_sf[t] = sf[sf_offset(g * N + n, c, sf_cols)];
 }
 
+// ------------------------------------------------------------------------ row-path tails
+// When S is a large share of K the kernels above spend their issue slots on one scattered load
+// per selected element.  This one reads R whole rows with 16-byte loads, expands every channel's
+// value into shared memory (fp32, one pad word after every 16 channels, so that lanes on
+// neighbouring 16-channel blocks hit distinct banks), then gathers the selected channels from
+// there and quantizes them into the tail:
+//   kResidual   activations: the residual fl(x - fl(V * d_b)), the code recomputed from x and the
+//               stored block scale exactly as the gather kernel does (bit-identical to the first pass);
+//   !kResidual  weights: the dequantized stored weight fl(V * fl(sb * S_dec)).
+constexpr int kRowThreads = 256;
+constexpr int kRowElems = 8192;  // channels expanded per CTA: R = max(1, 8192 / K) rows
+
+__host__ __device__ constexpr int row_tile_rows(int K) { return K >= kRowElems ? 1 : kRowElems / K; }
+__host__ __device__ constexpr int padded_ch(int j) { return j + (j >> 4); }
+
+inline size_t row_tail_smem(int K) { return (size_t)row_tile_rows(K) * (padded_ch(K) * sizeof(float) + sizeof(int)); }
+
+template <bool kResidual>
+__global__ void __launch_bounds__(kRowThreads)
+    row_tail_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, uint8_t* __restrict__ codes, int64_t ld_codes,
+                    uint8_t* __restrict__ sf, int64_t sf_cols, int K, int k, Groups gr,
+                    const nvq_tensor_scale* __restrict__ ts, const int32_t* __restrict__ idx, int idx_per_group,
+                    int idx_vec)
+{
+    extern __shared__ __align__(16) float rt_smem[];
+    const int R = row_tile_rows(K);
+    const int stride = padded_ch(K);
+    int* s_g = reinterpret_cast<int*>(rt_smem + (size_t)R * stride);  // group of each row, -1: not written
+    const int64_t row0 = (int64_t)blockIdx.x * R;
+    const int tid = threadIdx.x;
+    for (int r = tid; r < R; r += kRowThreads) {
+        const int64_t row = row0 + r;
+        int g = -1;
+        if (row < gr.total_rows) {
+            g = group_of_row(gr, row);
+            int64_t b0, b1;
+            group_range(gr, g, b0, b1);
+            if (row < b0 || row >= b1) g = -1;
+        }
+        s_g[r] = g;
+    }
+    __syncthreads();
+    // 1. expand: thread per (row, 16-channel block)
+    const int nb = K / 16;
+    for (int w = tid; w < R * nb; w += kRowThreads) {
+        const int r = w / nb, b = w - r * nb;
+        const int g = s_g[r];
+        if (g < 0) continue;
+        const int64_t row = row0 + r;
+        const uint32_t sb = sf[sf_offset(row, b, sf_cols)];
+        const float sbv = e4m3_value(sb);
+        float* dst = rt_smem + (size_t)r * stride + padded_ch(16 * b);
+        if constexpr (kResidual) {
+            const float e_b = (sb == 0 || sb == 127) ? 0.0f : __fdiv_rn(ts[g].s_enc, sbv);
+            const float d_b = (sb == 127) ? 0.0f : __fmul_rn(sbv, ts[g].s_dec);
+            const uint4* xp = reinterpret_cast<const uint4*>(x + row * ldx + 16 * b);
+            const uint4 v0 = __ldg(xp), v1 = __ldg(xp + 1);
+            const uint32_t xw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float xa = bf16lo(xw[i]), xb = bf16hi(xw[i]);
+                const float2 q = e2m1x2_value(e2m1x2(__fmul_rn(xa, e_b), __fmul_rn(xb, e_b)));
+                dst[2 * i] = __fsub_rn(xa, __fmul_rn(q.x, d_b));
+                dst[2 * i + 1] = __fsub_rn(xb, __fmul_rn(q.y, d_b));
+            }
+        } else {
+            const float d_b = __fmul_rn(sbv, ts[g].s_dec);
+            const uint2 c = *reinterpret_cast<const uint2*>(codes + row * ld_codes + 8 * b);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float2 q = e2m1x2_value(((i < 4 ? c.x : c.y) >> (8 * (i & 3))) & 0xffu);
+                dst[2 * i] = __fmul_rn(q.x, d_b);
+                dst[2 * i + 1] = __fmul_rn(q.y, d_b);
+            }
+        }
+    }
+    __syncthreads();
+    // 2. gather + quantize: thread per (row, tail block)
+    const int nbt = k / 16;
+    for (int w = tid; w < R * nbt; w += kRowThreads) {
+        const int r = w / nbt, b = w - r * nbt;
+        const int g = s_g[r];
+        if (g < 0) continue;
+        const int64_t row = row0 + r;
+        const int32_t* sel = idx + (idx_per_group ? (int64_t)g * k : 0) + 16 * b;
+        int j[16];
+        if (idx_vec) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int4 v = __ldg(reinterpret_cast<const int4*>(sel) + q);
+                j[4 * q] = v.x; j[4 * q + 1] = v.y; j[4 * q + 2] = v.z; j[4 * q + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) j[i] = __ldg(sel + i);
+        }
+        const float* src = rt_smem + (size_t)r * stride;
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = src[padded_ch(j[i])];
+        const BlockOut o = quantize16(v, ts[g].s_enc, ts[g].s_dec);
+        *reinterpret_cast<uint2*>(codes + row * ld_codes + K / 2 + 8 * b) = make_uint2(o.code_lo, o.code_hi);
+        sf[sf_offset(row, nb + b, sf_cols)] = (uint8_t)o.sb;
+        if (b == 0)
+            for (int64_t c = (K + k) / 16; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
+    }
+}
+
+// Row path when the setting asks for it, or (NVQ_TAIL_AUTO) past the crossover measured on GB300
+// at the MoE shapes: k >= K / 4 for activation tails and for weight tails gathered from the
+// row-major operand; k > K / 2 for weight tails with the channel-major copy (whose gather reads
+// only the selected channels' bytes, 16 at a time).
+inline bool use_row_tail(int K, int k, bool channel_major)
+{
+    if (tail_path() != NVQ_TAIL_AUTO) return tail_path() == NVQ_TAIL_ROWS;
+    return channel_major ? 2 * k > K : 4 * k >= K;
+}
+
+template <bool kResidual>
+nvq_status launch_row_tail(const void* x, int64_t ldx, uint8_t* codes, int64_t ld_codes, uint8_t* sf, int64_t sf_cols,
+                           int K, int k, Groups gr, const nvq_tensor_scale* ts, const int32_t* idx, int idx_per_group,
+                           cudaStream_t st)
+{
+    const int R = row_tile_rows(K);
+    const int64_t tiles = (gr.total_rows + R - 1) / R;
+    const int idx_vec = aligned(idx, 16) ? 1 : 0;  // per-group offsets g * k * 4 bytes keep 16-byte alignment
+    row_tail_kernel<kResidual><<<(unsigned)tiles, kRowThreads, row_tail_smem(K), st>>>(
+        static_cast<const __nv_bfloat16*>(x), ldx, codes, ld_codes, sf, sf_cols, K, k, gr, ts, idx, idx_per_group, idx_vec);
+    NVQ_LAUNCH_CHECK(kResidual ? "row_tail_kernel<residual>" : "row_tail_kernel<weight>");
+    return NVQ_OK;
+}
+
 nvq_status weight_tail_impl(uint8_t* codes, int64_t ld_codes, uint8_t* sf, int64_t sf_cols, int64_t N, int K, int k,
                             int G, const nvq_tensor_scale* ts, const int32_t* idx, int idx_per_group, cudaStream_t st)
 {
@@ -470,6 +604,8 @@ static nvq_status launch_act_tail(const void* x, int64_t rows, int64_t K, int64_
                                   const nvq_tensor_scale* tscale, const int32_t* idx, int32_t k, uint8_t* codes,
                                   int64_t ld_codes, uint8_t* sf, int64_t sf_cols, cudaStream_t st)
 {
+    if (k > 0 && use_row_tail((int)K, k, false) && aligned(x, 16))
+        return launch_row_tail<true>(x, ldx, codes, ld_codes, sf, sf_cols, (int)K, k, gr, tscale, idx, 1, st);
     const int64_t tiles = (rows + kTailRows - 1) / kTailRows;
     // split a row's tail blocks over threads until there are ~8 CTAs' worth of threads per SM
     int sms = 148, dev = 0;
@@ -564,9 +700,12 @@ extern "C" nvq_status rac_weight_tail(int32_t groups, int64_t N, int64_t K, int3
     NVQ_CHECK_ARG(b_sf_cols % 4 == 0 && b_sf_cols >= (K + k) / 16, NVQ_ERR_SHAPE, "rac_weight_tail: b_sf_cols too small");
     set_error("");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (use_row_tail((int)K, k, cm_codes != nullptr))
+        return launch_row_tail<false>(nullptr, 0, b_codes, ldb, b_sf, b_sf_cols, (int)K, k,
+                                      Groups{nullptr, nullptr, groups, (int64_t)groups * N}, b_tscale, idx, idx_per_group, st);
     if (!cm_codes) return weight_tail_impl(b_codes, ldb, b_sf, b_sf_cols, N, (int)K, k, groups, b_tscale, idx, idx_per_group, st);
     const size_t smem = (size_t)(k < kWtChunk ? k : kWtChunk) * 96;
-    const dim3 grid((unsigned)(N / kWtRows), (unsigned)groups);
+    const dim3 grid((unsigned)(N / kWtRows), (unsigned)groups, (unsigned)((k + kWtChunk - 1) / kWtChunk));
     weight_tail_cm_kernel<<<grid, kWtRows, smem, st>>>(b_codes, ldb, b_sf, b_sf_cols, N, (int)K, k, b_tscale, idx,
                                                       idx_per_group, cm_codes, cm_sf);
     NVQ_LAUNCH_CHECK("weight_tail_cm_kernel");

@@ -117,15 +117,18 @@ class MoERacLayer:
               rows of every token.
     """
 
-    def __init__(self, w13: torch.Tensor, w2: torch.Tensor, k: int, topk: int, max_tokens: int):
+    def __init__(self, w13: torch.Tensor, w2: torch.Tensor, k: int, topk: int, max_tokens: int,
+                 k2: Optional[int] = None):
+        """k: compensated channels at the gate/up site (of H), k2 at the down site (of I; default k)."""
         dev = w13.device
         self.E, twoI, self.H = w13.shape
         self.I = twoI // 2
-        self.k, self.topk, self.T = k, topk, max_tokens
+        k2 = k if k2 is None else k2
+        self.k, self.k2, self.topk, self.T = k, k2, topk, max_tokens
         self.w13 = quantize_weights(w13, k)
-        self.w2 = quantize_weights(w2, k)
+        self.w2 = quantize_weights(w2, k2)
         self.w13_cm = ChannelMajor.of(self.w13, self.E, twoI) if k else None
-        self.w2_cm = ChannelMajor.of(self.w2, self.E, self.H) if k else None
+        self.w2_cm = ChannelMajor.of(self.w2, self.E, self.H) if k2 else None
         cap = L.moe_capacity(max_tokens, topk, self.E)
         self.cap = cap
         E = self.E
@@ -140,9 +143,9 @@ class MoERacLayer:
         self.idx1 = torch.zeros(max(k, 1), dtype=torch.int32, device=dev)
         self.a_routed = Operand.empty(cap, self.H, k, 1, device=dev)
         self.h = torch.zeros(cap, self.I, dtype=torch.bfloat16, device=dev)
-        self.a2 = Operand.empty(cap, self.I, k, E, device=dev)
+        self.a2 = Operand.empty(cap, self.I, k2, E, device=dev)
         self.scores2 = torch.zeros(E, self.I, dtype=torch.int64, device=dev)
-        self.idx2 = torch.zeros(E, max(k, 1), dtype=torch.int32, device=dev)
+        self.idx2 = torch.zeros(E, max(k2, 1), dtype=torch.int32, device=dev)
         self.y = torch.zeros(cap, self.H, dtype=torch.bfloat16, device=dev)
         # side stream for the work that does not depend on dispatch (token quantization and
         # selection) or on the gather (the gate/up weight tail); events fork and join it, so
@@ -158,18 +161,19 @@ class MoERacLayer:
         """Kernels one forward() launches: dispatch 4; tokens: amax + quantize 2, selection and
         residual tail 2; gather 1; gate/up: weight tail 1, GEMM 1; h: quantize 1 (its amax comes
         from the GEMM epilogue), selection and residual tail 2; down: weight tail 1, GEMM 1;
-        combine 1.  Without RAC (k = 0) there is no selection, no residual or weight tail."""
-        rac = 1 if self.k else 0
-        tok = 2 + 2 * rac
-        h = 1 + 2 * rac
-        return 4 + tok + 1 + (rac + 1) + h + (rac + 1) + 1
+        combine 1.  A site without RAC (k = 0) has no selection, residual or weight tail."""
+        rac1 = 1 if self.k else 0
+        rac2 = 1 if self.k2 else 0
+        tok = 2 + 2 * rac1
+        h = 1 + 2 * rac2
+        return 4 + tok + 1 + (rac1 + 1) + h + (rac2 + 1) + 1
 
     def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, out: torch.Tensor,
                 stream=None, events: Optional[dict] = None):
         """events: optional dict that receives (start, end) CUDA events around the stages
         'quant_rac_tokens', 'gemm_gate_up' and 'gemm_down' (for per-kernel timing)."""
         T = x.shape[0]
-        k, E, H, I = self.k, self.E, self.H, self.I
+        k, k2, E, H, I = self.k, self.k2, self.E, self.H, self.I
         st = torch.cuda.current_stream() if stream is None else stream
         side = self.side
 
@@ -208,21 +212,21 @@ class MoERacLayer:
         # down input: per-expert tensor scale (amax of h measured by the gate/up epilogue) and
         # channel set
         L.nvfp4_quantize(self.h, self.a2.codes, self.a2.sf, self.a2.sf_cols, self.a2.tscale,
-                         scores=self.scores2 if k else None, grp_off=self.grp_off, grp_rows=self.grp_rows,
-                         groups=E, zero_pad=(k == 0), amax_given=True, stream=st)
-        if k:
+                         scores=self.scores2 if k2 else None, grp_off=self.grp_off, grp_rows=self.grp_rows,
+                         groups=E, zero_pad=(k2 == 0), amax_given=True, stream=st)
+        if k2:
             # selection, then the down weight tail (needs idx2 only) beside the residual tail of h
-            L.rac_select(self.scores2, I, k, self.idx2, groups=E, stream=st)
+            L.rac_select(self.scores2, I, k2, self.idx2, groups=E, stream=st)
             self.ev_sel2.record(st)
             side.wait_event(self.ev_sel2)
-            _weight_tail(self.w2, self.w2_cm, E, H, k, self.idx2, idx_per_group=True, stream=side)
+            _weight_tail(self.w2, self.w2_cm, E, H, k2, self.idx2, idx_per_group=True, stream=side)
             self.ev_wt2.record(side)
-            L.rac_residual_tail(self.h, self.a2.tscale, self.idx2, k, self.a2.codes, self.a2.sf, self.a2.sf_cols,
+            L.rac_residual_tail(self.h, self.a2.tscale, self.idx2, k2, self.a2.codes, self.a2.sf, self.a2.sf_cols,
                                 grp_off=self.grp_off, grp_rows=self.grp_rows, groups=E, stream=st)
             st.wait_event(self.ev_wt2)
         mark("gemm_down", 0)
         L.w4a4_rac_grouped_gemm(self.a2.codes, self.a2.sf, self.a2.sf_cols, self.a2.tscale, self.w2.codes,
-                                self.w2.sf, self.w2.sf_cols, self.w2.tscale, H, I, k, None,
+                                self.w2.sf, self.w2.sf_cols, self.w2.tscale, H, I, k2, None,
                                 self.y, groups=E, grp_off=self.grp_off, grp_rows=self.grp_rows, rows=self.cap,
                                 a_scale_per_group=True, idx_per_group=True, epilogue=L.NVQ_EPI_ROW_SCALE,
                                 row_w=self.row_w, stream=st)

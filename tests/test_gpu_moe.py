@@ -31,8 +31,9 @@ def _operand_rows(op, rows, ktot):
     return codes, sfl
 
 
-def _check_layer(L, T, H, E, topk, I, k, routing, seed, sample_rows=None, n_outliers=None, max_experts=None):
-    """sample_rows: routed rows checked in the gate/up GEMM (None: all); max_experts: experts
+def _check_layer(L, T, H, E, topk, I, k, routing, seed, sample_rows=None, n_outliers=None, max_experts=None,
+                 k2=None):
+    """k / k2: compensated channels at the gate/up / down site (k2 defaults to k); sample_rows: routed rows checked in the gate/up GEMM (None: all); max_experts: experts
     checked in the gate/up and down stages (None: all)."""
     from nvfp4_w4a4_quantized_quantize_gb300.layers import MoERacLayer
     cfg = wl.MoELayer("t", T=T, H=H, E=E, topk=topk, I=I, k=k, seed=seed, routing=routing,
@@ -42,7 +43,8 @@ def _check_layer(L, T, H, E, topk, I, k, routing, seed, sample_rows=None, n_outl
     dev = "cuda"
     w13 = bf16_tensor(w13_bits.reshape(E * 2 * I, H)).view(E, 2 * I, H)
     w2 = bf16_tensor(w2_bits.reshape(E * H, I)).view(E, H, I)
-    layer = MoERacLayer(w13, w2, k, topk, T)
+    k2 = k if k2 is None else k2
+    layer = MoERacLayer(w13, w2, k, topk, T, k2=k2)
     x = bf16_tensor(x_bits)
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     layer.forward(x, torch.from_numpy(ids).to(dev), torch.from_numpy(tw).to(dev), out)
@@ -123,10 +125,10 @@ def _check_layer(L, T, H, E, topk, I, k, routing, seed, sample_rows=None, n_outl
     for g in experts:
         c = int(grp_rows[g])
         rows_g = np.arange(grp_off[g], grp_off[g] + c)
-        hq = oracle.rac_quantize(h_gpu[rows_g], k)
+        hq = oracle.rac_quantize(h_gpu[rows_g], k2)
         assert np.float32(hq.ts.amax) == a2_amax[g] and np.float32(hq.ts.s_dec) == a2_sdec[g]
-        assert np.array_equal(idx2[g, :k], hq.idx)
-        ac, as_ = _operand_rows(layer.a2, rows_g, I + k)
+        assert np.array_equal(idx2[g, :k2], hq.idx)
+        ac, as_ = _operand_rows(layer.a2, rows_g, I + k2)
         assert np.array_equal(ac, np.concatenate([hq.codes, hq.tail_codes], 1))
         assert np.array_equal(as_, np.concatenate([hq.scales, hq.tail_scales], 1))
         if sample_rows is not None and c > 64:
@@ -137,7 +139,7 @@ def _check_layer(L, T, H, E, topk, I, k, routing, seed, sample_rows=None, n_outl
         wts = oracle.tensor_scale(wg)
         wc, ws = oracle.quantize(wg, wts)
         tc, tsc = oracle.weight_tail(wc, ws, wts, hq.idx)
-        bc, bs = _operand_rows(layer.w2, np.arange(g * H, (g + 1) * H), I + k)
+        bc, bs = _operand_rows(layer.w2, np.arange(g * H, (g + 1) * H), I + k2)
         assert np.array_equal(bc, np.concatenate([wc, tc], 1)) and np.array_equal(bs, np.concatenate([ws, tsc], 1))
         ref = oracle.gemm(ac[pick], as_[pick], bc, bs, hq.ts.s_dec, wts.s_dec)
         ref = ref * row_w[rows_g[pick]][:, None].astype(np.float64)
@@ -163,6 +165,12 @@ def test_moe_layer_small_uniform_topk8(L):
 
 def test_moe_layer_without_rac(L):
     _check_layer(L, T=130, H=256, E=4, topk=2, I=128, k=0, routing="uniform", seed=23)
+
+
+@pytest.mark.parametrize("k,k2", [(128, 64), (0, 32), (48, 0), (256, 128)])
+def test_moe_layer_per_site_k(L, k, k2):
+    """Different channel counts at the two sites, up to k = K at both (H = 256, I = 128)."""
+    _check_layer(L, T=260, H=256, E=8, topk=2, I=128, k=k, k2=k2, routing="zipf", seed=24 + k + k2)
 
 
 @pytest.mark.parametrize("use_graph", [True, False])

@@ -20,6 +20,17 @@ def L():
     return _lib
 
 
+@pytest.fixture
+def tail_path(L, request):
+    """Forces one schedule of the tail columns (nvq_set_tail_path) for the test, then restores auto."""
+    L.set_tail_path(request.param)
+    yield request.param
+    L.set_tail_path(L.NVQ_TAIL_AUTO)
+
+
+PATHS = pytest.mark.parametrize("tail_path", [1, 2], indirect=True, ids=["gather", "rows"])
+
+
 def _gpu_quant(L, x_bits, k=0, groups=1, grp_off=None, grp_rows=None, ktail=None):
     M, K = x_bits.shape
     x = bf16_tensor(x_bits)
@@ -119,7 +130,8 @@ def test_quantize_extreme_scales(L):
 @pytest.mark.parametrize("M,K,k", [(64, 256, 16), (200, 512, 64), (96, 768, 32), (50, 256, 256), (17, 4096, 64),
                                    (31, 6144, 128), (130, 768, 384), (40, 2048, 1024), (9, 4096, 4096),
                                    (64, 1024, 1024)])
-def test_rac_select_and_tail_dense(L, M, K, k):
+@PATHS
+def test_rac_select_and_tail_dense(L, M, K, k, tail_path):
     x, _ = wl.activations(M, K, seed=7 * M + K, n_outliers=max(2, K // 64), outlier_gain=16.0)
     g = _gpu_quant(L, x, k=k)
     q = oracle.rac_quantize(x, k)
@@ -147,7 +159,8 @@ def test_topk_ties_and_degenerate(L):
     assert list(g["idx"][0]) == list(range(32))
 
 
-def test_grouped_quantize_scores_and_tails(L):
+@PATHS
+def test_grouped_quantize_scores_and_tails(L, tail_path):
     """Row groups with padding gaps (the routed layout): per-group tensor scale, scores, S."""
     rng = np.random.default_rng(11)
     G, K, k = 6, 768, 32
@@ -241,7 +254,8 @@ def test_argument_errors_are_reported_before_launch(L):
                                                (2, 128, 16, 16, True), (4, 128, 1536, 48, True),
                                                (1, 128, 768, 400, False), (2, 128, 1536, 768, True),
                                                (1, 256, 256, 256, False)])
-def test_weight_tail_channel_major_path(L, G, N, K, k, per_group):
+@PATHS
+def test_weight_tail_channel_major_path(L, G, N, K, k, per_group, tail_path):
     """nvfp4_channel_major holds every code and scale of the weights at its channel-major place,
     and rac_weight_tail from that copy writes the same bytes as the row-major path and the oracle
     (ragged K: 272 = 17 blocks, 136 code bytes per row)."""
@@ -310,7 +324,8 @@ def test_quantize_with_given_amax_equals_measured(L):
     assert np.array_equal(scores.cpu().numpy().view(np.uint64), a["scores"])
 
 
-def test_select_and_residual_tail_split_equals_combined(L):
+@PATHS
+def test_select_and_residual_tail_split_equals_combined(L, tail_path):
     """rac_select followed by rac_residual_tail writes exactly what rac_select_quantize writes."""
     counts = [300, 0, 129]
     off = [0, 384, 384, 640]
