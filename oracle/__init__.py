@@ -88,6 +88,10 @@ def lib():
             "oracle_e4m3_encode_array": ([P, I64, P], None),
             "oracle_bf16_round_array": ([P, I64, P], None),
             "oracle_quantize_block16": ([P, C.c_float, P, P], None),
+            "oracle_fp8_scale_exponent": ([C.c_double], C.c_int32),
+            "oracle_fp8_encode": ([C.c_double], C.c_uint8),
+            "oracle_fp8_quantize": ([P, I64, I64, I64, I32, P, I64, P, I64], None),
+            "oracle_fp8_dequantize": ([P, I64, P, I64, I64, I64, I32, P, I64], None),
         }
         for name, (args, res) in sig.items():
             f = getattr(_lib, name)
@@ -326,3 +330,35 @@ def rac_quantize(x: np.ndarray, k: int) -> RacQuant:
         tc = np.zeros((x.shape[0], 0), np.uint8)
         tsc = np.zeros((x.shape[0], 0), np.uint8)
     return RacQuant(ts, codes, scales, s, idx, tc, tsc)
+
+
+# ---------------------------------------------------------------- FP8 W8A8 comparison baseline
+# QUADS §2.2 "FP8" (E4M3, a scale per tile of values) and §4.4.2 (FP8 W8A8 rollout as the
+# production baseline).  Tiles and scale encoding: readings R11-R13 of nvfp4_oracle.c.
+def fp8_scale_exponent(amax: float) -> int:
+    return int(lib().oracle_fp8_scale_exponent(float(amax)))
+
+
+def fp8_quantize(x: np.ndarray, tile_rows: int):
+    """bf16 bits [R, C] -> E4M3 codes [R, C] and UE8M0 tile bytes [ceil(R/tile_rows), ceil(C/128)]."""
+    x = _bf16(x)
+    R, Cc = x.shape
+    codes = np.zeros((R, Cc), np.uint8)
+    st = np.zeros(((R + tile_rows - 1) // tile_rows, (Cc + 127) // 128), np.uint8)
+    lib().oracle_fp8_quantize(_p(x), R, Cc, Cc, tile_rows, _p(codes), Cc, _p(st), st.shape[1])
+    return codes, st
+
+
+def fp8_dequantize(codes: np.ndarray, scales: np.ndarray, tile_rows: int) -> np.ndarray:
+    codes = np.ascontiguousarray(codes)
+    scales = np.ascontiguousarray(scales)
+    R, Cc = codes.shape
+    out = np.zeros((R, Cc), np.float64)
+    lib().oracle_fp8_dequantize(_p(codes), Cc, _p(scales), scales.shape[1], R, Cc, tile_rows, _p(out), Cc)
+    return out
+
+
+def fp8_gemm(a_codes, a_scales, b_codes, b_scales) -> np.ndarray:
+    """Y = DQ(A) DQ(B)^T in fp64 (A: 1 x 128 tiles, B: 128 x 128 tiles); the products of
+    dequantized values are exact and the matmul accumulates in fp64."""
+    return fp8_dequantize(a_codes, a_scales, 1) @ fp8_dequantize(b_codes, b_scales, 128).T

@@ -37,6 +37,16 @@
  *      is quantized with blocks of 16 gathered channels and the activation's own S_enc.
  *   R10 Weight tail: the weight columns that multiply the correction are the dequantized
  *      stored weights on the selected channels, re-quantized with the weight's own S_enc.
+ *   R11 FP8 W8A8 baseline (§2.2 "FP8": "each tile of values carries its own alpha in
+ *      Eq. (4)", tile sizes unstated): activation tiles of 1 x 128 (one row, 128 consecutive
+ *      channels), weight tiles of 128 x 128 (128 output rows x 128 input channels); a tile cut
+ *      by the matrix edge covers what is left.
+ *   R12 FP8 tile scale alpha = 2^e, e the smallest integer with 448 * 2^e >= amax of the tile,
+ *      clamped to [-127, 127] (an all-zero tile gets -127): a power of two, stored as the byte
+ *      e + 127 (UE8M0).
+ *   R13 FP8 element: E4M3 of x * 2^-e, nearest value, ties to the even code, sign kept (a
+ *      negative value that rounds to zero gives 0x80); |x * 2^-e| <= 448 by R12.  The
+ *      dequantized value V * 2^e is exact.
  *
  * Arithmetic: IEEE binary32 with round-to-nearest-even for every step the method performs in
  * FP32 (compile with -ffp-contract=off so that no multiply-add is fused); fp64 / exact
@@ -115,10 +125,9 @@ double oracle_e4m3_value(uint8_t b)
     return s ? -mag : mag;
 }
 
-/* Reading R3: for t >= 0, nearest finite non-negative E4M3 value, ties to the even code. */
-uint8_t oracle_e4m3_encode(float t)
+/* Nearest finite non-negative E4M3 code to a >= 0, ties to the even code (readings R3, R13). */
+static uint8_t e4m3_nearest(double a)
 {
-    double a = (double)t;
     int best = 0;
     double bestd = INFINITY;
     for (int c = 0; c <= 0x7e; ++c) {
@@ -130,6 +139,9 @@ uint8_t oracle_e4m3_encode(float t)
     }
     return (uint8_t)best;
 }
+
+/* Reading R3: for t >= 0, nearest finite non-negative E4M3 value, ties to the even code. */
+uint8_t oracle_e4m3_encode(float t) { return e4m3_nearest((double)t); }
 
 /* ------------------------------------------------------------------------------------------
  * Per-tensor FP32 scale (QUADS §2.2 "FP4", the second scaling level; formula: reading R4).
@@ -463,4 +475,60 @@ void oracle_bf16_round_array(const float* f, int64_t n, uint16_t* out)
 void oracle_quantize_block16(const float* v, float s_enc, uint8_t* codes, uint8_t* sb)
 {
     quantize_block16(v, s_enc, codes, sb);
+}
+
+/* ------------------------------------------------------------------------------------------
+ * FP8 W8A8 with fine-grained tile scaling, the comparison baseline of QUADS §2.2 "FP8" and
+ * §4.4.2 (readings R11-R13).
+ * ---------------------------------------------------------------------------------------- */
+
+/* Reading R12, by search: the smallest e in [-127, 127] with 448 * 2^e >= amax. */
+int32_t oracle_fp8_scale_exponent(double amax)
+{
+    if (!(amax > 0.0)) return -127;
+    int32_t e = -127;
+    while (e < 127 && ldexp(448.0, e) < amax) ++e;
+    return e;
+}
+
+/* Reading R13 for a value already divided by its tile scale: sign bit, then the nearest
+ * magnitude code. */
+uint8_t oracle_fp8_encode(double v)
+{
+    uint8_t mag = e4m3_nearest(fabs(v));
+    return (uint8_t)(signbit(v) ? (mag | 0x80u) : mag);
+}
+
+/* Tiles of tile_rows x 128 (tile_rows 1: activations, 128: weights), row-major codes
+ * [rows][ld_codes] and one UE8M0 byte per tile in scales[row tile][column tile]. */
+void oracle_fp8_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx, int32_t tile_rows,
+                         uint8_t* codes, int64_t ld_codes, uint8_t* scales, int64_t ld_scales)
+{
+    for (int64_t r0 = 0; r0 < rows; r0 += tile_rows)
+        for (int64_t c0 = 0; c0 < cols; c0 += 128) {
+            const int64_t r1 = r0 + tile_rows < rows ? r0 + tile_rows : rows;
+            const int64_t c1 = c0 + 128 < cols ? c0 + 128 : cols;
+            double amax = 0.0;
+            for (int64_t i = r0; i < r1; ++i)
+                for (int64_t j = c0; j < c1; ++j) {
+                    const double a = fabs((double)bf16_value(x[i * ldx + j]));
+                    if (a > amax) amax = a;
+                }
+            const int32_t e = oracle_fp8_scale_exponent(amax);
+            scales[(r0 / tile_rows) * ld_scales + c0 / 128] = (uint8_t)(e + 127);
+            for (int64_t i = r0; i < r1; ++i)
+                for (int64_t j = c0; j < c1; ++j)
+                    codes[i * ld_codes + j] = oracle_fp8_encode(ldexp((double)bf16_value(x[i * ldx + j]), -e));
+        }
+}
+
+/* V * 2^e in fp64, out [rows][ld_out]. */
+void oracle_fp8_dequantize(const uint8_t* codes, int64_t ld_codes, const uint8_t* scales, int64_t ld_scales,
+                           int64_t rows, int64_t cols, int32_t tile_rows, double* out, int64_t ld_out)
+{
+    for (int64_t i = 0; i < rows; ++i)
+        for (int64_t j = 0; j < cols; ++j) {
+            const int32_t e = (int32_t)scales[(i / tile_rows) * ld_scales + j / 128] - 127;
+            out[i * ld_out + j] = ldexp(oracle_e4m3_value(codes[i * ld_codes + j]), e);
+        }
 }

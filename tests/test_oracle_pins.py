@@ -398,3 +398,92 @@ def test_swiglu_and_combine_against_torch():
         acc = acc + yt[:, s]
     ref = acc.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(out, ref)
+
+
+# ---------------------------------------------------------------- FP8 W8A8 baseline (readings R11-R13)
+def test_fp8_encode_matches_torch_float8_on_every_bf16_value():
+    """Reading R13's E4M3 rounding (nearest, ties to even, sign kept) against torch's own
+    float8_e4m3fn conversion, for every finite bf16 value of magnitude <= 448."""
+    import torch
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):
+        v = wl.bf16_bits_to_f32(bits).astype(np.float64)
+    ok = np.isfinite(v) & (np.abs(v) <= 448.0)
+    v = v[ok]
+    ours = np.array([oracle.lib().oracle_fp8_encode(float(t)) for t in v], np.uint8)
+    ref = torch.from_numpy(v.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_fp8_scale_exponent_closed_form():
+    """Reading R12: e = max(-127, ceil(log2(amax / 448))), computed with exact rationals, on
+    random and boundary magnitudes."""
+    import math
+    rng = np.random.default_rng(40)
+    vals = list(np.exp(rng.uniform(-90, 90, 2000)))
+    for k in range(-130, 128, 7):
+        b = math.ldexp(448.0, k)
+        vals += [b, np.nextafter(b, 0), np.nextafter(b, np.inf)]
+    vals += [1e-45, 5e-40, 448.0, 449.0, 3.0e38]
+    from fractions import Fraction
+    for a in vals:
+        # ceil(log2(a / 448)) by exact rational comparison with powers of two
+        q = Fraction(float(a)) / 448
+        c = math.ceil(math.log2(q))
+        while Fraction(2) ** c < q:
+            c += 1
+        while Fraction(2) ** (c - 1) >= q:
+            c -= 1
+        assert oracle.fp8_scale_exponent(a) == max(-127, min(127, c)), a
+    assert oracle.fp8_scale_exponent(0.0) == -127
+
+
+def test_fp8_tiles_scale_independently_and_round_trip_within_e4m3_bound():
+    """1 x 128 activation tiles and 128 x 128 weight tiles (reading R11): scaling one tile by a
+    power of two changes only its scale byte, by that power, and none of the codes; every
+    element dequantizes within half an E4M3 step of its value (relative 2^-4 in the normal
+    range, absolute 2^(e-10) below it); ragged edges form partial tiles."""
+    x = _rand_x(5, 300, 41, outliers=3)  # 300 = 2 x 128 + 44
+    c, s = oracle.fp8_quantize(x, 1)
+    assert s.shape == (5, 3)
+    xf = wl.bf16_bits_to_f32(x).astype(np.float64)
+    x2 = xf.copy()
+    x2[3, 128:256] *= 2.0 ** 5
+    c2, s2 = oracle.fp8_quantize(wl.to_bf16_bits(x2), 1)
+    assert np.array_equal(c, c2)
+    d = s2.astype(int) - s.astype(int)
+    assert d[3, 1] == 5 and np.count_nonzero(d) == 1
+    dq = oracle.fp8_dequantize(c, s, 1)
+    e = np.repeat(s.astype(np.int64) - 127, 128, axis=1)[:, :300]
+    scaled = np.abs(xf) * 2.0 ** (-e)
+    err = np.abs(dq - xf) * 2.0 ** (-e)
+    normal = scaled >= 2.0 ** -6
+    assert np.all(err[normal] <= scaled[normal] * 2.0 ** -4)
+    assert np.all(err[~normal] <= 2.0 ** -10)
+    # the tile maximum maps to at most 448 and above 224 (the scale is the smallest power)
+    for i in range(5):
+        for t in range(3):
+            m = np.abs(xf[i, 128 * t:128 * (t + 1)]).max()
+            if m > 0:
+                assert 224.0 < m * 2.0 ** (127 - int(s[i, t])) <= 448.0
+    # weights: 128 x 128 tiles; an outlier in one tile leaves the others' scales alone
+    w = wl.weights((256, 256), 0.02, 42)
+    wc, ws = oracle.fp8_quantize(w, 128)
+    wf = wl.bf16_bits_to_f32(w).astype(np.float64)
+    wf[200, 30] = 50.0
+    wc2, ws2 = oracle.fp8_quantize(wl.to_bf16_bits(wf), 128)
+    assert ws.shape == (2, 2) and ws2[1, 0] > ws[1, 0]
+    assert ws2[0, 0] == ws[0, 0] and ws2[0, 1] == ws[0, 1] and ws2[1, 1] == ws[1, 1]
+
+
+def test_fp8_gemm_against_torch_float8_decode():
+    """fp8_gemm against the same product with torch's float8_e4m3fn decoding of the codes."""
+    import torch
+    x = _rand_x(40, 384, 43, outliers=4)
+    w = wl.weights((136, 384), 0.02, 44)
+    ac, asc = oracle.fp8_quantize(x, 1)
+    bc, bsc = oracle.fp8_quantize(w, 128)
+    dec = lambda c: torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    a = dec(ac) * np.exp2(np.repeat(asc.astype(np.float64) - 127, 128, axis=1))
+    b = dec(bc) * np.exp2(np.repeat(np.repeat(bsc.astype(np.float64) - 127, 128, axis=0)[:136], 128, axis=1))
+    assert np.allclose(oracle.fp8_gemm(ac, asc, bc, bsc), a @ b.T, rtol=1e-12, atol=0)
