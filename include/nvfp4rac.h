@@ -372,6 +372,62 @@ nvq_status nvfp4_gather_rows(const uint8_t* codes, int64_t ld_codes, const uint8
 nvq_status moe_combine(const void* y, int64_t ldy, const int64_t* row_of, int64_t tokens,
                        int32_t topk, int64_t hidden, void* out, int64_t ldo, void* stream);
 
+/* ==========================================================================================
+ * FP8 W8A8 block-scaled baseline.  The paper's throughput comparison (§4.4.2: plain W4A4 about
+ * 1.3x FP8, W4A4 + RAC about 1.16x) is against FP8 W8A8 rollout with fine-grained block scaling
+ * (§2.2 "FP8": E4M3 elements, maximum 448, "each tile of values carries its own alpha", as
+ * DeepGEMM does).  Readings where the pages are silent: activation tiles are 1 x 128 (one row,
+ * 128 consecutive channels), weight tiles 128 x 128; the tile scale is the power of two
+ * alpha = 2^e with e the smallest integer such that 448 * 2^e >= amax of the tile, clamped to
+ * [-127, 127] (an all-zero tile gets -127), stored as the UE8M0 byte e + 127 and applied by
+ * the tensor core (kind::mxf8f6f4, one scale per 32 elements); an element is E4M3 of
+ * x * 2^-e, nearest, ties to even, sign kept.
+ *
+ * Operand layout: codes [rows][ld] E4M3 bytes, K-major; scales in the blocked layout of
+ * nvq_sf_offset with sf_cols = nvq_fp8_sf_cols(K) columns of one UE8M0 byte per 32 elements
+ * (a tile's byte repeated in its 4 columns and, for weights, its 128 rows); a buffer for R rows
+ * holds nvq_sf_bytes(R, sf_cols) bytes.
+ * ========================================================================================== */
+int64_t nvq_fp8_sf_cols(int64_t K);  /* roundup(K / 32, 4) */
+
+/*
+ * fp8_quantize -- x [rows][ldx] bf16 (16-byte aligned rows) to E4M3 codes [rows][ld_codes]
+ * (ld_codes % 16 == 0, 16-byte aligned) and UE8M0 tile scales in sf.  tile_rows 1: 1 x 128
+ * activation tiles; tile_rows 128: 128 x 128 weight tiles starting at row 0 (for stacked
+ * per-expert weights of N rows each, N % 128 == 0 keeps every tile inside one expert).
+ * K % 32 == 0, 32 <= K <= 16384.  Scale columns of a partial last tile beyond K / 32 are zeroed
+ * within its 4-column word; rows beyond `rows` are not written.  Errors: NVQ_ERR_ARG,
+ * NVQ_ERR_SHAPE, NVQ_ERR_ALIGN, NVQ_ERR_CUDA.
+ */
+nvq_status fp8_quantize(const void* x, int64_t rows, int64_t K, int64_t ldx, int32_t tile_rows, uint8_t* codes,
+                        int64_t ld_codes, uint8_t* sf, int64_t sf_cols, void* stream);
+
+/*
+ * fp8_blockscaled_grouped_gemm -- Y[r, n] = sum_c V[a_rc] 2^ea(r, c/128) V[b_nc] 2^eb(n/128, c/128)
+ * over row groups (routed experts), the FP8 counterpart of w4a4_rac_grouped_gemm (same tcgen05
+ * kernel with E4M3 operands and UE8M0 scales; no tensor scale and no RAC columns).  Arguments as
+ * for w4a4_rac_grouped_gemm: groups / grp_off / grp_rows / rows, A codes [rows][lda], B codes
+ * [groups * N][ldb] (lda, ldb multiples of 16 covering K bytes, 16-byte aligned), scales with
+ * sf_cols >= nvq_fp8_sf_cols(K), N % 256 == 0, epilogue NVQ_EPI_STORE / SWIGLU / ROW_SCALE /
+ * STORE_F32 with row_w, out [rows][ldo].  K % 32 == 0, 32 <= K <= 16384.  Device waits are bounded
+ * (nvq_device_status).  Errors as for w4a4_rac_grouped_gemm.
+ */
+nvq_status fp8_blockscaled_grouped_gemm(int32_t groups, const int64_t* grp_off, const int64_t* grp_rows, int64_t rows,
+                                        const uint8_t* a_codes, int64_t lda, const uint8_t* a_sf, int64_t a_sf_cols,
+                                        const uint8_t* b_codes, int64_t ldb, const uint8_t* b_sf, int64_t b_sf_cols,
+                                        int64_t N, int64_t K, int32_t epilogue, const float* row_w, void* out,
+                                        int64_t ldo, void* stream);
+
+/*
+ * fp8_gather_rows -- nvfp4_gather_rows for FP8 operands: row i of the routed layout receives
+ * the K code bytes and the scales of token row_src[i] / topk (zeros where row_src[i] < 0).
+ * capacity = the routed layout's rows (a multiple of 128); out_sf has capacity rows of sf_cols
+ * columns.  Errors: NVQ_ERR_ARG, NVQ_ERR_SHAPE, NVQ_ERR_ALIGN, NVQ_ERR_CUDA.
+ */
+nvq_status fp8_gather_rows(const uint8_t* codes, int64_t ld_codes, const uint8_t* sf, int64_t sf_cols, int64_t src_rows,
+                           const int32_t* row_src, int32_t topk, int64_t capacity, int64_t K, uint8_t* out_codes,
+                           int64_t ld_out, uint8_t* out_sf, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

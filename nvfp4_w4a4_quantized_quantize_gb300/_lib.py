@@ -39,6 +39,11 @@ _SIGS = {
     "moe_dispatch": ([_P, _P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _I64, _P, C.c_size_t, _P], C.c_int),
     "moe_dispatch_static_scratch": ([_P, _P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _I64, _P], C.c_int),
     "nvfp4_gather_rows": ([_P, _I64, _P, _I64, _I64, _P, _I32, _I64, _I64, _I64, _P, _I64, _P, _P], C.c_int),
+    "nvq_fp8_sf_cols": ([_I64], _I64),
+    "fp8_quantize": ([_P, _I64, _I64, _I64, _I32, _P, _I64, _P, _I64, _P], C.c_int),
+    "fp8_blockscaled_grouped_gemm": ([_I32, _P, _P, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _I32, _P, _P,
+                                      _I64, _P], C.c_int),
+    "fp8_gather_rows": ([_P, _I64, _P, _I64, _I64, _P, _I32, _I64, _I64, _P, _I64, _P, _P], C.c_int),
     "moe_combine": ([_P, _I64, _P, _I64, _I32, _I64, _P, _I64, _P], C.c_int),
 }
 
@@ -226,6 +231,32 @@ def nvfp4_gather_rows(codes, sf, sf_cols_, src_rows, row_src, topk, ktot, out_co
     _check("nvfp4_gather_rows", LIB.nvfp4_gather_rows(
         _ptr(codes), codes.stride(0), _ptr(sf), sf_cols_, src_rows, _ptr(row_src), topk, row_src.numel(), ktot, col0,
         _ptr(out_codes), out_codes.stride(0) if out_codes is not None else 0, _ptr(out_sf), _stream(stream)))
+
+
+def fp8_sf_cols(K: int) -> int:
+    return int(LIB.nvq_fp8_sf_cols(K))
+
+
+def fp8_quantize(x, codes, sf, sf_cols_, tile_rows=1, rows=None, K=None, stream=None):
+    rows = x.shape[0] if rows is None else rows
+    K = x.shape[-1] if K is None else K
+    _check("fp8_quantize", LIB.fp8_quantize(
+        _ptr(x), rows, K, x.stride(-2), tile_rows, _ptr(codes), codes.stride(0), _ptr(sf), sf_cols_, _stream(stream)))
+
+
+def fp8_blockscaled_grouped_gemm(a_codes, a_sf, a_sf_cols, b_codes, b_sf, b_sf_cols, N, K, out, groups=1, grp_off=None,
+                                 grp_rows=None, rows=None, epilogue=NVQ_EPI_STORE, row_w=None, stream=None):
+    rows = a_codes.shape[0] if rows is None else rows
+    _check("fp8_blockscaled_grouped_gemm", LIB.fp8_blockscaled_grouped_gemm(
+        groups, _ptr(grp_off), _ptr(grp_rows), rows, _ptr(a_codes), a_codes.stride(0), _ptr(a_sf), a_sf_cols,
+        _ptr(b_codes), b_codes.stride(0), _ptr(b_sf), b_sf_cols, N, K, epilogue, _ptr(row_w), _ptr(out), out.stride(0),
+        _stream(stream)))
+
+
+def fp8_gather_rows(codes, sf, sf_cols_, src_rows, row_src, topk, K, out_codes, out_sf, stream=None):
+    _check("fp8_gather_rows", LIB.fp8_gather_rows(
+        _ptr(codes), codes.stride(0), _ptr(sf), sf_cols_, src_rows, _ptr(row_src), topk, row_src.numel(), K,
+        _ptr(out_codes), out_codes.stride(0), _ptr(out_sf), _stream(stream)))
 
 
 def moe_combine(y, row_of, tokens, topk, hidden, out, stream=None):

@@ -24,6 +24,11 @@
 //              12 small copies per K-tile cost about 40% of the MMA rate;
 //   warps 6-13 epilogue: tcgen05.ld of the accumulator, alpha scaling, bf16 store, with the
 //              SwiGLU or routing-weight variants.
+// The same kernel, instantiated for E4M3 operands (kind::mxf8f6f4, scale_vec::1X, one UE8M0
+// scale per 32 elements, K = 32 per MMA, 128 elements per 128-byte K-tile row, no tensor
+// scale), is the FP8 W8A8 block-scaled baseline the paper compares against (§2.2 "FP8",
+// §4.4.2): a stage then holds one scale atom per 128 rows, and MMA j of the stage reads byte j
+// of each scale word (the scale-factor ID fields of the instruction descriptor).
 // Every mbarrier wait is bounded; on expiry the kernel records NVQ_ERR_TIMEOUT and unwinds.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -33,20 +38,15 @@
 
 namespace nvq {
 
-constexpr int kBM = 128, kBN = 256, kBK = 256;  // kBK in FP4 elements (128 bytes per row)
-constexpr int kAtoms = kBK / 64;            // K = 64 steps per stage: MMAs, and scale atoms per 128 rows
-constexpr int kStages = 4;                  // 4 x 54 KB (a 128-element K-tile in 8 x 27 KB was slower:
-                                            // twice the per-stage hand-offs)
-constexpr int kRowBytes = kBK / 2;          // bytes of a tile row in shared memory = swizzle span
-constexpr uint32_t kSwizzleLayout = kRowBytes == 128 ? 2u : 4u;  // tcgen05 smem layout: 128B = 2, 64B = 4
+constexpr int kBM = 128, kBN = 256;
+constexpr int kRowBytes = 128;              // bytes of a K-tile row in shared memory = swizzle span
+constexpr int kStages = 4;                  // 4 x 54 KB for FP4 (a 128-element K-tile in 8 x 27 KB was
+                                            // slower: twice the per-stage hand-offs)
+constexpr uint32_t kSwizzleLayout = 2u;     // tcgen05 smem layout: 128-byte swizzle
 constexpr uint32_t kSBO = 8 * kRowBytes;    // stride between 8-row core-matrix groups
-constexpr int kABytes = kBM * kBK / 2;      // 16384
-constexpr int kBBytes = kBN * kBK / 2;      // 32768
-constexpr int kSFABytes = kBM * kBK / 16;   // 2048: kAtoms atoms of 512 B
-constexpr int kSFBBytes = kBN * kBK / 16;   // 4096: 2 row blocks x kAtoms atoms
-constexpr int kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;  // 55296 (54 x 1024)
-static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned");
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+constexpr int kABytes = kBM * kRowBytes;    // 16384
+constexpr int kBBytes = kBN * kRowBytes;    // 32768
+constexpr int kMmaPerStage = 4;             // 32 bytes of every tile row per MMA
 constexpr int kThreads = 448;  // warp 0 TMA, warp 1 MMA, warps 2-5 scale staging, warps 6-13 epilogue
 constexpr int kFirstEpiWarp = 6;
 constexpr int kEpiThreads = 256;
@@ -54,8 +54,65 @@ constexpr int kMaxGroups = 512;
 constexpr int kCluster = 2;  // CTAs sharing one weight tile by multicast
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;                  // 256 fp32 columns
-constexpr uint32_t kSFCol = 256;                 // + stage * 48: SFA 16 columns, SFB 32 columns
-constexpr uint32_t kSFColsPerStage = 12 * kAtoms;  // SFA 4 columns + SFB 8 columns per K = 64
+constexpr uint32_t kSFCol = 256;                 // + stage * F::kSFColsPerStage
+
+// Operand formats.  A scale atom is the blocked layout's 512 bytes: 128 rows x 4 scale columns.
+struct Fp4 {  // NVFP4: E2M1 x E2M1, one UE4M3 scale per 16 elements, scale_vec::4X
+    static constexpr int kElemsPerStage = 256;  // per 128-byte row
+    static constexpr int kMmaK = 64;
+    static constexpr int kSfVec = 16;
+    // A/B format E2M1 (1) in bits 7-9 / 10-12, K-major A and B, N >> 3 in bits 17-22, scale
+    // type UE4M3 (bit 23 = 0), M >> 4 in bits 24-28.
+    static constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+    static constexpr uint32_t idesc(int) { return kIdesc; }
+    __device__ static void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t sfa_tmem,
+                               uint32_t sfb_tmem, uint32_t accumulate)
+    {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+                d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+            : "memory");
+    }
+};
+
+struct Fp8 {  // FP8: E4M3 x E4M3, one UE8M0 scale per 32 elements, scale_vec::1X
+    static constexpr int kElemsPerStage = 128;
+    static constexpr int kMmaK = 32;
+    static constexpr int kSfVec = 32;
+    // A/B format E4M3 (0), K-major, N >> 3 in bits 17-22, scale type UE8M0 (bit 23 = 1),
+    // M >> 4 in bits 24-28; the scale-factor IDs (byte of the 32-bit scale word) of B in bits
+    // 4-5 and of A in bits 29-30.
+    static constexpr uint32_t kIdesc = ((uint32_t)(kBN >> 3) << 17) | (1u << 23) | ((uint32_t)(kBM >> 4) << 24);
+    static constexpr uint32_t idesc(int j) { return kIdesc | ((uint32_t)j << 4) | ((uint32_t)j << 29); }
+    __device__ static void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t sfa_tmem,
+                               uint32_t sfb_tmem, uint32_t accumulate)
+    {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+                d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+            : "memory");
+    }
+};
+
+// Per-format stage geometry.
+template <class F>
+struct Geo {
+    static constexpr int kSfAtoms = F::kElemsPerStage / (4 * F::kSfVec);  // per 128 rows: FP4 4, FP8 1
+    static constexpr int kSFABytes = 512 * kSfAtoms;
+    static constexpr int kSFBBytes = 1024 * kSfAtoms;                     // 2 row blocks
+    static constexpr int kStageBytes = (kABytes + kBBytes + kSFABytes + kSFBBytes + 1023) / 1024 * 1024;
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+    static constexpr uint32_t kSFColsPerStage = 12 * kSfAtoms;            // SFA 4 + SFB 8 per atom
+    // scale atom of MMA j of a stage (FP4: one per MMA; FP8: one for all four)
+    static constexpr int atom_of(int j) { return (j * F::kMmaK) / (4 * F::kSfVec); }
+    // atoms holding the scales of the first n MMAs
+    static constexpr int atoms_for(int n_mma) { return (n_mma * F::kMmaK + 4 * F::kSfVec - 1) / (4 * F::kSfVec); }
+};
+static_assert(Geo<Fp4>::kStageBytes == 55296 && Geo<Fp8>::kStageBytes == 51200, "stage sizes");
 
 struct GemmArgs {
     Groups gr;              // A row groups
@@ -195,21 +252,6 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
            ((uint64_t)((sbo >> 4) & 0x3fffu) << 32) | (1ull << 46) | ((uint64_t)layout << 61);
 }
 
-// Instruction descriptor, block-scaled kinds: A/B format E2M1 (1) in bits 7-9 / 10-12,
-// K-major A and B, N >> 3 in bits 17-22, scale type UE4M3 (bit 23 = 0), M >> 4 in bits 24-28.
-constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-
-__device__ __forceinline__ void mma_fp4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t sfa_tmem,
-                                        uint32_t sfb_tmem, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
-            d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
-        : "memory");
-}
-
 // Two 32-column accumulator loads, one wait.
 __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float* va, float* vb)
 {
@@ -237,7 +279,14 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float* va,
     }
 }
 
-// 8 / 16 / 32 consecutive TMEM columns of this warp's 32 lanes from registers.
+// 4 / 8 / 16 / 32 consecutive TMEM columns of this warp's 32 lanes from registers.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t* v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+                 "r"(v[3])
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v)
 {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
@@ -376,9 +425,15 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
         : "memory");
 }
 
+template <class F>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                            const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a)
 {
+    using GF = Geo<F>;
+    constexpr int kStageBytes = GF::kStageBytes;
+    constexpr int kSFABytes = GF::kSFABytes, kSFBBytes = GF::kSFBBytes;
+    constexpr int kSfAtoms = GF::kSfAtoms;
+    constexpr uint32_t kSFColsPerStage = GF::kSFColsPerStage;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kStages], sf_bar[kStages], empty_bar[kStages], acc_full, acc_empty, drain_bar;
     __shared__ uint32_t tmem_base_slot;
@@ -450,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int total_mtiles = tab.mt_pre[G];
     const int n_tiles = (int)(a.N / kBN);
     const int64_t total_tiles = (int64_t)total_mtiles * n_tiles;
-    const int num_kt = (a.ktot + kBK - 1) / kBK;
+    const int num_kt = (a.ktot + F::kElemsPerStage - 1) / F::kElemsPerStage;
     volatile int* abrt = &abort_flag;
 
     if (warp == 0) {
@@ -473,8 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             if (lane == 0) {
                 for (int kt = 0; kt < num_kt; ++kt) {
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1, a, abrt, 1)) break;
-                    const int kleft = a.ktot - kt * kBK;
-                    const int n_atoms = kleft >= kBK ? kAtoms : (kleft + 63) / 64;
+                    const int kleft = a.ktot - kt * F::kElemsPerStage;
+                    const int n_mma = kleft >= F::kElemsPerStage ? kMmaPerStage : (kleft + F::kMmaK - 1) / F::kMmaK;
+                    const int n_atoms = GF::atoms_for(n_mma);
                     uint8_t* sA = smem + stage * kStageBytes;
                     uint8_t* sB = sA + kABytes;
                     uint8_t* sSFA = sB + kBBytes;
@@ -482,15 +538,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     mbar_expect_tx(&full_bar[stage], kABytes + kBBytes + 3u * 512u * n_atoms);
                     // own A tile and scales; this CTA's halves of the weight tile and their scales
                     // into every CTA of the cluster (the peer sends the other half)
-                    tma_load_2d(sA, &tmap_a, kt * (kBK / 2), T.lrow0, &full_bar[stage]);
-                    const uint8_t* srcA = a.a_sf + ((int64_t)(T.lrow0 >> 7) * (a.a_sf_cols >> 2) + kt * kAtoms) * 512;
+                    tma_load_2d(sA, &tmap_a, kt * kRowBytes, T.lrow0, &full_bar[stage]);
+                    const uint8_t* srcA = a.a_sf + ((int64_t)(T.lrow0 >> 7) * (a.a_sf_cols >> 2) + kt * kSfAtoms) * 512;
                     bulk_load(sSFA, srcA, 512u * n_atoms, &full_bar[stage]);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         if (h % kCluster != (int)rank) continue;
                         const int64_t brow = h ? brow1 : brow0;
-                        tma_load_2d_mc(sB + h * (kBBytes / 2), &tmap_b, kt * (kBK / 2), (int)brow, &full_bar[stage], pol_keep);
-                        const uint8_t* srcB = a.b_sf + ((brow >> 7) * (a.b_sf_cols >> 2) + kt * kAtoms) * 512;
+                        tma_load_2d_mc(sB + h * (kBBytes / 2), &tmap_b, kt * kRowBytes, (int)brow, &full_bar[stage], pol_keep);
+                        const uint8_t* srcB = a.b_sf + ((brow >> 7) * (a.b_sf_cols >> 2) + kt * kSfAtoms) * 512;
                         bulk_load_mc(sSFB + h * (kSFBBytes / 2), srcB, 512u * n_atoms, &full_bar[stage]);
                     }
                     ++issued;
@@ -509,6 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         // ---------------- MMA issuer: waits for the stage's scale factors to be in TMEM (which
         // implies its operand tiles are in shared memory), then up to 4 MMAs and one commit
         // that frees the stage.  Descriptors are precomputed; nothing else is in this loop.
+        // MMA j reads scale atom atom_of(j) (SFA 4 columns, SFB 8 columns per atom) and, for
+        // FP8, byte j of its scale words.
         const uint32_t base = smem_u32(smem);
         const uint64_t a_desc0 = smem_desc(base, 16, kSBO, kSwizzleLayout);
         const uint64_t b_desc0 = smem_desc(base + kABytes, 16, kSBO, kSwizzleLayout);
@@ -523,17 +581,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             for (int kt = 0; kt < num_kt; ++kt) {
                 if (!mbar_wait(&sf_bar[stage], phase, a, abrt, 3)) { ok = false; break; }
                 tc_fence_after();
-                const int kleft = a.ktot - kt * kBK;
-                const int n_mma = kleft >= kBK ? kAtoms : (kleft + 63) / 64;
+                const int kleft = a.ktot - kt * F::kElemsPerStage;
+                const int n_mma = kleft >= F::kElemsPerStage ? kMmaPerStage : (kleft + F::kMmaK - 1) / F::kMmaK;
                 if (lane == 0) {
                     const uint64_t so = (uint64_t)stage * kStageStep;
                     const uint32_t sfa_t = tmem + kSFCol + stage * kSFColsPerStage;
-                    const uint32_t sfb_t = sfa_t + 4 * kAtoms;
+                    const uint32_t sfb_t = sfa_t + 4 * kSfAtoms;
 #pragma unroll
-                    for (int j = 0; j < kAtoms; ++j)  // K = 64 step j: 32 bytes into the tile rows
+                    for (int j = 0; j < kMmaPerStage; ++j)  // step j: 32 bytes into the tile rows
                         if (j < n_mma)
-                            mma_fp4(tmem + kAccCol, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, sfa_t + 4 * j, sfb_t + 8 * j,
-                                    (kt > 0 || j > 0) ? 1u : 0u);
+                            F::mma(tmem + kAccCol, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, F::idesc(j),
+                                   sfa_t + 4 * GF::atom_of(j), sfb_t + 8 * GF::atom_of(j), (kt > 0 || j > 0) ? 1u : 0u);
                     tc_commit_both(&empty_bar[stage]);  // the stage also holds the peer's weight half
                     issued_any = true;
                 }
@@ -552,9 +610,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         __syncwarp();
     } else if (warp < kFirstEpiWarp) {
         // ---------------- scale staging (warps 2-5, TMEM lane quarter = warp % 4): per K-tile,
-        // lane i loads row i (16 bytes) of each of the stage's 3 * kAtoms scale atoms from shared
-        // memory and stores them to its TMEM lane, SFA atom j at columns 4j, SFB atom j of weight
-        // half h at 4 kAtoms + 8j + 4h; then fence and arrive on sf_bar for the MMA warp.
+        // lane i loads row i (16 bytes) of each of the stage's 3 * kSfAtoms scale atoms from
+        // shared memory and stores them to its TMEM lane, SFA atom j at columns 4j, SFB atom j
+        // of weight half h at 4 kSfAtoms + 8j + 4h; then fence and arrive on sf_bar for the MMA
+        // warp.
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
         int stage = 0;
         uint32_t phase = 0;
@@ -563,9 +622,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             for (int kt = 0; kt < num_kt; ++kt) {
                 if (!mbar_wait(&full_bar[stage], phase, a, abrt, 5)) { ok = false; break; }
                 const uint8_t* sf = smem + stage * kStageBytes + kABytes + kBBytes + lane * 16;
-                uint32_t va[4 * kAtoms], vb[8 * kAtoms];
+                uint32_t va[4 * kSfAtoms], vb[8 * kSfAtoms];
 #pragma unroll
-                for (int j = 0; j < kAtoms; ++j) {
+                for (int j = 0; j < kSfAtoms; ++j) {
                     const uint4 x = *reinterpret_cast<const uint4*>(sf + j * 512);
                     va[4 * j] = x.x; va[4 * j + 1] = x.y; va[4 * j + 2] = x.z; va[4 * j + 3] = x.w;
 #pragma unroll
@@ -575,12 +634,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     }
                 }
                 const uint32_t sfa_t = tmem + kSFCol + stage * kSFColsPerStage + lane_addr;
-                if constexpr (kAtoms == 4) {
+                if constexpr (kSfAtoms == 4) {
                     tmem_st16(sfa_t, va);
                     tmem_st32(sfa_t + 16, vb);
-                } else {
+                } else if constexpr (kSfAtoms == 2) {
                     tmem_st8(sfa_t, va);
                     tmem_st16(sfa_t + 8, vb);
+                } else {
+                    static_assert(kSfAtoms == 1, "scale atoms per stage");
+                    tmem_st4(sfa_t, va);
+                    tmem_st8(sfa_t + 4, vb);
                 }
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
@@ -605,7 +668,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const Tile T = tile_of(t, n_tiles, tab, G, (int)rank);
             const bool valid = r_in_tile < T.rows;
             const int64_t grow = (int64_t)T.row0 + r_in_tile;
-            const float alpha = __fmul_rn(a.a_ts[a.a_ts_per_group ? T.g : 0].s_dec, a.b_ts[T.g].s_dec);
+            // NVFP4: alpha_g = S_dec(A) S_dec(W); FP8 (no tensor scales): 1
+            const float alpha = a.a_ts ? __fmul_rn(a.a_ts[a.a_ts_per_group ? T.g : 0].s_dec, a.b_ts[T.g].s_dec) : 1.0f;
             const float w = (a.epilogue == NVQ_EPI_ROW_SCALE && valid) ? a.row_w[grow] : 1.0f;
             if (!mbar_wait(&acc_full, acc_phase, a, abrt, 4)) break;
             tc_fence_after();
@@ -717,6 +781,86 @@ static nvq_status make_map(CUtensorMap* m, const void* base, int64_t inner_bytes
 nvq_status weight_tail_impl(uint8_t* codes, int64_t ld_codes, uint8_t* sf, int64_t sf_cols, int64_t N, int K, int k,
                             int G, const nvq_tensor_scale* ts, const int32_t* idx, int idx_per_group, cudaStream_t st);
 
+// Persistent launch in clusters of two: one cluster per SM pair that can hold one (occupancy
+// query), no more than the tile pairs of the work.
+template <class F>
+nvq_status launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& ga, int32_t groups, int64_t N,
+                       cudaStream_t st)
+{
+    constexpr int kSmem = Geo<F>::kSmemBytes;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(gemm_kernel)");
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3((unsigned)sms);
+    int max_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, gemm_kernel<F>, &cfg) != cudaSuccess || max_clusters < 1)
+        max_clusters = sms / kCluster;
+    const int64_t max_pairs = (int64_t)(ga.total_mtiles_max / kCluster + 1 + groups) * (N / kBN);
+    const int clusters = (int)(max_pairs < max_clusters ? max_pairs : max_clusters);
+    cfg.gridDim = dim3((unsigned)(clusters * kCluster));
+    e = cudaLaunchKernelEx(&cfg, gemm_kernel<F>, ma, mb, ga);
+    if (e != cudaSuccess) return cuda_status(e, "cudaLaunchKernelEx(gemm_kernel)");
+    NVQ_LAUNCH_CHECK("gemm_kernel");
+    return NVQ_OK;
+}
+
+// Arguments shared by both entries.
+static nvq_status check_gemm_common(const char* fn, int32_t groups, const int64_t* grp_off, int64_t rows, int64_t N,
+                                    int32_t epilogue, const float* row_w, int64_t ldo, const void* out)
+{
+    NVQ_CHECK_ARG(epilogue == NVQ_EPI_STORE || epilogue == NVQ_EPI_SWIGLU || epilogue == NVQ_EPI_ROW_SCALE ||
+                      epilogue == NVQ_EPI_STORE_F32, NVQ_ERR_ARG, "%s: unknown epilogue %d", fn, epilogue);
+    NVQ_CHECK_ARG(epilogue != NVQ_EPI_ROW_SCALE || row_w, NVQ_ERR_ARG, "%s: row_w required", fn);
+    NVQ_CHECK_ARG(groups >= 1 && groups <= kMaxGroups, NVQ_ERR_SHAPE, "%s: groups outside [1, %d]", fn, kMaxGroups);
+    NVQ_CHECK_ARG(grp_off || groups == 1, NVQ_ERR_SHAPE, "%s: grp_off required when groups > 1", fn);
+    NVQ_CHECK_ARG(rows >= 1 && rows <= (1ll << 24), NVQ_ERR_SHAPE, "%s: rows outside [1, 2^24]", fn);
+    NVQ_CHECK_ARG(N >= kBN && N % kBN == 0 && (int64_t)groups * N <= (1ll << 24), NVQ_ERR_SHAPE,
+                  "%s: N=%lld must be a positive multiple of %d", fn, (long long)N, kBN);
+    NVQ_CHECK_ARG(ldo % 8 == 0 && ldo >= (epilogue == NVQ_EPI_SWIGLU ? N / 2 : N), NVQ_ERR_ALIGN,
+                  "%s: ldo must be a multiple of 8 covering the output width", fn);
+    NVQ_CHECK_ARG(aligned(out, 16), NVQ_ERR_ALIGN, "%s: out must be 16-byte aligned", fn);
+    return NVQ_OK;
+}
+
+static GemmArgs gemm_args(int32_t groups, const int64_t* grp_off, const int64_t* grp_rows, int64_t rows,
+                          const uint8_t* a_sf, int64_t a_sf_cols, const uint8_t* b_sf, int64_t b_sf_cols, int64_t N,
+                          int64_t ktot, int32_t epilogue, const float* row_w, void* out, int64_t ldo)
+{
+    GemmArgs ga;
+    ga.gr = Groups{grp_off, grp_rows, groups, rows};
+    ga.total_mtiles_max = (int)((rows + kBM - 1) / kBM);
+    ga.a_sf = a_sf;
+    ga.a_sf_cols = a_sf_cols;
+    ga.b_sf = b_sf;
+    ga.b_sf_cols = b_sf_cols;
+    ga.a_ts = nullptr;
+    ga.a_ts_per_group = 0;
+    ga.b_ts = nullptr;
+    ga.N = N;
+    ga.ktot = (int32_t)ktot;
+    ga.epilogue = epilogue;
+    ga.row_w = row_w;
+    ga.out = static_cast<__nv_bfloat16*>(out);  // fp32 rows for NVQ_EPI_STORE_F32
+    ga.ldo = ldo;
+    ga.status = device_status_ptr();
+    ga.wait_limit = wait_limit();
+    ga.out_ts = nullptr;
+    return ga;
+}
+
 }  // namespace nvq
 
 using namespace nvq;
@@ -730,32 +874,23 @@ extern "C" nvq_status w4a4_rac_grouped_gemm(int32_t groups, const int64_t* grp_o
                                             const float* row_w, void* out, int64_t ldo, nvq_tensor_scale* out_tscale,
                                             void* stream)
 {
-    NVQ_CHECK_ARG(a_codes && a_sf && a_tscale && b_codes && b_sf && b_tscale && out, NVQ_ERR_ARG,
-                  "w4a4_rac_grouped_gemm: null pointer argument");
-    NVQ_CHECK_ARG(epilogue == NVQ_EPI_STORE || epilogue == NVQ_EPI_SWIGLU || epilogue == NVQ_EPI_ROW_SCALE ||
-                      epilogue == NVQ_EPI_STORE_F32, NVQ_ERR_ARG,
-                  "w4a4_rac_grouped_gemm: unknown epilogue %d", epilogue);
-    NVQ_CHECK_ARG(epilogue != NVQ_EPI_ROW_SCALE || row_w, NVQ_ERR_ARG, "w4a4_rac_grouped_gemm: row_w required");
-    NVQ_CHECK_ARG(groups >= 1 && groups <= kMaxGroups, NVQ_ERR_SHAPE, "w4a4_rac_grouped_gemm: groups outside [1, %d]", kMaxGroups);
-    NVQ_CHECK_ARG(grp_off || groups == 1, NVQ_ERR_SHAPE, "w4a4_rac_grouped_gemm: grp_off required when groups > 1");
-    NVQ_CHECK_ARG(rows >= 1 && rows <= (1ll << 24), NVQ_ERR_SHAPE, "w4a4_rac_grouped_gemm: rows outside [1, 2^24]");
-    NVQ_CHECK_ARG(N >= kBN && N % kBN == 0 && (int64_t)groups * N <= (1ll << 24), NVQ_ERR_SHAPE,
-                  "w4a4_rac_grouped_gemm: N=%lld must be a positive multiple of %d", (long long)N, kBN);
-    NVQ_CHECK_ARG(K >= 16 && K <= 8192 && K % 16 == 0, NVQ_ERR_SHAPE, "w4a4_rac_grouped_gemm: K must be a multiple of 16 in [16, 8192]");
-    NVQ_CHECK_ARG(k >= 0 && k <= K && k % 16 == 0, NVQ_ERR_SHAPE, "w4a4_rac_grouped_gemm: k=%d must be a multiple of 16 in [0, K]", k);
+    static const char* fn = "w4a4_rac_grouped_gemm";
+    NVQ_CHECK_ARG(a_codes && a_sf && a_tscale && b_codes && b_sf && b_tscale && out, NVQ_ERR_ARG, "%s: null pointer argument", fn);
+    nvq_status s = check_gemm_common(fn, groups, grp_off, rows, N, epilogue, row_w, ldo, out);
+    if (s != NVQ_OK) return s;
+    NVQ_CHECK_ARG(K >= 16 && K <= 8192 && K % 16 == 0, NVQ_ERR_SHAPE, "%s: K must be a multiple of 16 in [16, 8192]", fn);
+    NVQ_CHECK_ARG(k >= 0 && k <= K && k % 16 == 0, NVQ_ERR_SHAPE, "%s: k=%d must be a multiple of 16 in [0, K]", fn, k);
     const int64_t ktot = K + k;
     NVQ_CHECK_ARG(lda % 16 == 0 && ldb % 16 == 0 && lda >= ktot / 2 && ldb >= ktot / 2, NVQ_ERR_ALIGN,
-                  "w4a4_rac_grouped_gemm: lda/ldb must be multiples of 16 covering (K+k)/2 bytes");
+                  "%s: lda/ldb must be multiples of 16 covering (K+k)/2 bytes", fn);
     NVQ_CHECK_ARG(a_sf_cols % 4 == 0 && b_sf_cols % 4 == 0 && a_sf_cols >= nvq_sf_cols(ktot) && b_sf_cols >= nvq_sf_cols(ktot),
-                  NVQ_ERR_SHAPE, "w4a4_rac_grouped_gemm: sf_cols must be >= nvq_sf_cols(K+k)");
-    NVQ_CHECK_ARG(ldo % 8 == 0 && ldo >= (epilogue == NVQ_EPI_SWIGLU ? N / 2 : N), NVQ_ERR_ALIGN,
-                  "w4a4_rac_grouped_gemm: ldo must be a multiple of 8 covering the output width");
-    NVQ_CHECK_ARG(aligned(a_codes, 16) && aligned(b_codes, 16) && aligned(a_sf, 16) && aligned(b_sf, 16) && aligned(out, 16),
-                  NVQ_ERR_ALIGN, "w4a4_rac_grouped_gemm: operands must be 16-byte aligned");
+                  NVQ_ERR_SHAPE, "%s: sf_cols must be >= nvq_sf_cols(K+k)", fn);
+    NVQ_CHECK_ARG(aligned(a_codes, 16) && aligned(b_codes, 16) && aligned(a_sf, 16) && aligned(b_sf, 16), NVQ_ERR_ALIGN,
+                  "%s: operands must be 16-byte aligned", fn);
+    NVQ_CHECK_ARG(!out_tscale || epilogue != NVQ_EPI_STORE_F32, NVQ_ERR_ARG, "%s: out_tscale needs a bf16 epilogue", fn);
     set_error("");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-    nvq_status s = NVQ_OK;
     if (idx && k > 0) {
         s = weight_tail_impl(b_codes, ldb, b_sf, b_sf_cols, N, (int)K, k, groups, b_tscale, idx, idx_per_group, st);
         if (s != NVQ_OK) return s;
@@ -767,59 +902,46 @@ extern "C" nvq_status w4a4_rac_grouped_gemm(int32_t groups, const int64_t* grp_o
     s = make_map(&mb, b_codes, ktot / 2, (int64_t)groups * N, ldb);
     if (s != NVQ_OK) return s;
 
-    GemmArgs ga;
-    ga.gr = Groups{grp_off, grp_rows, groups, rows};
-    ga.total_mtiles_max = (int)((rows + kBM - 1) / kBM);
-    ga.a_sf = a_sf;
-    ga.a_sf_cols = a_sf_cols;
-    ga.b_sf = b_sf;
-    ga.b_sf_cols = b_sf_cols;
+    GemmArgs ga = gemm_args(groups, grp_off, grp_rows, rows, a_sf, a_sf_cols, b_sf, b_sf_cols, N, ktot, epilogue, row_w,
+                            out, ldo);
     ga.a_ts = a_tscale;
     ga.a_ts_per_group = a_scale_per_group;
     ga.b_ts = b_tscale;
-    ga.N = N;
-    ga.ktot = (int32_t)ktot;
-    ga.epilogue = epilogue;
-    ga.row_w = row_w;
-    ga.out = static_cast<__nv_bfloat16*>(out);  // fp32 rows for NVQ_EPI_STORE_F32
-    ga.ldo = ldo;
-    ga.status = device_status_ptr();
-    ga.wait_limit = wait_limit();
     ga.out_ts = out_tscale;
-    NVQ_CHECK_ARG(ga.status, NVQ_ERR_CUDA, "w4a4_rac_grouped_gemm: device status word unavailable");
-    NVQ_CHECK_ARG(!out_tscale || epilogue != NVQ_EPI_STORE_F32, NVQ_ERR_ARG,
-                  "w4a4_rac_grouped_gemm: out_tscale needs a bf16 epilogue");
+    NVQ_CHECK_ARG(ga.status, NVQ_ERR_CUDA, "%s: device status word unavailable", fn);
     if (out_tscale) {
         const cudaError_t me = cudaMemsetAsync(out_tscale, 0, sizeof(nvq_tensor_scale) * groups, st);
         if (me != cudaSuccess) return cuda_status(me, "cudaMemsetAsync(out_tscale)");
     }
+    return launch_gemm<Fp4>(ma, mb, ga, groups, N, st);
+}
 
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(gemm_kernel)");
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // one cluster per SM pair that can hold one at a time (persistent), no more than the work
-    cfg.gridDim = dim3((unsigned)sms);
-    int max_clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, gemm_kernel, &cfg) != cudaSuccess || max_clusters < 1)
-        max_clusters = sms / kCluster;
-    const int64_t max_pairs = (int64_t)(ga.total_mtiles_max / kCluster + 1 + groups) * (N / kBN);
-    const int clusters = (int)(max_pairs < max_clusters ? max_pairs : max_clusters);
-    cfg.gridDim = dim3((unsigned)(clusters * kCluster));
-    e = cudaLaunchKernelEx(&cfg, gemm_kernel, ma, mb, ga);
-    if (e != cudaSuccess) return cuda_status(e, "cudaLaunchKernelEx(gemm_kernel)");
-    NVQ_LAUNCH_CHECK("gemm_kernel");
-    return NVQ_OK;
+extern "C" nvq_status fp8_blockscaled_grouped_gemm(int32_t groups, const int64_t* grp_off, const int64_t* grp_rows,
+                                                   int64_t rows, const uint8_t* a_codes, int64_t lda, const uint8_t* a_sf,
+                                                   int64_t a_sf_cols, const uint8_t* b_codes, int64_t ldb,
+                                                   const uint8_t* b_sf, int64_t b_sf_cols, int64_t N, int64_t K,
+                                                   int32_t epilogue, const float* row_w, void* out, int64_t ldo,
+                                                   void* stream)
+{
+    static const char* fn = "fp8_blockscaled_grouped_gemm";
+    NVQ_CHECK_ARG(a_codes && a_sf && b_codes && b_sf && out, NVQ_ERR_ARG, "%s: null pointer argument", fn);
+    nvq_status s = check_gemm_common(fn, groups, grp_off, rows, N, epilogue, row_w, ldo, out);
+    if (s != NVQ_OK) return s;
+    NVQ_CHECK_ARG(K >= 32 && K <= 16384 && K % 32 == 0, NVQ_ERR_SHAPE, "%s: K must be a multiple of 32 in [32, 16384]", fn);
+    NVQ_CHECK_ARG(lda % 16 == 0 && ldb % 16 == 0 && lda >= K && ldb >= K, NVQ_ERR_ALIGN,
+                  "%s: lda/ldb must be multiples of 16 covering K bytes", fn);
+    NVQ_CHECK_ARG(a_sf_cols % 4 == 0 && b_sf_cols % 4 == 0 && a_sf_cols >= nvq_fp8_sf_cols(K) && b_sf_cols >= nvq_fp8_sf_cols(K),
+                  NVQ_ERR_SHAPE, "%s: sf_cols must be >= nvq_fp8_sf_cols(K)", fn);
+    NVQ_CHECK_ARG(aligned(a_codes, 16) && aligned(b_codes, 16) && aligned(a_sf, 16) && aligned(b_sf, 16), NVQ_ERR_ALIGN,
+                  "%s: operands must be 16-byte aligned", fn);
+    set_error("");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    CUtensorMap ma, mb;
+    s = make_map(&ma, a_codes, K, rows, lda);
+    if (s != NVQ_OK) return s;
+    s = make_map(&mb, b_codes, K, (int64_t)groups * N, ldb);
+    if (s != NVQ_OK) return s;
+    GemmArgs ga = gemm_args(groups, grp_off, grp_rows, rows, a_sf, a_sf_cols, b_sf, b_sf_cols, N, K, epilogue, row_w, out, ldo);
+    NVQ_CHECK_ARG(ga.status, NVQ_ERR_CUDA, "%s: device status word unavailable", fn);
+    return launch_gemm<Fp8>(ma, mb, ga, groups, N, st);
 }

@@ -169,13 +169,17 @@ __global__ void dispatch_scatter_kernel(const int32_t* __restrict__ ids, const f
     }
 }
 
-// CTA per 128-row block of the routed layout.  Codes: warp per row, 16-byte vectors.  Scales:
-// the block's output words are written in the blocked layout's own order (coalesced); each
-// reads its word from the source row's scales (token scales: small and L2 resident).
+// CTA per 128-row block of the routed layout.  Codes: bytes [byte0, byte_end) of every row,
+// 16-byte vectors (an 8-byte piece at the end when byte_end % 16 == 8).  Scales: the 512-byte
+// atoms [atom0, atom_end) of the row block (4 scale columns each), the block's output words
+// written in the blocked layout's own order (coalesced); each reads its word from the source
+// row's scales (token scales: small and L2 resident).  NVFP4 rows of ktot elements hold ktot / 2
+// code bytes and ktot / 64 atoms; FP8 rows of K elements hold K bytes and K / 128 atoms.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restrict__ codes, int64_t ld_codes,
                                                           const uint8_t* __restrict__ sf, int64_t sf_cols,
-                                                          const int32_t* __restrict__ row_src, int topk, int64_t ktot,
-                                                          int64_t col0, uint8_t* __restrict__ out_codes, int64_t ld_out,
+                                                          const int32_t* __restrict__ row_src, int topk, int64_t byte0,
+                                                          int64_t byte_end, int atom0, int atom_end,
+                                                          uint8_t* __restrict__ out_codes, int64_t ld_out,
                                                           uint8_t* __restrict__ out_sf)
 {
     __shared__ int src[128];
@@ -188,10 +192,10 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
     __syncthreads();
     if (out_codes != nullptr) {
         // four rows per warp at a time: all their loads are in flight before the stores
-        const int nvec = (int)(ktot / 32);  // 16-byte vectors of codes
-        const bool tail8 = (ktot % 32) != 0;
+        const int nvec = (int)(byte_end / 16);  // 16-byte vectors of codes
+        const bool tail8 = (byte_end % 16) != 0;
         for (int r4 = warp * 4; r4 < 128; r4 += 32) {
-            for (int v0 = (int)(col0 / 32); v0 < nvec; v0 += 32) {
+            for (int v0 = (int)(byte0 / 16); v0 < nvec; v0 += 32) {
                 const int v = v0 + lane;
                 uint4 val[4];
 #pragma unroll
@@ -213,9 +217,9 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
     }
     // scales: four words per thread at a time, loads before stores
     const int natoms = (int)(sf_cols / 4);
-    const int nwords = (int)((ktot + 63) / 64) * 128;  // atoms covering columns [col0, ktot)
+    const int nwords = atom_end * 128;
     uint32_t* outw = reinterpret_cast<uint32_t*>(out_sf + blockIdx.x * (int64_t)natoms * 512);
-    for (int w0 = (int)(col0 / 64) * 128 + tid; w0 < nwords; w0 += 4 * 256) {
+    for (int w0 = atom0 * 128 + tid; w0 < nwords; w0 += 4 * 256) {
         uint32_t val[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -326,8 +330,29 @@ extern "C" nvq_status nvfp4_gather_rows(const uint8_t* codes, int64_t ld_codes, 
                   NVQ_ERR_ALIGN, "nvfp4_gather_rows: codes need 16-byte aligned rows");
     set_error("");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    gather_rows_kernel<<<(unsigned)(capacity / 128), 256, 0, st>>>(codes, ld_codes, sf, sf_cols, row_src, topk, ktot,
-                                                                   col0, out_codes, ld_out, out_sf);
+    gather_rows_kernel<<<(unsigned)(capacity / 128), 256, 0, st>>>(codes, ld_codes, sf, sf_cols, row_src, topk, col0 / 2,
+                                                                   ktot / 2, (int)(col0 / 64), (int)((ktot + 63) / 64),
+                                                                   out_codes, ld_out, out_sf);
+    NVQ_LAUNCH_CHECK("gather_rows_kernel");
+    return NVQ_OK;
+}
+
+extern "C" nvq_status fp8_gather_rows(const uint8_t* codes, int64_t ld_codes, const uint8_t* sf, int64_t sf_cols,
+                                      int64_t src_rows, const int32_t* row_src, int32_t topk, int64_t capacity, int64_t K,
+                                      uint8_t* out_codes, int64_t ld_out, uint8_t* out_sf, void* stream)
+{
+    NVQ_CHECK_ARG(codes && sf && row_src && out_codes && out_sf, NVQ_ERR_ARG, "fp8_gather_rows: null pointer argument");
+    NVQ_CHECK_ARG(K >= 32 && K % 32 == 0 && sf_cols >= nvq_fp8_sf_cols(K) && sf_cols % 4 == 0, NVQ_ERR_SHAPE,
+                  "fp8_gather_rows: K must be a positive multiple of 32 and sf_cols >= nvq_fp8_sf_cols(K)");
+    NVQ_CHECK_ARG(capacity >= 1 && capacity % 128 == 0 && src_rows >= 1 && topk >= 1, NVQ_ERR_SHAPE,
+                  "fp8_gather_rows: capacity must be a positive multiple of 128");
+    NVQ_CHECK_ARG(ld_codes % 16 == 0 && ld_codes >= K && aligned(codes, 16) && aligned(sf, 4) && aligned(out_sf, 4) &&
+                      ld_out % 16 == 0 && ld_out >= K && aligned(out_codes, 16),
+                  NVQ_ERR_ALIGN, "fp8_gather_rows: codes need 16-byte aligned rows");
+    set_error("");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    gather_rows_kernel<<<(unsigned)(capacity / 128), 256, 0, st>>>(codes, ld_codes, sf, sf_cols, row_src, topk, 0, K, 0,
+                                                                   (int)((K + 127) / 128), out_codes, ld_out, out_sf);
     NVQ_LAUNCH_CHECK("gather_rows_kernel");
     return NVQ_OK;
 }
