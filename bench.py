@@ -357,6 +357,117 @@ def _time_replays(fn, flush, steps, warmup):
     return time_graph_replays(fn, flush, steps, warmup)
 
 
+def baseline_rows(args, layer, x, ids_d, tw_d, w13_bits, w2_bits, cfg, dev, flush, ms_rac, t_gu, t_dn):
+    """The comparison rows of the measurement plan: the same layer with k = 0 (W4A4 without RAC;
+    RAC cost = (t_RAC - t_noRAC) / t_noRAC), and the two expert GEMMs with SwiGLU in bf16 through
+    cuBLAS (a per-expert loop over this batch's routed rows, captured in a CUDA graph)."""
+    import torch
+    from nvfp4_w4a4_quantized_quantize_gb300.layers import MoERacLayer
+    E, H, I, T, topk = cfg.E, cfg.H, cfg.I, cfg.T, cfg.topk
+    steps = max(5, min(args.steps, 20))
+    w13 = _bf16(w13_bits.reshape(E * 2 * I, H), dev).view(E, 2 * I, H)
+    w2 = _bf16(w2_bits.reshape(E * H, I), dev).view(E, H, I)
+    layer0 = MoERacLayer(w13, w2, 0, topk, T)
+    out0 = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    ms0 = _time_replays(lambda: layer0.forward(x, ids_d, tw_d, out0), flush, steps, 3)
+    del layer0, out0
+    # bf16 expert GEMMs on the routed rows of this batch (the rows gathered outside the timing)
+    off = layer.grp_off.cpu().tolist()
+    cnt = layer.grp_rows.cpu().tolist()
+    src = layer.row_src.long()
+    xs, ys = [], []
+    for e in range(E):
+        r = src[off[e]:off[e] + cnt[e]]
+        xs.append(x[r // topk].contiguous() if cnt[e] else None)
+        ys.append(torch.empty(cnt[e], H, dtype=torch.bfloat16, device=dev) if cnt[e] else None)
+
+    def bf16_gemms():
+        for e in range(E):
+            if xs[e] is not None:
+                g = xs[e] @ w13[e].t()
+                h = torch.nn.functional.silu(g[:, :I]) * g[:, I:]
+                torch.matmul(h, w2[e].t(), out=ys[e])
+
+    ms_bf = _time_replays(bf16_gemms, flush, steps, 3)
+    rows = T * topk
+    flop_k0 = 2.0 * rows * (2 * I) * H + 2.0 * rows * H * I
+    del w13, w2, xs, ys
+    torch.cuda.empty_cache()
+    return {
+        "w4a4_no_rac_layer": {"ms_per_step": round(ms0, 4), "tokens_per_s": round(T / (ms0 * 1e-3), 1),
+                              "rac_cost": round((ms_rac - ms0) / ms0, 4)},
+        "bf16_expert_gemms": {"ms": round(ms_bf, 4), "tflops": round(flop_k0 / (ms_bf * 1e-3) / 1e12, 1),
+                              "impl": "cuBLAS per-expert loop (gate/up, SwiGLU, down) in a CUDA graph"},
+        "w4a4_rac_expert_gemms": {"ms": round(t_gu + t_dn, 4),
+                                  "useful_tflops": round(flop_k0 / ((t_gu + t_dn) * 1e-3) / 1e12, 1),
+                                  "speedup_vs_bf16": round(ms_bf / (t_gu + t_dn), 3)},
+    }
+
+
+def trainer_rows(args, L, dev, flush, peaks):
+    """Trainer-side rows: weight_qdq (QDQ_W of Eq. (12)) over all expert weights of the decode
+    workload shape (W13 [128, 3072, 4096] + W2 [128, 4096, 1536], 2.42 G elements, with the bf16
+    W-hat), against the HBM roofline; and a W4A16 QAT linear layer (forward + backward at
+    M = 4096, K = 4096, N = 14336) against the same layer in plain bf16."""
+    import torch
+    from nvfp4_w4a4_quantized_quantize_gb300.layers import Operand
+    from nvfp4_w4a4_quantized_quantize_gb300.qat import QATLinear
+    gen = torch.Generator(device=dev).manual_seed(5)
+    res = {}
+    total_ms, elems = 0.0, 0
+    for (G, N, K) in ((128, 3072, 4096), (128, 4096, 1536)):
+        w = (torch.randn(G, N, K, device=dev, generator=gen) * 0.02).bfloat16()
+        op = Operand.empty(G * N, K, 0, G, device=dev)
+        w_hat = torch.empty(G, N, K, dtype=torch.bfloat16, device=dev)
+
+        def qdq():
+            L.weight_qdq(w, G, N, K, op.codes, op.sf, op.sf_cols, op.tscale, w_hat=w_hat, w_hat_dtype=L.NVQ_BF16)
+        total_ms += _time_replays(qdq, flush, 5, 2)
+        elems += G * N * K
+        del w, op, w_hat
+        torch.cuda.empty_cache()
+    alg = elems * (2 + 0.5625 + 2)
+    res["weight_qdq"] = {"workload": "W13 [128,3072,4096] + W2 [128,4096,1536], bf16 W-hat", "elements": elems,
+                         "ms": round(total_ms, 4), "algorithmic_bytes": int(alg),
+                         "gbs": round(alg / (total_ms * 1e-3) / 1e9, 1),
+                         "frac_of_measured_hbm": round(alg / (total_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+    torch.manual_seed(6)
+    M, K, N = 4096, 4096, 14336
+    x = torch.randn(M, K, device=dev).bfloat16().requires_grad_(True)
+    lin = QATLinear(K, N, device=dev)
+    gy = torch.randn(M, N, device=dev).bfloat16()
+    w_plain = lin.weight.detach().clone().requires_grad_(True)
+
+    def step_qat():
+        y = lin(x)
+        y.backward(gy)
+
+    def step_bf16():
+        y = x @ w_plain.t()
+        y.backward(gy)
+
+    ts = {}
+    for name, fn in (("qat", step_qat), ("bf16", step_bf16)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(10):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        ts[name] = statistics.median(times)
+    res["qat_linear_4096x4096x14336"] = {"ms_fwd_bwd": round(ts["qat"], 4), "bf16_ms_fwd_bwd": round(ts["bf16"], 4),
+                                         "qdq_overhead": round((ts["qat"] - ts["bf16"]) / ts["bf16"], 4)}
+    del x, lin, gy, w_plain
+    torch.cuda.empty_cache()
+    return res
+
+
 def act_quant_bench(args, L, wl, dev, flush, peaks):
     import torch
     cfg = wl.CFG_ACT
