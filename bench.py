@@ -391,7 +391,27 @@ def baseline_rows(args, layer, x, ids_d, tw_d, w13_bits, w2_bits, cfg, dev, flus
     ms_bf = _time_replays(bf16_gemms, flush, steps, 3)
     rows = T * topk
     flop_k0 = 2.0 * rows * (2 * I) * H + 2.0 * rows * H * I
-    del w13, w2, xs, ys
+    del xs, ys
+    # FP8 W8A8 block-scaled baseline (E4M3, power-of-two scale per 1 x 128 / 128 x 128 tile): the
+    # whole layer, and each of its two grouped GEMMs alone
+    from nvfp4_w4a4_quantized_quantize_gb300 import _lib as L
+    from nvfp4_w4a4_quantized_quantize_gb300.layers import Fp8MoELayer
+    f8 = Fp8MoELayer(w13, w2, topk, T)
+    del w13, w2
+    out8 = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    ms8 = _time_replays(lambda: f8.forward(x, ids_d, tw_d, out8), flush, steps, 3)
+    f8.forward(x, ids_d, tw_d, out8)
+    t8_gu = _time_replays(lambda: L.fp8_blockscaled_grouped_gemm(
+        f8.a_routed.codes, f8.a_routed.sf, f8.a_routed.sf_cols, f8.w13.codes, f8.w13.sf, f8.w13.sf_cols, 2 * I, H, f8.h,
+        groups=E, grp_off=f8.grp_off, grp_rows=f8.grp_rows, rows=f8.cap, epilogue=L.NVQ_EPI_SWIGLU), flush, steps, 3)
+    t8_dn = _time_replays(lambda: L.fp8_blockscaled_grouped_gemm(
+        f8.a2.codes, f8.a2.sf, f8.a2.sf_cols, f8.w2.codes, f8.w2.sf, f8.w2.sf_cols, H, I, f8.y, groups=E,
+        grp_off=f8.grp_off, grp_rows=f8.grp_rows, rows=f8.cap, epilogue=L.NVQ_EPI_ROW_SCALE, row_w=f8.row_w),
+        flush, steps, 3)
+    peaks, src = _peaks()
+    fp8_peak = peaks["bf16_tflops"] * 2.0
+    flop_gu8 = 2.0 * rows * (2 * I) * H
+    del f8, out8
     torch.cuda.empty_cache()
     return {
         "w4a4_no_rac_layer": {"ms_per_step": round(ms0, 4), "tokens_per_s": round(T / (ms0 * 1e-3), 1),
@@ -401,6 +421,14 @@ def baseline_rows(args, layer, x, ids_d, tw_d, w13_bits, w2_bits, cfg, dev, flus
         "w4a4_rac_expert_gemms": {"ms": round(t_gu + t_dn, 4),
                                   "useful_tflops": round(flop_k0 / ((t_gu + t_dn) * 1e-3) / 1e12, 1),
                                   "speedup_vs_bf16": round(ms_bf / (t_gu + t_dn), 3)},
+        "fp8_w8a8_layer": {"ms_per_step": round(ms8, 4), "tokens_per_s": round(T / (ms8 * 1e-3), 1),
+                           "w4a4_over_fp8": round(ms8 / ms0, 3), "w4a4_rac_over_fp8": round(ms8 / ms_rac, 3),
+                           "gemm_gate_up_ms": round(t8_gu, 4), "gemm_down_ms": round(t8_dn, 4),
+                           "gate_up_tflops": round(flop_gu8 / (t8_gu * 1e-3) / 1e12, 1),
+                           "gate_up_frac_of_fp8_peak": round(flop_gu8 / (t8_gu * 1e-3) / 1e12 / fp8_peak, 4),
+                           "fp8_peak_tflops": round(fp8_peak, 1),
+                           "peak_source": f"{src} bf16 burst x nominal FP8/BF16 ratio 2",
+                           "impl": "Fp8MoELayer: E4M3, power-of-two scale per 1x128 / 128x128 tile, tcgen05 kind::mxf8f6f4"},
     }
 
 

@@ -233,3 +233,74 @@ class MoERacLayer:
         mark("gemm_down", 1)
         L.moe_combine(self.y, self.row_of, T, self.topk, H, out, stream=st)
         return out
+
+
+@dataclass
+class Fp8Operand:
+    """An FP8 GEMM operand: E4M3 codes [rows, ld] and blocked UE8M0 tile scales."""
+    codes: torch.Tensor
+    sf: torch.Tensor
+    sf_cols: int
+
+    @staticmethod
+    def empty(rows: int, K: int, device="cuda") -> "Fp8Operand":
+        cols = L.fp8_sf_cols(K)
+        return Fp8Operand(torch.zeros(rows, _round_up(K, 16), dtype=torch.uint8, device=device),
+                          torch.zeros(L.sf_bytes(rows, cols), dtype=torch.uint8, device=device), cols)
+
+
+class Fp8MoELayer:
+    """The same routed SwiGLU expert layer as MoERacLayer on the FP8 W8A8 baseline the paper
+    compares against (§2.2 "FP8", §4.4.2): E4M3 activations with a power-of-two scale per
+    1 x 128 tile, E4M3 weights with one per 128 x 128 tile, block-scaled tcgen05 GEMMs.
+
+    dispatch; tokens -> FP8 (fp8_quantize); gather into the routed layout; gate/up GEMM with the
+    SwiGLU epilogue -> h; h -> FP8 (every routed row, padding rows included: they hold zeros);
+    down GEMM with the routing-weight epilogue -> y; combine."""
+
+    def __init__(self, w13: torch.Tensor, w2: torch.Tensor, topk: int, max_tokens: int):
+        dev = w13.device
+        self.E, twoI, self.H = w13.shape
+        self.I = twoI // 2
+        self.topk, self.T = topk, max_tokens
+        E, H, I = self.E, self.H, self.I
+        self.w13 = Fp8Operand.empty(E * twoI, H, device=dev)
+        L.fp8_quantize(w13.reshape(E * twoI, H), self.w13.codes, self.w13.sf, self.w13.sf_cols, tile_rows=128)
+        self.w2 = Fp8Operand.empty(E * H, I, device=dev)
+        L.fp8_quantize(w2.reshape(E * H, I), self.w2.codes, self.w2.sf, self.w2.sf_cols, tile_rows=128)
+        cap = L.moe_capacity(max_tokens, topk, E)
+        self.cap = cap
+        self.grp_off = torch.zeros(E + 1, dtype=torch.int64, device=dev)
+        self.grp_rows = torch.zeros(E, dtype=torch.int64, device=dev)
+        self.row_src = torch.zeros(cap, dtype=torch.int32, device=dev)
+        self.row_of = torch.zeros(max_tokens * topk, dtype=torch.int64, device=dev)
+        self.row_w = torch.zeros(cap, dtype=torch.float32, device=dev)
+        self.ws = torch.zeros(L.moe_dispatch_workspace_size(max_tokens, topk, E), dtype=torch.uint8, device=dev)
+        self.a_tok = Fp8Operand.empty(max_tokens, H, device=dev)
+        self.a_routed = Fp8Operand.empty(cap, H, device=dev)
+        self.h = torch.zeros(cap, I, dtype=torch.bfloat16, device=dev)
+        self.a2 = Fp8Operand.empty(cap, I, device=dev)
+        self.y = torch.zeros(cap, H, dtype=torch.bfloat16, device=dev)
+
+    def kernel_launches_per_step(self) -> int:
+        """dispatch 4, token quantize 1, gather 1, gate/up GEMM 1, h quantize 1, down GEMM 1, combine 1."""
+        return 10
+
+    def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, out: torch.Tensor, stream=None):
+        T = x.shape[0]
+        E, H, I = self.E, self.H, self.I
+        L.moe_dispatch(topk_ids, topk_w, E, self.grp_off, self.grp_rows, self.row_src, self.row_of, self.row_w,
+                       self.ws, stream=stream)
+        L.fp8_quantize(x, self.a_tok.codes, self.a_tok.sf, self.a_tok.sf_cols, tile_rows=1, stream=stream)
+        L.fp8_gather_rows(self.a_tok.codes, self.a_tok.sf, self.a_tok.sf_cols, T, self.row_src, self.topk, H,
+                          self.a_routed.codes, self.a_routed.sf, stream=stream)
+        L.fp8_blockscaled_grouped_gemm(self.a_routed.codes, self.a_routed.sf, self.a_routed.sf_cols, self.w13.codes,
+                                       self.w13.sf, self.w13.sf_cols, 2 * I, H, self.h, groups=E, grp_off=self.grp_off,
+                                       grp_rows=self.grp_rows, rows=self.cap, epilogue=L.NVQ_EPI_SWIGLU, stream=stream)
+        L.fp8_quantize(self.h, self.a2.codes, self.a2.sf, self.a2.sf_cols, tile_rows=1, stream=stream)
+        L.fp8_blockscaled_grouped_gemm(self.a2.codes, self.a2.sf, self.a2.sf_cols, self.w2.codes, self.w2.sf,
+                                       self.w2.sf_cols, H, I, self.y, groups=E, grp_off=self.grp_off,
+                                       grp_rows=self.grp_rows, rows=self.cap, epilogue=L.NVQ_EPI_ROW_SCALE,
+                                       row_w=self.row_w, stream=stream)
+        L.moe_combine(self.y, self.row_of, T, self.topk, H, out, stream=stream)
+        return out

@@ -171,3 +171,50 @@ def test_fp8_gather_rows(L):
             assert np.array_equal(got_c[i], src_c[t]) and np.array_equal(got_s[i], src_s[t])
         else:
             assert not got_c[i].any() and not got_s[i].any()
+
+
+def test_fp8_moe_layer_stages(L):
+    """Fp8MoELayer on a small Zipf-routed batch, stage by stage against the oracle: token codes
+    and scales bit for bit, gate/up + SwiGLU and down + routing weight within the GEMM
+    tolerance (each from the GPU's own previous stage), h codes bit for bit, combine exact."""
+    from nvfp4_w4a4_quantized_quantize_gb300.layers import Fp8MoELayer
+    T, H, E, topk, I = 300, 256, 8, 2, 128
+    cfg = wl.MoELayer("t", T=T, H=H, E=E, topk=topk, I=I, k=0, seed=25, routing="zipf", n_outliers=3)
+    x_bits, ids, tw, _ = cfg.make_tokens()
+    w13_bits, w2_bits = cfg.make_weights()
+    w13 = bf16_tensor(w13_bits.reshape(E * 2 * I, H)).view(E, 2 * I, H)
+    w2 = bf16_tensor(w2_bits.reshape(E * H, I)).view(E, H, I)
+    layer = Fp8MoELayer(w13, w2, topk, T)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    layer.forward(bf16_tensor(x_bits), torch.from_numpy(ids).cuda(), torch.from_numpy(tw).cuda(), out)
+    torch.cuda.synchronize()
+    assert L.device_status() == (0, 0)
+    tc, tst = oracle.fp8_quantize(x_bits, 1)
+    assert np.array_equal(layer.a_tok.codes.cpu().numpy()[:, :H], tc)
+    assert np.array_equal(unswizzle(layer.a_tok.sf, T, layer.a_tok.sf_cols, layer.a_tok.sf_cols),
+                          _expected_sf(tst, T, H, 1))
+    grp_off = layer.grp_off.cpu().numpy()
+    grp_rows = layer.grp_rows.cpu().numpy()
+    row_src = layer.row_src.cpu().numpy()
+    row_w = layer.row_w.cpu().numpy().astype(np.float64)
+    h_gpu = bf16_bits(layer.h)
+    y_gpu = bf16_bits(layer.y)
+    worst_h = worst_y = 0.0
+    for g in range(E):
+        c = int(grp_rows[g])
+        if not c:
+            continue
+        rows = np.arange(grp_off[g], grp_off[g] + c)
+        toks = row_src[rows] // topk
+        w13c, w13s = oracle.fp8_quantize(w13_bits[g], 128)
+        ref = oracle.fp8_gemm(tc[toks], tst[toks], w13c, w13s)
+        href = oracle.swiglu(ref[:, :I], ref[:, I:]).reshape(c, I)
+        worst_h = max(worst_h, gemm_error(wl.bf16_bits_to_f32(h_gpu[rows]), href))
+        hc, hst = oracle.fp8_quantize(h_gpu[rows], 1)
+        assert np.array_equal(layer.a2.codes.cpu().numpy()[rows][:, :I], hc)
+        w2c, w2s = oracle.fp8_quantize(w2_bits[g], 128)
+        yref = oracle.fp8_gemm(hc, hst, w2c, w2s) * row_w[rows][:, None]
+        worst_y = max(worst_y, gemm_error(wl.bf16_bits_to_f32(y_gpu[rows]), yref))
+    assert worst_h <= GEMM_RTOL and worst_y <= GEMM_RTOL, (worst_h, worst_y)
+    pos = layer.row_of.cpu().numpy()
+    assert np.array_equal(bf16_bits(out), oracle.moe_combine(y_gpu, pos, topk))
