@@ -334,7 +334,7 @@ def rac_quantize(x: np.ndarray, k: int) -> RacQuant:
 
 # ---------------------------------------------------------------- FP8 W8A8 comparison baseline
 # QUADS §2.2 "FP8" (E4M3, a scale per tile of values) and §4.4.2 (FP8 W8A8 rollout as the
-# production baseline).  Tiles and scale encoding: readings R11-R13 of nvfp4_oracle.c.
+# production baseline).  Tiles and scale encoding: readings R16-R18 of nvfp4_oracle.c.
 def fp8_scale_exponent(amax: float) -> int:
     return int(lib().oracle_fp8_scale_exponent(float(amax)))
 

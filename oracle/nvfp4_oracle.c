@@ -37,15 +37,15 @@
  *      is quantized with blocks of 16 gathered channels and the activation's own S_enc.
  *   R10 Weight tail: the weight columns that multiply the correction are the dequantized
  *      stored weights on the selected channels, re-quantized with the weight's own S_enc.
- *   R11 FP8 W8A8 baseline (§2.2 "FP8": "each tile of values carries its own alpha in
+ *   R16 FP8 W8A8 baseline (§2.2 "FP8": "each tile of values carries its own alpha in
  *      Eq. (4)", tile sizes unstated): activation tiles of 1 x 128 (one row, 128 consecutive
  *      channels), weight tiles of 128 x 128 (128 output rows x 128 input channels); a tile cut
  *      by the matrix edge covers what is left.
- *   R12 FP8 tile scale alpha = 2^e, e the smallest integer with 448 * 2^e >= amax of the tile,
+ *   R17 FP8 tile scale alpha = 2^e, e the smallest integer with 448 * 2^e >= amax of the tile,
  *      clamped to [-127, 127] (an all-zero tile gets -127): a power of two, stored as the byte
  *      e + 127 (UE8M0).
- *   R13 FP8 element: E4M3 of x * 2^-e, nearest value, ties to the even code, sign kept (a
- *      negative value that rounds to zero gives 0x80); |x * 2^-e| <= 448 by R12.  The
+ *   R18 FP8 element: E4M3 of x * 2^-e, nearest value, ties to the even code, sign kept (a
+ *      negative value that rounds to zero gives 0x80); |x * 2^-e| <= 448 by R17.  The
  *      dequantized value V * 2^e is exact.
  *
  * Arithmetic: IEEE binary32 with round-to-nearest-even for every step the method performs in
@@ -125,7 +125,7 @@ double oracle_e4m3_value(uint8_t b)
     return s ? -mag : mag;
 }
 
-/* Nearest finite non-negative E4M3 code to a >= 0, ties to the even code (readings R3, R13). */
+/* Nearest finite non-negative E4M3 code to a >= 0, ties to the even code (readings R3, R18). */
 static uint8_t e4m3_nearest(double a)
 {
     int best = 0;
@@ -479,10 +479,10 @@ void oracle_quantize_block16(const float* v, float s_enc, uint8_t* codes, uint8_
 
 /* ------------------------------------------------------------------------------------------
  * FP8 W8A8 with fine-grained tile scaling, the comparison baseline of QUADS §2.2 "FP8" and
- * §4.4.2 (readings R11-R13).
+ * §4.4.2 (readings R16-R18).
  * ---------------------------------------------------------------------------------------- */
 
-/* Reading R12, by search: the smallest e in [-127, 127] with 448 * 2^e >= amax. */
+/* Reading R17, by search: the smallest e in [-127, 127] with 448 * 2^e >= amax. */
 int32_t oracle_fp8_scale_exponent(double amax)
 {
     if (!(amax > 0.0)) return -127;
@@ -491,7 +491,7 @@ int32_t oracle_fp8_scale_exponent(double amax)
     return e;
 }
 
-/* Reading R13 for a value already divided by its tile scale: sign bit, then the nearest
+/* Reading R18 for a value already divided by its tile scale: sign bit, then the nearest
  * magnitude code. */
 uint8_t oracle_fp8_encode(double v)
 {

@@ -400,9 +400,9 @@ def test_swiglu_and_combine_against_torch():
     assert np.array_equal(out, ref)
 
 
-# ---------------------------------------------------------------- FP8 W8A8 baseline (readings R11-R13)
+# ---------------------------------------------------------------- FP8 W8A8 baseline (readings R16-R18)
 def test_fp8_encode_matches_torch_float8_on_every_bf16_value():
-    """Reading R13's E4M3 rounding (nearest, ties to even, sign kept) against torch's own
+    """Reading R18's E4M3 rounding (nearest, ties to even, sign kept) against torch's own
     float8_e4m3fn conversion, for every finite bf16 value of magnitude <= 448."""
     import torch
     bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
@@ -416,7 +416,7 @@ def test_fp8_encode_matches_torch_float8_on_every_bf16_value():
 
 
 def test_fp8_scale_exponent_closed_form():
-    """Reading R12: e = max(-127, ceil(log2(amax / 448))), computed with exact rationals, on
+    """Reading R17: e = max(-127, ceil(log2(amax / 448))), computed with exact rationals, on
     random and boundary magnitudes."""
     import math
     rng = np.random.default_rng(40)
@@ -439,7 +439,7 @@ def test_fp8_scale_exponent_closed_form():
 
 
 def test_fp8_tiles_scale_independently_and_round_trip_within_e4m3_bound():
-    """1 x 128 activation tiles and 128 x 128 weight tiles (reading R11): scaling one tile by a
+    """1 x 128 activation tiles and 128 x 128 weight tiles (reading R16): scaling one tile by a
     power of two changes only its scale byte, by that power, and none of the codes; every
     element dequantizes within half an E4M3 step of its value (relative 2^-4 in the normal
     range, absolute 2^(e-10) below it); ragged edges form partial tiles."""
