@@ -659,7 +659,8 @@ def profile_case(name: str):
     """Small cases for ncu captures (no timing, no JSON line): 'moe_small' runs two MoE layer
     forwards at E=32, T=4096, H=2048, I=768, top-8, k=32 (about 1 GB on the device);
     'act_256mb' quantizes and selects twice on a 32768 x 4096 bf16 activation (256 MB, larger
-    than L2), k=64."""
+    than L2), k=64; 'act_8192x4096' runs the activation workload of the bench line three times
+    (64 MB, L2 flushed before each)."""
     import torch
     from nvfp4_w4a4_quantized_quantize_gb300 import _lib as L
     from nvfp4_w4a4_quantized_quantize_gb300 import workloads as wl
@@ -677,6 +678,20 @@ def profile_case(name: str):
         ids_d, tw_d = torch.from_numpy(ids).to(dev), torch.from_numpy(tw).to(dev)
         for _ in range(2):
             layer.forward(x, ids_d, tw_d, out)
+    elif name == "act_8192x4096":
+        # the activation workload of the bench line, three times, L2 flushed before each
+        cfg = wl.CFG_ACT
+        x_bits, _, _ = cfg.make()
+        M, K, k = cfg.M, cfg.K, cfg.k
+        x = _bf16(x_bits, dev)
+        op = Operand.empty(M, K, k)
+        sc = torch.empty(K, dtype=torch.int64, device=dev)
+        idx = torch.empty(k, dtype=torch.int32, device=dev)
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            flush.zero_()
+            L.nvfp4_quantize(x, op.codes, op.sf, op.sf_cols, op.tscale, scores=sc)
+            L.rac_select_quantize(x, op.tscale, sc, k, op.codes, op.sf, op.sf_cols, idx)
     else:
         M, K, k = 32768, 4096, 64
         gen = torch.Generator(device=dev).manual_seed(11)
@@ -704,7 +719,7 @@ def main():
     ap.add_argument("--sweep-k", action="store_true",
                     help="residual channel ratio sweep (0 to 100 %% of K) at the activation, dense and MoE "
                          "workloads: error and time per ratio, one JSON line, then exit")
-    ap.add_argument("--profile-case", choices=["moe_small", "act_256mb"],
+    ap.add_argument("--profile-case", choices=["moe_small", "act_256mb", "act_8192x4096"],
                     help="run a small case twice for an ncu capture and exit (no timing)")
     args = ap.parse_args()
     if args.profile_case:

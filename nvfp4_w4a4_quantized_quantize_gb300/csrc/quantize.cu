@@ -36,11 +36,24 @@ __device__ __forceinline__ float amax_u4(uint4 w)
     return fmaxf(__low2float(r), __high2float(r));
 }
 
+// 16-byte load that marks its L2 lines evict-last: the quantize pass reads the same rows next,
+// and an input up to about half of L2 then stays there for it.
+__device__ __forceinline__ uint4 ld_keep(const uint4* p, uint64_t pol)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
 __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, int K,
                                                              Groups gr, int64_t rows_per_cta,
                                                              nvq_tensor_scale* __restrict__ ts)
 {
     __shared__ float red[kAmaxThreads / 32];
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
     const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
     const int64_t r1 = min(r0 + rows_per_cta, gr.total_rows);
     if (r0 >= r1) return;
@@ -61,15 +74,15 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const __nv_bfloat16*
                 for (; i + (kAmaxUnroll - 1) * kAmaxThreads < n; i += kAmaxUnroll * kAmaxThreads) {
                     uint4 w[kAmaxUnroll];
 #pragma unroll
-                    for (int u = 0; u < kAmaxUnroll; ++u) w[u] = __ldg(p + i + u * kAmaxThreads);
+                    for (int u = 0; u < kAmaxUnroll; ++u) w[u] = ld_keep(p + i + u * kAmaxThreads, pol);
 #pragma unroll
                     for (int u = 0; u < kAmaxUnroll; ++u) m = fmaxf(m, amax_u4(w[u]));
                 }
-                for (; i < n; i += kAmaxThreads) m = fmaxf(m, amax_u4(__ldg(p + i)));
+                for (; i < n; i += kAmaxThreads) m = fmaxf(m, amax_u4(ld_keep(p + i, pol)));
             } else {
                 for (int64_t r = a; r < b; ++r) {
                     const uint4* p = reinterpret_cast<const uint4*>(x + r * ldx);
-                    for (int v = threadIdx.x; v < vpr; v += kAmaxThreads) m = fmaxf(m, amax_u4(__ldg(p + v)));
+                    for (int v = threadIdx.x; v < vpr; v += kAmaxThreads) m = fmaxf(m, amax_u4(ld_keep(p + v, pol)));
                 }
             }
         }
@@ -132,10 +145,13 @@ __device__ __forceinline__ bool q_wait(uint64_t* bar, uint32_t parity, volatile 
     }
 }
 
-__device__ __forceinline__ void q_bulk_row(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+// Bulk copy of rows into the ring; the cache policy puts the lines the amax pass marked
+// evict-last back to normal priority once they are consumed.
+__device__ __forceinline__ void q_bulk_row(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol)
 {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(sa32(dst)),
-                 "l"(src), "r"(bytes), "r"(sa32(bar))
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+                     sa32(dst)),
+                 "l"(src), "r"(bytes), "r"(sa32(bar)), "l"(pol)
                  : "memory");
 }
 
@@ -231,11 +247,13 @@ __device__ __forceinline__ bool cursor_issue(const QuantArgs& qa, LoadCursor& c,
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa32(&full_bar[s])),
                  "r"((uint32_t)(nr * row_bytes))
                  : "memory");
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
     if (qa.ldx * 2 == row_bytes)  // contiguous rows: the whole stage in one copy
-        q_bulk_row(ring + s * kQStageBytes, qa.x + c.r * qa.ldx, (uint32_t)(nr * row_bytes), &full_bar[s]);
+        q_bulk_row(ring + s * kQStageBytes, qa.x + c.r * qa.ldx, (uint32_t)(nr * row_bytes), &full_bar[s], pol);
     else
         for (int j = 0; j < nr; ++j)
-            q_bulk_row(ring + s * kQStageBytes + j * row_bytes, qa.x + (c.r + j) * qa.ldx, row_bytes, &full_bar[s]);
+            q_bulk_row(ring + s * kQStageBytes + j * row_bytes, qa.x + (c.r + j) * qa.ldx, row_bytes, &full_bar[s], pol);
     ++c.it;
     c.r += R;
     if (c.r >= c.b) {

@@ -50,8 +50,11 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
 // Radix select of the k-th largest score, MSB first, 8 bits per pass.  Every thread keeps its
 // (at most 8) channels' scores in registers; per pass each warp folds equal digits with
 // __match_any_sync before one shared atomic per distinct digit, so the histogram sees no
-// contention.  The threshold T is exact; channels above T are all taken and the lowest-index
-// channels equal to T fill the rest (ties to the lower channel index).
+// contention.  The select stops as soon as the bin holding the k-th largest score holds exactly
+// the channels still needed (usually after two or three passes): every channel whose decided
+// high bits are above the prefix, and every channel of that bin, is taken.  Otherwise it runs to
+// the last bit and the threshold T is exact; channels above T are all taken and the
+// lowest-index channels equal to T fill the rest (ties to the lower channel index).
 static constexpr int kTopkPer = 8;  // channels per thread: K <= 8192
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const unsigned long long* __restrict__ scores, int K, int k,
@@ -60,7 +63,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const unsigned long 
     __shared__ unsigned int hist2[2][256];
     __shared__ int warp_sums[32];
     __shared__ unsigned long long s_prefix, s_or;
-    __shared__ int s_remaining;
+    __shared__ int s_remaining, s_done;
     const int g = blockIdx.x;
     const unsigned long long* src = scores + (int64_t)g * K;
     int32_t* out = idx + (int64_t)g * k;
@@ -75,7 +78,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const unsigned long 
         key[q] = (q < per && j < K) ? src[j] : 0ull;
         orv |= key[q];
     }
-    if (tid == 0) { s_or = 0; s_prefix = 0; s_remaining = k; }
+    if (tid == 0) { s_or = 0; s_prefix = 0; s_remaining = k; s_done = 0; }
     __syncthreads();
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) orv |= __shfl_xor_sync(0xffffffffu, orv, o);
@@ -119,6 +122,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const unsigned long 
                     if (above < rem && rem <= above + cnt[i]) {
                         s_prefix = prefix | ((unsigned long long)(255 - 8 * tid - i) << shift);
                         s_remaining = rem - above;
+                        s_done = cnt[i] == rem - above;  // the whole bin is needed
                     }
                     above += cnt[i];
                 }
@@ -126,7 +130,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const unsigned long 
         }
         mask |= 255ull << shift;
         __syncthreads();
+        if (s_done) break;  // uniform: read after the barrier
     }
+    // compare on the decided bits (all of them unless the select stopped early)
+#pragma unroll
+    for (int q = 0; q < kTopkPer; ++q) key[q] &= mask;
     const unsigned long long T = s_prefix;
     const int take_eq = s_remaining;
     int n_eq = 0;
