@@ -660,7 +660,10 @@ def profile_case(name: str):
     forwards at E=32, T=4096, H=2048, I=768, top-8, k=32 (about 1 GB on the device);
     'act_256mb' quantizes and selects twice on a 32768 x 4096 bf16 activation (256 MB, larger
     than L2), k=64; 'act_8192x4096' runs the activation workload of the bench line three times
-    (64 MB, L2 flushed before each)."""
+    (64 MB, L2 flushed before each); 'fp8_moe_small' runs two forwards of the FP8 W8A8 layer on the
+    'moe_small' shapes; 'row_tails_kK' runs the row-path tails once each at k = K: the gate/up
+    weight tail of 128 experts (N 1536, K 2048) and the residual tail of h (131072 x 768, 128
+    groups)."""
     import torch
     from nvfp4_w4a4_quantized_quantize_gb300 import _lib as L
     from nvfp4_w4a4_quantized_quantize_gb300 import workloads as wl
@@ -678,6 +681,36 @@ def profile_case(name: str):
         ids_d, tw_d = torch.from_numpy(ids).to(dev), torch.from_numpy(tw).to(dev)
         for _ in range(2):
             layer.forward(x, ids_d, tw_d, out)
+    elif name == "fp8_moe_small":
+        from nvfp4_w4a4_quantized_quantize_gb300.layers import Fp8MoELayer
+        E, T, H, I, topk = 32, 4096, 2048, 768, 8
+        cfg = wl.MoELayer("moe_small", T=T, H=H, E=E, topk=topk, I=I, k=0, seed=7, routing="zipf", n_outliers=20)
+        x_bits, ids, tw, _ = cfg.make_tokens()
+        w13_bits, w2_bits = cfg.make_weights()
+        layer = Fp8MoELayer(_bf16(w13_bits.reshape(E * 2 * I, H), dev).view(E, 2 * I, H),
+                            _bf16(w2_bits.reshape(E * H, I), dev).view(E, H, I), topk, T)
+        x = _bf16(x_bits, dev)
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        ids_d, tw_d = torch.from_numpy(ids).to(dev), torch.from_numpy(tw).to(dev)
+        for _ in range(2):
+            layer.forward(x, ids_d, tw_d, out)
+    elif name == "row_tails_kK":
+        from nvfp4_w4a4_quantized_quantize_gb300.layers import quantize_weights
+        L.set_tail_path(L.NVQ_TAIL_ROWS)
+        gen = torch.Generator(device=dev).manual_seed(13)
+        G, N, K = 128, 1536, 2048
+        op = quantize_weights((torch.randn(G, N, K, device=dev, generator=gen) * 0.02).bfloat16(), K)
+        idx = torch.arange(K, dtype=torch.int32, device=dev).unsqueeze(0)
+        L.rac_weight_tail(G, N, K, K, idx, op.codes, op.sf, op.sf_cols, op.tscale)
+        del op
+        M, K2, G2 = 131072, 768, 128
+        x = torch.randn(M, K2, device=dev, generator=gen).bfloat16()
+        a = Operand.empty(M, K2, K2, G2)
+        sc = torch.zeros(G2, K2, dtype=torch.int64, device=dev)
+        L.nvfp4_quantize(x, a.codes, a.sf, a.sf_cols, a.tscale, scores=sc, groups=G2)
+        idx2 = torch.arange(K2, dtype=torch.int32, device=dev).repeat(G2, 1).contiguous()
+        L.rac_residual_tail(x, a.tscale, idx2, K2, a.codes, a.sf, a.sf_cols, groups=G2)
+        L.set_tail_path(L.NVQ_TAIL_AUTO)
     elif name == "act_8192x4096":
         # the activation workload of the bench line, three times, L2 flushed before each
         cfg = wl.CFG_ACT
@@ -719,7 +752,7 @@ def main():
     ap.add_argument("--sweep-k", action="store_true",
                     help="residual channel ratio sweep (0 to 100 %% of K) at the activation, dense and MoE "
                          "workloads: error and time per ratio, one JSON line, then exit")
-    ap.add_argument("--profile-case", choices=["moe_small", "act_256mb", "act_8192x4096"],
+    ap.add_argument("--profile-case", choices=["moe_small", "fp8_moe_small", "act_256mb", "act_8192x4096", "row_tails_kK"],
                     help="run a small case twice for an ncu capture and exit (no timing)")
     args = ap.parse_args()
     if args.profile_case:
