@@ -509,38 +509,29 @@ def act_quant_bench(args, L, wl, dev, flush, peaks):
     ts = torch.empty(1, 4, dtype=torch.float32, device=dev)
     scores = torch.empty(K, dtype=torch.int64, device=dev)
     idx = torch.empty(k, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
+    def quant():
         L.nvfp4_quantize(x, codes, sf, sfc, ts, scores=scores)
-        if ev is not None:
-            ev[1].record(stream)
-        L.rac_select_quantize(x, ts, scores, k, codes, sf, sfc, idx)
-        if ev is not None:
-            ev[2].record(stream)
 
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    evs = []
-    for _ in range(args.steps):
-        flush.zero_()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        step(ev)
-        evs.append(ev)
-    torch.cuda.synchronize()
-    t_all = sum(e[0].elapsed_time(e[2]) for e in evs) / len(evs)
-    t_q = sum(e[0].elapsed_time(e[1]) for e in evs) / len(evs)
-    t_r = sum(e[1].elapsed_time(e[2]) for e in evs) / len(evs)
+    def select():
+        L.rac_select_quantize(x, ts, scores, k, codes, sf, sfc, idx)
+
+    def step():
+        quant()
+        select()
+
+    # CUDA-graph replays (as the layer step), L2 flushed before each: the whole path, and each
+    # half alone (the selection replays over the scores the last quantize left)
+    t_all = _time_replays(step, flush, args.steps, args.warmup)
+    t_q = _time_replays(quant, flush, args.steps, args.warmup)
+    t_r = _time_replays(select, flush, args.steps, args.warmup)
     algo = M * K * (2 + 0.5 + 1 / 16) + M * k * (2 + 0.5 + 1 / 16) + k * 4
     q_bytes = M * K * (2 + 0.5 + 1 / 16)
     hbm = peaks["hbm_gbs"]
     return {"workload": cfg.name, "algorithmic_bytes": int(algo), "ms": round(t_all, 4),
             "gbs": round(algo / (t_all * 1e-3) / 1e9, 1), "frac_of_measured_hbm": round(algo / (t_all * 1e-3) / 1e9 / hbm, 4),
             "nvfp4_quantize_ms": round(t_q, 4), "nvfp4_quantize_gbs": round(q_bytes / (t_q * 1e-3) / 1e9, 1),
-            "rac_select_quantize_ms": round(t_r, 4)}
+            "rac_select_quantize_ms": round(t_r, 4),
+            "timing": "median of CUDA-graph replays, L2 flushed (512 MiB write) before each"}
 
 
 # ----------------------------------------------------------------------------- oracle (CPU)
