@@ -101,7 +101,8 @@ nvq_status nvq_set_wait_limit(uint64_t cycles);
  * least traffic when k is a small share of K); NVQ_TAIL_ROWS reads whole rows with 16-byte
  * loads, expands them in shared memory and gathers from there (fewer instructions per tail
  * element when k is a large share); NVQ_TAIL_AUTO (the default) takes the row path when
- * k >= K / 4, and for a weight tail given the channel-major copy when k > K / 2.  A process-wide setting for launches made after the call; NVQ_ERR_ARG for an
+ * k >= K / 4, except for a weight tail given the channel-major copy, which always gathers.
+ * A process-wide setting for launches made after the call; NVQ_ERR_ARG for an
  * unknown value.  Not part of the paper's method: a choice between two schedules of Eq. (21). */
 enum nvq_tail_path { NVQ_TAIL_AUTO = 0, NVQ_TAIL_GATHER = 1, NVQ_TAIL_ROWS = 2 };
 nvq_status nvq_set_tail_path(int32_t path);

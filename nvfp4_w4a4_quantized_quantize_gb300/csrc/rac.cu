@@ -300,21 +300,20 @@ __global__ void __launch_bounds__(256) weight_tail_kernel(uint8_t* __restrict__ 
 }
 
 // Same tail from the channel-major copy (nvfp4_channel_major): CTA per (group, 64 weight rows,
-// chunk of up to 256 selected channels).  The CTA first stages, for each channel of its chunk,
-// the 32 code bytes and 64 scale bytes of its rows into shared memory with 16-byte loads (all in
-// flight together); then thread t builds row t's tail blocks of the chunk from there: 8 code
-// bytes per block, and the tail scale bytes as whole 32-bit words when they start on one
-// (K/16 % 4 == 0; every chunk but the last holds 16 blocks).  The CTA of the last chunk also
-// zeroes the scale padding.
+// chunk of up to 256 selected channels), split threads per row (1, 2 or 4: the tail blocks of
+// a row are dealt round-robin to them).  The CTA first stages, for each channel of its chunk,
+// the 32 code bytes and 64 scale bytes of its rows into shared memory with 16-byte loads (all
+// in flight together); then each thread builds its blocks of its row from there: 8 code bytes
+// and the scale byte per block.  The thread holding a row's last tail block of the last chunk
+// also zeroes the row's scale padding.
 constexpr int kWtRows = 64;
 constexpr int kWtChunk = 256;  // selected channels staged per pass (24 KB of shared memory)
+constexpr int kWtMaxSplit = 4;
 
-__global__ void __launch_bounds__(kWtRows) weight_tail_cm_kernel(uint8_t* __restrict__ codes, int64_t ld_codes,
-                                                                  uint8_t* __restrict__ sf, int64_t sf_cols, int64_t N,
-                                                                  int K, int k, const nvq_tensor_scale* __restrict__ ts,
-                                                                  const int32_t* __restrict__ idx, int idx_per_group,
-                                                                  const uint8_t* __restrict__ cm_codes,
-                                                                  const uint8_t* __restrict__ cm_sf)
+__global__ void __launch_bounds__(kWtRows * kWtMaxSplit) weight_tail_cm_kernel(
+    uint8_t* __restrict__ codes, int64_t ld_codes, uint8_t* __restrict__ sf, int64_t sf_cols, int64_t N, int K, int k,
+    const nvq_tensor_scale* __restrict__ ts, const int32_t* __restrict__ idx, int idx_per_group,
+    const uint8_t* __restrict__ cm_codes, const uint8_t* __restrict__ cm_sf)
 {
     extern __shared__ __align__(16) uint8_t wt_smem[];
     const int kc = k < kWtChunk ? k : kWtChunk;   // channels staged at a time
@@ -323,61 +322,46 @@ __global__ void __launch_bounds__(kWtRows) weight_tail_cm_kernel(uint8_t* __rest
     const int c0 = blockIdx.z * kWtChunk;
     const int g = blockIdx.y;
     const int64_t n0 = (int64_t)blockIdx.x * kWtRows;
-    const int t = threadIdx.x;
+    const int nthr = blockDim.x;
+    const int split = nthr / kWtRows;
+    const int t = threadIdx.x % kWtRows;   // row in the tile
+    const int part = threadIdx.x / kWtRows;
     const int nsb = K / 16;
     const int32_t* sel = idx + (idx_per_group ? (int64_t)g * k : 0);
-    const int64_t n = n0 + t;
     const float s_enc = ts[g].s_enc, s_dec = ts[g].s_dec;
-    const int64_t row = (int64_t)g * N + n;
+    const int64_t row = (int64_t)g * N + n0 + t;
     uint8_t* crow = codes + row * ld_codes + K / 2;
-    const bool word_sf = (nsb % 4) == 0;
-    uint32_t sfw = 0;  // tail scale bytes of the current 4-column group
-    {
-        const int cnt = k - c0 < kc ? k - c0 : kc;  // channels of this chunk (a multiple of 16)
-        // stage: per channel 2 x 16 code bytes + 4 x 16 scale bytes
-        for (int w = t; w < cnt * 6; w += kWtRows) {
-            const int c = w / 6, part = w % 6;
-            const int j = sel[c0 + c];
-            uint4 v;
-            if (part < 2)
-                v = __ldg(reinterpret_cast<const uint4*>(cm_codes + ((int64_t)g * K + j) * (N / 2) + n0 / 2) + part);
-            else
-                v = __ldg(reinterpret_cast<const uint4*>(cm_sf + ((int64_t)g * nsb + (j >> 4)) * N + n0) + (part - 2));
-            if (part < 2) reinterpret_cast<uint4*>(s_codes + c * 32)[part] = v;
-            else reinterpret_cast<uint4*>(s_sf + c * 64)[part - 2] = v;
-        }
-        __syncthreads();
-        for (int b = c0 / 16; b < (c0 + cnt) / 16; ++b) {
-            float wv[16];
+    const int cnt = k - c0 < kc ? k - c0 : kc;  // channels of this chunk (a multiple of 16)
+    // stage: per channel 2 x 16 code bytes + 4 x 16 scale bytes
+    for (int w = threadIdx.x; w < cnt * 6; w += nthr) {
+        const int c = w / 6, q = w % 6;
+        const int j = sel[c0 + c];
+        uint4 v;
+        if (q < 2)
+            v = __ldg(reinterpret_cast<const uint4*>(cm_codes + ((int64_t)g * K + j) * (N / 2) + n0 / 2) + q);
+        else
+            v = __ldg(reinterpret_cast<const uint4*>(cm_sf + ((int64_t)g * nsb + (j >> 4)) * N + n0) + (q - 2));
+        if (q < 2) reinterpret_cast<uint4*>(s_codes + c * 32)[q] = v;
+        else reinterpret_cast<uint4*>(s_sf + c * 64)[q - 2] = v;
+    }
+    __syncthreads();
+    const int b_end = (c0 + cnt) / 16;
+    for (int b = c0 / 16 + part; b < b_end; b += split) {
+        float wv[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int c = b * 16 + i - c0;
-                const uint32_t code = (s_codes[c * 32 + (t >> 1)] >> ((t & 1) * 4)) & 0xfu;
-                const uint32_t sb = s_sf[c * 64 + t];
-                wv[i] = __fmul_rn(e2m1_value(code), __fmul_rn(e4m3_value(sb), s_dec));
-            }
-            const BlockOut o = quantize16(wv, s_enc, s_dec);
-            *reinterpret_cast<uint2*>(crow + 8 * b) = make_uint2(o.code_lo, o.code_hi);
-            if (word_sf) {
-                sfw |= o.sb << (8 * (b & 3));
-                if ((b & 3) == 3) {
-                    *reinterpret_cast<uint32_t*>(sf + sf_offset(row, nsb + b - 3, sf_cols)) = sfw;
-                    sfw = 0;
-                }
-            } else {
-                sf[sf_offset(row, nsb + b, sf_cols)] = (uint8_t)o.sb;
-            }
+        for (int i = 0; i < 16; ++i) {
+            const int c = b * 16 + i - c0;
+            const uint32_t code = (s_codes[c * 32 + (t >> 1)] >> ((t & 1) * 4)) & 0xfu;
+            const uint32_t sb = s_sf[c * 64 + t];
+            wv[i] = __fmul_rn(e2m1_value(code), __fmul_rn(e4m3_value(sb), s_dec));
         }
+        const BlockOut o = quantize16(wv, s_enc, s_dec);
+        *reinterpret_cast<uint2*>(crow + 8 * b) = make_uint2(o.code_lo, o.code_hi);
+        sf[sf_offset(row, nsb + b, sf_cols)] = (uint8_t)o.sb;
     }
-    if (c0 + kWtChunk < k) return;  // not the last chunk
-    const int64_t cend = (K + k) / 16;
-    if (word_sf && (cend & 3)) {
-        // the last partial group: its remaining bytes are padding (zero)
-        *reinterpret_cast<uint32_t*>(sf + sf_offset(row, cend & ~3ll, sf_cols)) = sfw;
-        for (int64_t c = (cend | 3) + 1; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
-    } else {
-        for (int64_t c = cend; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
-    }
+    // scale padding of the row: by the thread that holds the row's last tail block
+    if (c0 + kWtChunk < k || part != (b_end - 1 - c0 / 16) % split) return;
+    for (int64_t c = (K + k) / 16; c < sf_cols; ++c) sf[sf_offset(row, c, sf_cols)] = 0;
 }
 
 // Channel-major copy of the codes: CTA per (group, 64 rows, 128 channels) tile, transposed
@@ -544,12 +528,13 @@ __global__ void __launch_bounds__(kRowThreads)
 
 // Row path when the setting asks for it, or (NVQ_TAIL_AUTO) past the crossover measured on GB300
 // at the MoE shapes: k >= K / 4 for activation tails and for weight tails gathered from the
-// row-major operand; k > K / 2 for weight tails with the channel-major copy (whose gather reads
-// only the selected channels' bytes, 16 at a time).
+// row-major operand.  A weight tail with the channel-major copy keeps its gather at every k (it
+// reads only the selected channels' bytes, 16 at a time, and measured at or below the row path
+// up to k = K).
 inline bool use_row_tail(int K, int k, bool channel_major)
 {
     if (tail_path() != NVQ_TAIL_AUTO) return tail_path() == NVQ_TAIL_ROWS;
-    return channel_major ? 2 * k > K : 4 * k >= K;
+    return !channel_major && 4 * k >= K;
 }
 
 template <bool kResidual>
@@ -714,7 +699,8 @@ extern "C" nvq_status rac_weight_tail(int32_t groups, int64_t N, int64_t K, int3
     if (!cm_codes) return weight_tail_impl(b_codes, ldb, b_sf, b_sf_cols, N, (int)K, k, groups, b_tscale, idx, idx_per_group, st);
     const size_t smem = (size_t)(k < kWtChunk ? k : kWtChunk) * 96;
     const dim3 grid((unsigned)(N / kWtRows), (unsigned)groups, (unsigned)((k + kWtChunk - 1) / kWtChunk));
-    weight_tail_cm_kernel<<<grid, kWtRows, smem, st>>>(b_codes, ldb, b_sf, b_sf_cols, N, (int)K, k, b_tscale, idx,
+    const int split = k / 16 < kWtMaxSplit ? k / 16 : kWtMaxSplit;  // threads per row
+    weight_tail_cm_kernel<<<grid, kWtRows * split, smem, st>>>(b_codes, ldb, b_sf, b_sf_cols, N, (int)K, k, b_tscale, idx,
                                                       idx_per_group, cm_codes, cm_sf);
     NVQ_LAUNCH_CHECK("weight_tail_cm_kernel");
     return NVQ_OK;
