@@ -145,8 +145,9 @@ __device__ __forceinline__ bool q_wait(uint64_t* bar, uint32_t parity, volatile 
     }
 }
 
-// Bulk copy of rows into the ring; the cache policy puts the lines the amax pass marked
-// evict-last back to normal priority once they are consumed.
+// Bulk copy of rows into the ring with a cache policy: normal priority (the lines the amax
+// pass marked evict-last go back to normal once consumed), or evict-last when the amax came
+// from the producer and the residual tail will read the rows again.
 __device__ __forceinline__ void q_bulk_row(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol)
 {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
@@ -205,6 +206,7 @@ struct QuantArgs {
     void* w_hat;
     DeviceStatus* status;
     unsigned long long wait_limit;
+    int keep_l2;  // mark the rows evict-last (the residual tail re-reads them) instead of normal
 };
 
 // BPT = 16-element blocks per thread along K (1: K / 16 <= kQCompute).
@@ -248,7 +250,10 @@ __device__ __forceinline__ bool cursor_issue(const QuantArgs& qa, LoadCursor& c,
                  "r"((uint32_t)(nr * row_bytes))
                  : "memory");
     uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    if (qa.keep_l2)
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    else
+        asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
     if (qa.ldx * 2 == row_bytes)  // contiguous rows: the whole stage in one copy
         q_bulk_row(ring + s * kQStageBytes, qa.x + c.r * qa.ldx, (uint32_t)(nr * row_bytes), &full_bar[s], pol);
     else
@@ -539,6 +544,9 @@ nvq_status quantize_impl(const void* x, int64_t rows, int64_t K, int64_t ldx, Gr
     qa.w_hat = w_hat;
     qa.status = device_status_ptr();
     qa.wait_limit = wait_limit();
+    // with the amax given there was no amax pass to leave x in L2: keep what fits for the
+    // residual tail, which reads part of every row again (and demotes the lines as it goes)
+    qa.keep_l2 = (amax_given && scores) ? 1 : 0;
     NVQ_CHECK_ARG(qa.status, NVQ_ERR_CUDA, "quantize: device status word unavailable");
     const int grid = (int)((rows + qa.rows_per_cta - 1) / qa.rows_per_cta);
     const bool sc = scores != nullptr;

@@ -178,6 +178,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const unsigned long 
 // with groups that do not start on 64-row boundaries) compute the factors directly.
 constexpr int kTailRows = 64;
 
+// A gathered bf16 element, its L2 line marked evict-first: after the tail the activation is
+// not read again, so whatever the quantize pass kept in L2 for the tail is released.
+__device__ __forceinline__ float ld_bf16_last_use(const __nv_bfloat16* p, uint64_t pol)
+{
+    unsigned short v;
+    asm volatile("ld.global.nc.L2::cache_hint.b16 %0, [%1], %2;" : "=h"(v) : "l"(p), "l"(pol));
+    return __uint_as_float((uint32_t)v << 16);
+}
+
 __global__ void __launch_bounds__(512) act_tail_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, int K, int k,
                                                        Groups gr, const nvq_tensor_scale* __restrict__ ts,
                                                        const int32_t* __restrict__ idx, uint8_t* __restrict__ codes,
@@ -200,6 +209,8 @@ __global__ void __launch_bounds__(512) act_tail_kernel(const __nv_bfloat16* __re
         db_tab[e] = (e == 127) ? 0.0f : __fmul_rn(sbv, s_dec0);
     }
     const bool sel_smem = k <= 512;  // larger channel sets are read from global memory
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     if (sel_smem)
         for (int c = tid; c < k; c += blockDim.x) s_sel[c] = idx[(int64_t)g0 * k + c];
     __syncthreads();
@@ -228,7 +239,7 @@ __global__ void __launch_bounds__(512) act_tail_kernel(const __nv_bfloat16* __re
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int j = (own && sel_smem) ? s_sel[b * 16 + i] : sel_g[b * 16 + i];
-            xv[i] = __bfloat162float(xr[j]);
+            xv[i] = ld_bf16_last_use(xr + j, pol);
             sb[i] = sf[sf_offset(row, j >> 4, sf_cols)];
         }
         float rv[16];
