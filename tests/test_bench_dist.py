@@ -67,3 +67,31 @@ def test_single_process_defaults():
     assert bench.dist_setup() == (1, 0, 0)
     assert bench.max_over_ranks(1.25, 1) == 1.25
     assert bench.job_throughput(100, 1, 10.0) == pytest.approx(1e4)
+
+
+def test_gemm_traffic_is_reported_only_for_the_profiled_source(tmp_path, monkeypatch):
+    """roofline.traffic comes from the committed ncu summary while gemm.cu is the source those
+    counters were taken on (SHA-256 recorded beside them), and is None once it differs."""
+    import hashlib
+
+    import bench
+    src = tmp_path / "gemm.cu"
+    src.write_text("kernel v1")
+    sha = hashlib.sha256(b"kernel v1").hexdigest()
+    prof = tmp_path / "traffic.md"
+    prof.write_text(f"traffic: launch=gate_up dram_read=100 dram_write=23 gemm_cu_sha256={sha}\n"
+                    f"traffic: launch=down dram_read=7 dram_write=8 gemm_cu_sha256={sha}\n")
+    monkeypatch.setattr(bench, "GEMM_SOURCE", str(src))
+    monkeypatch.setattr(bench, "TRAFFIC_PROFILE", str(prof))
+    assert bench.gemm_traffic_per_launch("gate_up") == 123
+    assert bench.gemm_traffic_per_launch("down") == 15
+    assert bench.gemm_traffic_per_launch("other") is None
+    src.write_text("kernel v2")
+    assert bench.gemm_traffic_per_launch("gate_up") is None
+
+
+def test_committed_traffic_matches_the_current_gemm_source():
+    """The committed summary carries the SHA-256 of the gemm.cu in the tree, so the bench line
+    reports traffic for the kernel it times."""
+    import bench
+    assert bench.gemm_traffic_per_launch("gate_up") is not None
