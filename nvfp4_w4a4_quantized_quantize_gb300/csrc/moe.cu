@@ -6,7 +6,8 @@
 //   dispatch   stable counting sort of the (token, slot) pairs by expert; every expert's rows
 //              start on a multiple of 128 so that a 128-row GEMM tile never spans two experts
 //              and the blocked scale layout stays tile-aligned;
-//   gather     copies each routed row's quantized codes and scales from its token row;
+//   gather     copies each routed row's quantized codes and scales from its token row (NVFP4
+//              rows, with their RAC tail, or the FP8 baseline's rows);
 //   combine    sums each token's topk expert outputs in slot order (fp32) and rounds to bf16.
 #include <cuda_bf16.h>
 

@@ -2,9 +2,10 @@
 // Q_W of Eq. (7) and the trainer's QDQ_W of Eq. (12)) with the per-channel residual score of
 // Eq. (23) fused into the same pass over the input.
 //
-// Two kernels per call, both HBM-bound:
-//   amax_kernel          per-group max |x| (the FP32 tensor scale's statistic): 16-byte loads,
-//                        8 in flight per thread, one atomicMax per (CTA, group run);
+// Two kernels per call (the first skipped when the producer of x measured the amax):
+//   amax_kernel          per-group max |x| (the FP32 tensor scale's statistic), HBM-bound:
+//                        16-byte loads marked evict-last in L2, 8 in flight per thread, one
+//                        atomicMax per (CTA, group run);
 //   quant_score_kernel   codes + blocked E4M3 scales + residual + integer channel score (+ the
 //                        dequantized values for the trainer-side QDQ).  One CTA of 16 warps per
 //                        SM: one lane streams the CTA's band of rows into a 5-stage shared
@@ -13,7 +14,8 @@
 //                        quantizes one 16-element block per row from shared memory, two or
 //                        more rows per stage (fewer hand-offs per element).  The CTA re-reads the
 //                        rows amax_kernel's CTAs just streamed, so most of that second read is
-//                        served by L2.
+//                        served by L2.  Bound by instruction issue (the exact score costs about
+//                        as much as the quantization), not by HBM.
 #include <cuda_bf16.h>
 
 #include "common.cuh"

@@ -1,16 +1,22 @@
 // rac.cu -- Residual Activation Compensation (QUADS §3.3).
 //
-//   topk_kernel        S = TopK of the channel scores (Eq. (24)), one CTA per group: an
-//                      MSB-first radix select over the uint64 scores in shared memory finds the
-//                      k-th largest score, ties at the threshold go to the lower channel index,
-//                      and a block scan emits the selected channels in ascending order.
-//   act_tail_kernel    second pass of Eq. (21): the residual X - DQ(Q(X)) on the selected
-//                      channels (recomputed from x and the stored block scale, bit-identical to
-//                      the first pass) is quantized, 16 selected channels per block, into the
-//                      tail columns [K, K + k) of the activation operand.
-//   weight_tail_kernel the weight columns that multiply the correction: dequantized stored
-//                      weights on the selected channels, re-quantized with the weight's S_enc,
-//                      into the tail columns of the weight operand.
+//   topk_kernel            S = TopK of the channel scores (Eq. (24)), one CTA per group: an
+//                          MSB-first radix select over the uint64 scores finds the k-th largest
+//                          score (stopping once its bin holds exactly the channels still
+//                          needed), ties at the threshold go to the lower channel index, and a
+//                          block scan emits the selected channels in ascending order.
+//   act_tail_kernel        second pass of Eq. (21): the residual X - DQ(Q(X)) on the selected
+//                          channels (recomputed from x and the stored block scale,
+//                          bit-identical to the first pass) is quantized, 16 selected channels
+//                          per block, into the tail columns [K, K + k) of the activation operand.
+//   weight_tail_kernel     the weight columns that multiply the correction: dequantized stored
+//                          weights on the selected channels, re-quantized with the weight's
+//                          S_enc, into the tail columns of the weight operand (gathered from
+//                          the row-major operand);
+//   weight_tail_cm_kernel  the same tail from a channel-major copy of the weights
+//                          (channel_major_codes_kernel / channel_major_sf_kernel make it);
+//   row_tail_kernel        both tails for a large share of channels: whole rows expanded in
+//                          shared memory, then gathered (the schedule nvq_set_tail_path picks).
 #include <cuda_bf16.h>
 
 #include "common.cuh"
