@@ -76,9 +76,13 @@ LIB_PATH = _build.LIB
 
 
 def _ptr(t):
+    """Address of a buffer argument (None -> NULL).  Every buffer the library takes is device
+    memory; a host tensor would reach a kernel as an invalid address, so it is refused here."""
     if t is None:
         return None
     if isinstance(t, torch.Tensor):
+        if not t.is_cuda:
+            raise ValueError(f"expected a CUDA tensor, got a tensor on {t.device}")
         return C.c_void_p(t.data_ptr())
     return C.c_void_p(t)
 

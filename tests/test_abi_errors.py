@@ -77,3 +77,13 @@ def test_tail_path_setting():
 
 def test_fp8_layout_helper():
     assert [Lmod.fp8_sf_cols(K) for K in (32, 128, 160, 768, 2048, 2080)] == [4, 4, 8, 24, 64, 68]
+
+
+def test_binding_refuses_host_tensors():
+    """A host tensor handed to the binding is refused before the library sees its address."""
+    import torch
+    x = torch.zeros(4, 32, dtype=torch.bfloat16)
+    codes = torch.zeros(4, 32, dtype=torch.uint8)
+    sf = torch.zeros(512, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        Lmod.fp8_quantize(x, codes, sf, 4)
