@@ -487,3 +487,19 @@ def test_fp8_gemm_against_torch_float8_decode():
     a = dec(ac) * np.exp2(np.repeat(asc.astype(np.float64) - 127, 128, axis=1))
     b = dec(bc) * np.exp2(np.repeat(np.repeat(bsc.astype(np.float64) - 127, 128, axis=0)[:136], 128, axis=1))
     assert np.allclose(oracle.fp8_gemm(ac, asc, bc, bsc), a @ b.T, rtol=1e-12, atol=0)
+
+
+def test_fp8_hand_worked_tiles():
+    """The FP8 oracle against a row quantized by hand from readings R16-R18
+    (tests/golden/fp8_tile_example.json: a full tile and an edge tile, signed zeros, a value
+    that flushes to zero, and a scale below one)."""
+    ex = json.load(open(os.path.join(GOLDEN, "fp8_tile_example.json")))
+    x = np.zeros((1, ex["cols"]), np.float64)
+    for j, v in ex["nonzero_x"].items():
+        x[0, int(j)] = -0.0 if v == "-0" else v
+    codes, scales = oracle.fp8_quantize(wl.to_bf16_bits(x), 1)
+    assert list(scales[0]) == ex["scale_bytes"]
+    want = np.zeros(ex["cols"], np.uint8)
+    for j, c in ex["codes_nonzero"].items():
+        want[int(j)] = c
+    assert np.array_equal(codes[0], want)
