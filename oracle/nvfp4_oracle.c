@@ -24,6 +24,9 @@
  *      amax == 0 gives S_enc = S_dec = 1.
  *   R5 Block scale: sb = e4m3(fl(fl(amax_b / 6) * S_enc)); element code
  *      q = e2m1(fl(x * fl(S_enc / sb))); sb == 0 gives code 0 (0x8 for a negative sign bit).
+ *      The quotient fl(S_enc / sb) saturates at FLT_MAX like S_enc itself (R4): it can overflow
+ *      only when S_enc was clamped (amax below 2688 / FLT_MAX) and sb < 1, and saturation keeps
+ *      every product finite (x = 0 then encodes as a signed zero, never as the code of a NaN).
  *   R6 Dequantization: fl(V[q] * fl(sb * S_dec)).
  *   R7 Residual r = fl(x - DQ(Q(x))) (= -dX_q of Eq. (20)).  The channel score of Eq. (23) is
  *      the exact integer sum over rows of q^2 with q = rint(|r| * 2^(20 - E)) (nearest integer,
@@ -52,10 +55,13 @@
  * FP32 (compile with -ffp-contract=off so that no multiply-add is fused); fp64 / exact
  * integers for reductions and the GEMM reference.
  */
+#define _POSIX_C_SOURCE 200809L
 #include <math.h>
+#include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#include <unistd.h>
 
 /* ------------------------------------------------------------------------------------------
  * bf16 (the activation and weight storage type of the rollout path)
@@ -204,6 +210,7 @@ static void quantize_block16(const float* v, float s_enc, uint8_t* codes, uint8_
         return;
     }
     float e_b = s_enc / (float)oracle_e4m3_value(sb);
+    if (isinf(e_b)) e_b = 3.4028234663852886e38f; /* reading R5: saturates, as S_enc does (R4) */
     for (int i = 0; i < 16; ++i) {
         float y = v[i] * e_b;
         codes[i] = oracle_e2m1_encode(y);
@@ -375,12 +382,22 @@ void oracle_weight_tail(const uint8_t* wcodes, int64_t ld_wcodes, const uint8_t*
  * int64 (|term| < 2^43, at most 2^13 terms); the only rounding is the final fp64 scaling.
  * Evaluated at the (m, n) pairs given (row indices into A, row indices into B).
  * ---------------------------------------------------------------------------------------- */
-void oracle_gemm_pairs(const uint8_t* a_codes, int64_t lda, const uint8_t* a_scales, int64_t ld_as,
-                       const uint8_t* b_codes, int64_t ldb, const uint8_t* b_scales, int64_t ld_bs,
-                       int64_t ktot, double s_dec_a, double s_dec_b, const int64_t* mi,
-                       const int64_t* ni, int64_t npairs, double* y)
+typedef struct gemm_job {
+    const uint8_t *a_codes, *a_scales, *b_codes, *b_scales;
+    int64_t lda, ld_as, ldb, ld_bs, ktot;
+    double s_dec_a, s_dec_b;
+    const int64_t *mi, *ni;
+    int64_t p0, p1;
+    double* y;
+} gemm_job;
+
+static void gemm_pair_range(const gemm_job* j)
 {
-    for (int64_t p = 0; p < npairs; ++p) {
+    const uint8_t *a_codes = j->a_codes, *a_scales = j->a_scales, *b_codes = j->b_codes, *b_scales = j->b_scales;
+    const int64_t lda = j->lda, ld_as = j->ld_as, ldb = j->ldb, ld_bs = j->ld_bs, ktot = j->ktot;
+    const int64_t *mi = j->mi, *ni = j->ni;
+    double* y = j->y;
+    for (int64_t p = j->p0; p < j->p1; ++p) {
         const uint8_t* ar = a_codes + mi[p] * lda;
         const uint8_t* br = b_codes + ni[p] * ldb;
         const uint8_t* as = a_scales + mi[p] * ld_as;
@@ -393,8 +410,54 @@ void oracle_gemm_pairs(const uint8_t* a_codes, int64_t lda, const uint8_t* a_sca
             int64_t sbv = (int64_t)llround(ldexp(oracle_e4m3_value(bs[c / 16]), 9));
             acc += va * vb * sa * sbv;
         }
-        y[p] = ldexp((double)acc, -20) * s_dec_a * s_dec_b;
+        y[p] = ldexp((double)acc, -20) * j->s_dec_a * j->s_dec_b;
     }
+}
+
+static void* gemm_thread(void* arg)
+{
+    gemm_pair_range((const gemm_job*)arg);
+    return NULL;
+}
+
+/* Host threads the pairs are spread over (1 by default).  Every pair is computed by one thread
+ * with the same arithmetic, so the result does not depend on the count. */
+static int g_threads = 1;
+
+void oracle_set_threads(int n) { g_threads = n < 1 ? 1 : (n > 1024 ? 1024 : n); }
+
+int oracle_hardware_threads(void)
+{
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n < 1 ? 1 : (int)n;
+}
+
+void oracle_gemm_pairs(const uint8_t* a_codes, int64_t lda, const uint8_t* a_scales, int64_t ld_as,
+                       const uint8_t* b_codes, int64_t ldb, const uint8_t* b_scales, int64_t ld_bs,
+                       int64_t ktot, double s_dec_a, double s_dec_b, const int64_t* mi,
+                       const int64_t* ni, int64_t npairs, double* y)
+{
+    gemm_job base = {a_codes, a_scales, b_codes, b_scales, lda, ld_as, ldb, ld_bs, ktot, s_dec_a, s_dec_b,
+                     mi, ni, 0, npairs, y};
+    int nt = g_threads;
+    if ((int64_t)nt > npairs / 16) nt = (int)(npairs / 16);
+    if (nt <= 1) {
+        gemm_pair_range(&base);
+        return;
+    }
+    gemm_job jobs[1024];
+    pthread_t tids[1024];
+    int created[1024];
+    for (int t = 0; t < nt; ++t) {
+        jobs[t] = base;
+        jobs[t].p0 = npairs * t / nt;
+        jobs[t].p1 = npairs * (t + 1) / nt;
+        created[t] = t > 0 && pthread_create(&tids[t], NULL, gemm_thread, &jobs[t]) == 0;
+        if (t > 0 && !created[t]) gemm_pair_range(&jobs[t]);  /* no thread: compute it here */
+    }
+    gemm_pair_range(&jobs[0]);
+    for (int t = 1; t < nt; ++t)
+        if (created[t]) pthread_join(tids[t], NULL);
 }
 
 /* The same product as plain fp64 arithmetic on the dequantized operands (cross-check). */

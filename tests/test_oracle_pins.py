@@ -206,6 +206,27 @@ def test_tensor_scale_edge_cases():
     assert ts.s_enc == 448.0 and ts.shift_e == 4
 
 
+def test_tiny_tensor_encode_factor_saturates_and_zeros_stay_signed_zeros():
+    """Tensor amax below 2688 / FLT_MAX: S_enc is clamped to FLT_MAX (R4), and for a block scale
+    below 1 the quotient fl(S_enc / sb) would overflow.  It saturates at FLT_MAX (R5), so every
+    product x * e_b is finite: +0 and -0 encode as 0x0 and 0x8 (never as the code of a NaN,
+    whose sign differs between hosts) and a non-zero x as the E2M1 of x * FLT_MAX."""
+    fmax = np.float32(np.finfo(np.float32).max)
+    v = 0x0080  # bf16 2^-126, the smallest normal
+    x = np.array([[v, 0x0000, 0x8000, v | 0x8000] + [0x0000] * 12], np.uint16)
+    ts = oracle.tensor_scale(x)
+    assert ts.s_enc == fmax
+    t = np.float32(np.float32(2.0 ** -126) / np.float32(6.0)) * fmax
+    sb = oracle.e4m3_encode(np.array([t], np.float32))[0]
+    assert 0 < oracle.e4m3_value(int(sb)) < 1.0   # the quotient S_enc / sb overflows binary32
+    c, s = oracle.quantize(x, ts)
+    assert s[0, 0] == sb
+    codes = [(c[0, i // 2] >> (4 * (i % 2))) & 0xF for i in range(16)]
+    big = oracle.e2m1_encode(np.array([np.float32(2.0 ** -126) * fmax], np.float32))[0]
+    assert codes[:4] == [big, 0x0, 0x8, big | 0x8]
+    assert codes[4:] == [0x0] * 12
+
+
 # ------------------------------------------------------------------------------ RAC
 def test_scores_rank_like_l2_norm():
     """Eq. (23): the integer score ranks channels as the L2 norm of the residual does."""
