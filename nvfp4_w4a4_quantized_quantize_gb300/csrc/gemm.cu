@@ -5,12 +5,10 @@
 // Y[r, n] = alpha_g * sum_{c < K+k} V[a_rc] sa_{r,c/16} V[b_nc] sb_{n,c/16},
 // alpha_g = S_dec(A_g) * S_dec(W_g), for the rows r of group g and the weight rows of group g.
 //
-// sm_103a design (one CTA per SM, persistent, clusters of two CTAs):
-//   tile 128 x 256 x 256 (M x N x K-tile of FP4 elements = 128 bytes per row) per CTA; the two
-//   CTAs of a cluster take adjacent 128-row tiles of the same group and the same N tile, so
-//   they need the same weight tile: each loads one 128-row half of it (and of its scales)
-//   and multicasts it into both CTAs' shared memory.  That cuts the L2-to-SM traffic per
-//   MMA by a third, the limit of the single-CTA kernel;
+// sm_103a design (one CTA per SM, persistent):
+//   tile 128 x 256 x 256 (M x N x K-tile of FP4 elements = 128 bytes per row) per CTA; tiles run
+//   N-fastest inside each 128-row block, so the CTAs working at the same time read one A block
+//   and one group's weights, which L2 serves to all of them;
 //   warp 0     TMA producer: A and B code tiles by cp.async.bulk.tensor (128-byte swizzle,
 //              out-of-range columns zero-filled), scale atoms by cp.async.bulk (the blocked
 //              scale layout makes every 128-row x 64-column scale tile one contiguous 512 B);
@@ -51,7 +49,6 @@ constexpr int kThreads = 448;  // warp 0 TMA, warp 1 MMA, warps 2-5 scale stagin
 constexpr int kFirstEpiWarp = 6;
 constexpr int kEpiThreads = 256;
 constexpr int kMaxGroups = 512;
-constexpr int kCluster = 2;  // CTAs sharing one weight tile by multicast
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;                  // 256 fp32 columns
 constexpr uint32_t kSFCol = 256;                 // + stage * F::kSFColsPerStage
@@ -177,7 +174,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (!draining && *abort_flag) return false;
-        if ((unsigned long long)(clock64() - t0) > a.wait_limit) {
+        if ((unsigned long long)(clock64() - t0) > (draining ? drain_limit(a.wait_limit) : a.wait_limit)) {
             report_timeout(a.status, where);
             *abort_flag = 1;
             return false;
@@ -209,39 +206,6 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
-}
-
-// Commit that arrives on the barrier at the same offset in both CTAs of the cluster.
-__device__ __forceinline__ void tc_commit_both(uint64_t* bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                     smem_u32(bar)),
-                 "h"((uint16_t)((1u << kCluster) - 1u))
-                 : "memory");
-}
-
-// Weight tile half and scale atoms into the same offset of both CTAs' shared memory; each
-// destination's barrier at the same offset receives the byte count.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"((uint16_t)((1u << kCluster) - 1u)), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_load_mc(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], %4;" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar)), "h"((uint16_t)((1u << kCluster) - 1u))
-                 : "memory");
-}
-
-__device__ __forceinline__ void cluster_sync_all()
-{
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
 // Shared-memory matrix descriptor (tcgen05 format): start >> 4, LBO >> 4, SBO >> 4, version 1,
@@ -380,37 +344,34 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v
 struct Tile {
     int g;
     int row0;       // first A row of this CTA's 128-row tile (rows < 2^24)
-    int rows;       // valid rows in the tile (0..128; 0: the group has no second tile here)
-    int lrow0;      // first A row loaded (row0, or the pair's first tile when rows == 0)
+    int rows;       // valid rows in the tile (1..128)
     int nt;         // N tile
 };
 
 // Per-group tables in shared memory, filled once per CTA: first row, row count and the prefix
-// of 256-row tile pairs (one pair per cluster).  Pairs run N-fastest inside each 256-row block
-// so that the clusters working at the same time share one A block (read from HBM once) and one
-// group's weights (kept in L2).
+// of 128-row tiles.  Tiles run N-fastest inside each 128-row block, so that the CTAs working at
+// the same time share one A block (read from HBM once) and one group's weights (kept in L2).
 struct GroupTab {
     int start[kMaxGroups];
     int rows[kMaxGroups];
     int mt_pre[kMaxGroups + 1];
 };
 
-__device__ __forceinline__ Tile tile_of(int64_t t, int n_tiles, const GroupTab& tab, int G, int rank)
+__device__ __forceinline__ Tile tile_of(int64_t t, int n_tiles, const GroupTab& tab, int G)
 {
     Tile T;
     T.nt = (int)(t % n_tiles);
-    const int gp = (int)(t / n_tiles);
+    const int gm = (int)(t / n_tiles);  // global 128-row tile index
     int lo = 0, hi = G - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (tab.mt_pre[mid] <= gp) lo = mid; else hi = mid - 1;
+        if (tab.mt_pre[mid] <= gm) lo = mid; else hi = mid - 1;
     }
     T.g = lo;
-    const int mt = kCluster * (gp - tab.mt_pre[lo]) + rank;
+    const int mt = gm - tab.mt_pre[lo];
     T.row0 = tab.start[lo] + mt * kBM;
     const int left = tab.rows[lo] - mt * kBM;
-    T.rows = left <= 0 ? 0 : (left < kBM ? left : kBM);
-    T.lrow0 = T.rows > 0 ? T.row0 : tab.start[lo] + (mt - rank) * kBM;
+    T.rows = left < kBM ? left : kBM;
     return T;
 }
 
@@ -443,9 +404,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = a.gr.G;
-    uint32_t rank;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
-    const int64_t cluster_id = blockIdx.x / kCluster, n_clusters = gridDim.x / kCluster;
 
     // per-group tables: rows and starts in parallel, the tile prefix by warp 0
     for (int g = threadIdx.x; g < G; g += kThreads) {
@@ -459,12 +417,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&full_bar[i], 1);
             mbar_init(&sf_bar[i], 4);  // the four scale-staging warps
-            mbar_init(&empty_bar[i], kCluster);  // both CTAs' MMAs release a stage
+            mbar_init(&empty_bar[i], 1);  // the MMA commit releases a stage
         }
         mbar_init(&acc_full, 1);
         mbar_init(&acc_empty, kEpiThreads);
         mbar_init(&drain_bar, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");  // visible to the async proxy
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncthreads();
@@ -474,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
         for (int i = 0; i < kPer; ++i) {
             const int g = lane * kPer + i;
-            cnt[i] = g < G ? ((tab.rows[g] + kBM - 1) / kBM + kCluster - 1) / kCluster : 0;
+            cnt[i] = g < G ? (tab.rows[g] + kBM - 1) / kBM : 0;
             sum += cnt[i];
         }
         int incl = sum;
@@ -499,7 +457,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
     tc_fence_before();
     __syncthreads();
-    cluster_sync_all();  // the peer's barriers are initialised before any multicast reaches them
     tc_fence_after();
     const uint32_t tmem = tmem_base_slot;
     const int total_mtiles = tab.mt_pre[G];
@@ -515,8 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
         int stage = 0;
         uint32_t phase = 0, issued = 0;
-        for (int64_t t = cluster_id; t < total_tiles && !*abrt; t += n_clusters) {
-            const Tile T = tile_of(t, n_tiles, tab, G, (int)rank);
+        for (int64_t t = blockIdx.x; t < total_tiles && !*abrt; t += gridDim.x) {
+            const Tile T = tile_of(t, n_tiles, tab, G);
             int64_t brow0, brow1;
             if (a.epilogue == NVQ_EPI_SWIGLU) {
                 brow0 = (int64_t)T.g * a.N + (int64_t)T.nt * (kBN / 2);
@@ -536,18 +493,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     uint8_t* sSFA = sB + kBBytes;
                     uint8_t* sSFB = sSFA + kSFABytes;
                     mbar_expect_tx(&full_bar[stage], kABytes + kBBytes + 3u * 512u * n_atoms);
-                    // own A tile and scales; this CTA's halves of the weight tile and their scales
-                    // into every CTA of the cluster (the peer sends the other half)
-                    tma_load_2d(sA, &tmap_a, kt * kRowBytes, T.lrow0, &full_bar[stage]);
-                    const uint8_t* srcA = a.a_sf + ((int64_t)(T.lrow0 >> 7) * (a.a_sf_cols >> 2) + kt * kSfAtoms) * 512;
+                    // the A tile and its scales; the two 128-row halves of the weight tile and theirs
+                    tma_load_2d(sA, &tmap_a, kt * kRowBytes, T.row0, &full_bar[stage]);
+                    const uint8_t* srcA = a.a_sf + ((int64_t)(T.row0 >> 7) * (a.a_sf_cols >> 2) + kt * kSfAtoms) * 512;
                     bulk_load(sSFA, srcA, 512u * n_atoms, &full_bar[stage]);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        if (h % kCluster != (int)rank) continue;
                         const int64_t brow = h ? brow1 : brow0;
-                        tma_load_2d_mc(sB + h * (kBBytes / 2), &tmap_b, kt * kRowBytes, (int)brow, &full_bar[stage], pol_keep);
+                        tma_load_2d_hint(sB + h * (kBBytes / 2), &tmap_b, kt * kRowBytes, (int)brow, &full_bar[stage], pol_keep);
                         const uint8_t* srcB = a.b_sf + ((brow >> 7) * (a.b_sf_cols >> 2) + kt * kSfAtoms) * 512;
-                        bulk_load_mc(sSFB + h * (kSFBBytes / 2), srcB, 512u * n_atoms, &full_bar[stage]);
+                        bulk_load(sSFB + h * (kSFBBytes / 2), srcB, 512u * n_atoms, &full_bar[stage]);
                     }
                     ++issued;
                     if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -574,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         int stage = 0;
         uint32_t phase = 0, acc_phase = 0;
         bool issued_any = false;
-        for (int64_t t = cluster_id; t < total_tiles && !*abrt; t += n_clusters) {
+        for (int64_t t = blockIdx.x; t < total_tiles && !*abrt; t += gridDim.x) {
             if (!mbar_wait(&acc_empty, acc_phase ^ 1, a, abrt, 2)) break;
             tc_fence_after();
             bool ok = true;
@@ -592,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         if (j < n_mma)
                             F::mma(tmem + kAccCol, a_desc0 + so + 2 * j, b_desc0 + so + 2 * j, F::idesc(j),
                                    sfa_t + 4 * GF::atom_of(j), sfb_t + 8 * GF::atom_of(j), (kt > 0 || j > 0) ? 1u : 0u);
-                    tc_commit_both(&empty_bar[stage]);  // the stage also holds the peer's weight half
+                    tc_commit(&empty_bar[stage]);
                     issued_any = true;
                 }
                 __syncwarp();
@@ -617,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
         int stage = 0;
         uint32_t phase = 0;
-        for (int64_t t = cluster_id; t < total_tiles && !*abrt; t += n_clusters) {
+        for (int64_t t = blockIdx.x; t < total_tiles && !*abrt; t += gridDim.x) {
             bool ok = true;
             for (int kt = 0; kt < num_kt; ++kt) {
                 if (!mbar_wait(&full_bar[stage], phase, a, abrt, 5)) { ok = false; break; }
@@ -664,8 +619,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const bool wide = (a.ldo % 16) == 0 && (reinterpret_cast<uintptr_t>(a.out) % 32) == 0;
         uint32_t acc_phase = 0;
-        for (int64_t t = cluster_id; t < total_tiles && !*abrt; t += n_clusters) {
-            const Tile T = tile_of(t, n_tiles, tab, G, (int)rank);
+        for (int64_t t = blockIdx.x; t < total_tiles && !*abrt; t += gridDim.x) {
+            const Tile T = tile_of(t, n_tiles, tab, G);
             const bool valid = r_in_tile < T.rows;
             const int64_t grow = (int64_t)T.row0 + r_in_tile;
             // NVFP4: alpha_g = S_dec(A) S_dec(W); FP8 (no tensor scales): 1
@@ -740,7 +695,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
     tc_fence_before();
     __syncthreads();
-    cluster_sync_all();  // no multicast of the peer still targets this CTA's shared memory
     tc_fence_after();
     if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
@@ -781,8 +735,7 @@ static nvq_status make_map(CUtensorMap* m, const void* base, int64_t inner_bytes
 nvq_status weight_tail_impl(uint8_t* codes, int64_t ld_codes, uint8_t* sf, int64_t sf_cols, int64_t N, int K, int k,
                             int G, const nvq_tensor_scale* ts, const int32_t* idx, int idx_per_group, cudaStream_t st);
 
-// Persistent launch in clusters of two: one cluster per SM pair that can hold one (occupancy
-// query), no more than the tile pairs of the work.
+// Persistent launch: one CTA per SM, no more CTAs than tiles.
 template <class F>
 nvq_status launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& ga, int32_t groups, int64_t N,
                        cudaStream_t st)
@@ -793,26 +746,10 @@ nvq_status launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmA
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(gemm_kernel)");
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmem;
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cfg.gridDim = dim3((unsigned)sms);
-    int max_clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, gemm_kernel<F>, &cfg) != cudaSuccess || max_clusters < 1)
-        max_clusters = sms / kCluster;
-    const int64_t max_pairs = (int64_t)(ga.total_mtiles_max / kCluster + 1 + groups) * (N / kBN);
-    const int clusters = (int)(max_pairs < max_clusters ? max_pairs : max_clusters);
-    cfg.gridDim = dim3((unsigned)(clusters * kCluster));
-    e = cudaLaunchKernelEx(&cfg, gemm_kernel<F>, ma, mb, ga);
-    if (e != cudaSuccess) return cuda_status(e, "cudaLaunchKernelEx(gemm_kernel)");
+    // an upper bound of the tiles: every group adds at most one partial 128-row tile
+    const int64_t max_tiles = (int64_t)(ga.total_mtiles_max + groups) * (N / kBN);
+    const int ctas = (int)(max_tiles < sms ? max_tiles : sms);
+    gemm_kernel<F><<<ctas, kThreads, kSmem, st>>>(ma, mb, ga);
     NVQ_LAUNCH_CHECK("gemm_kernel");
     return NVQ_OK;
 }
