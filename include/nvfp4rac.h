@@ -89,11 +89,16 @@ enum nvq_dtype { NVQ_BF16 = 0, NVQ_F32 = 1 };
 const char* nvq_last_error(void);
 
 /* Reads and clears the device status word of the current device (synchronises the stream).
- * *status receives NVQ_OK or NVQ_ERR_TIMEOUT; *where an identifier of the wait that ran out. */
+ * *status receives the first error a kernel recorded since the last read: NVQ_OK, or
+ * NVQ_ERR_TIMEOUT (a bounded wait ran out), or NVQ_ERR_ARG (moe_dispatch met an expert id
+ * outside [0, groups)); *where identifies the wait or check. */
 nvq_status nvq_device_status(void* stream, int32_t* status, int32_t* where);
 
-/* Sets the bound of every device-side wait, in GPU clock cycles (default 2^32, about 2 s).
- * Applies to launches made after the call on the current device. */
+/* Sets the bound of every device-side wait, in GPU clock cycles (default 2^32, about 2 s; any
+ * value >= 1).  Applies to launches made after the call.  A wait that runs out records
+ * NVQ_ERR_TIMEOUT and its CTA unwinds: before it exits, the CTA waits for the asynchronous copies
+ * it already issued, with a bound of its own of at least 2^26 cycles, so a very small limit (as
+ * tests use to exercise the timeout path) gives errors, never a copy into a finished CTA. */
 nvq_status nvq_set_wait_limit(uint64_t cycles);
 
 /* How rac_select_quantize, rac_residual_tail and rac_weight_tail build the tail columns; every
@@ -113,6 +118,14 @@ nvq_status nvq_set_tail_path(int32_t path);
  * three scale-factor copies into TMEM that the GEMM issues per MMA.  Synchronous on `stream`;
  * *tflops receives the achieved TFLOP/s. */
 nvq_status nvq_fp4_mma_rate(int32_t mmas_per_sm, int32_t with_cp, float* tflops, void* stream);
+
+/* Self-check of the quantizer's division of a block amax by 6 (not part of the paper's method:
+ * the kernels form fl(amax_b / 6) with a multiply and an FMA correction instead of a division).
+ * Runs every finite non-negative bf16 value through both that form and the IEEE division
+ * __fdiv_rn on the GPU.  result: device uint32 [2] out; result[0] = number of values whose
+ * results differ (0 expected), result[1] = the lowest such bf16 bit pattern (0xffffffff if
+ * none).  Asynchronous on `stream`. */
+nvq_status nvq_check_block_scale_division(uint32_t* result, void* stream);
 
 /* Scale-layout helpers (host functions, no device access). */
 int64_t nvq_sf_cols(int64_t ktot);                      /* roundup(ktot / 16, 4) */
@@ -147,6 +160,17 @@ nvq_status nvfp4_quantize(const void* x, int64_t rows, int64_t K, int64_t ldx,
                           uint8_t* codes, int64_t ld_codes, uint8_t* sf, int64_t sf_cols,
                           int32_t zero_pad, nvq_tensor_scale* tscale, uint64_t* scores,
                           int32_t amax_given, void* stream);
+
+/*
+ * nvfp4_amax -- the statistic of the FP32 tensor scale (QUADS §2.2 "FP4", second scaling
+ * level) alone: tscale[g] is zeroed, then tscale[g].amax = max |x| over group g's rows (exact).
+ * The other fields stay 0; nvfp4_quantize(..., amax_given = 1) fills them from amax.  With rows
+ * of one batch split over processes, each one's amax, combined by a maximum across processes,
+ * is the amax of the whole batch, so the quantization is that of the unsplit batch (the
+ * token-sharded path).  Arguments as for nvfp4_quantize.
+ */
+nvq_status nvfp4_amax(const void* x, int64_t rows, int64_t K, int64_t ldx, const int64_t* grp_off,
+                      const int64_t* grp_rows, int32_t groups, nvq_tensor_scale* tscale, void* stream);
 
 /*
  * rac_select_quantize -- channel selection of QUADS Eq. (24) and the second-pass quantization
@@ -303,11 +327,14 @@ nvq_status nvfp4_channel_major(int32_t groups, int64_t N, int64_t K, const uint8
  * a stable counting sort of the tokens * topk (token, slot) pairs by expert.
  *
  *   topk_ids  int32 [tokens][topk] expert ids in [0, groups).   topk_w  fp32 [tokens][topk] or NULL.
+ *             An id outside [0, groups) is not written out of bounds: its pair is left out of
+ *             the routing (row_of = -1, which moe_combine skips) and the device status word
+ *             records NVQ_ERR_ARG (nvq_device_status).
  *   grp_off   int64 [groups + 1] out: group g starts at row grp_off[g] (multiple of 128);
  *             grp_rows int64 [groups] out: number of routed rows of group g.
  *   row_src   int32 [capacity] out: routed row -> token * topk + slot (-1 on padding rows);
  *             inside a group rows are in ascending (token, slot) order.
- *   row_of    int64 [tokens * topk] out: routed row of each (token, slot).
+ *   row_of    int64 [tokens * topk] out: routed row of each (token, slot) (-1: left out).
  *   row_w     fp32 [capacity] out (NULL allowed): topk_w of the routed row, 0 on padding.
  *   capacity  >= moe_capacity(tokens, topk, groups).
  *   workspace device bytes >= moe_dispatch_workspace_size(tokens, topk, groups).
@@ -334,11 +361,13 @@ nvq_status moe_dispatch(const int32_t* topk_ids, const float* topk_w, int64_t to
  * Limit: moe_dispatch_workspace_size(tokens, topk, groups) must be <= 1 MiB; otherwise the call
  * returns NVQ_ERR_SHAPE, launches nothing, and nvq_last_error() names the sizes.  At 128
  * experts the limit is 2048 units of 256 (token, slot) pairs: 65536 tokens at top-8.  groups
- * must be in [1, 768].
+ * must be in [1, 1024], as for moe_dispatch.
  *
  * First call: on each device, the first call looks up the array's device address with
  * cudaGetSymbolAddress, with that device current, and caches it.  Make that first call before
- * any stream capture.  A failed lookup returns NVQ_ERR_CUDA.
+ * any stream capture.  A failed lookup returns NVQ_ERR_CUDA.  The cached address belongs to the
+ * device's primary context at that time: after cudaDeviceReset on a device, this entry must not
+ * be called again on that device in the same process.
  *
  * Sharing: all calls on one device share the array.  Nothing in it needs to start at zero,
  * because each call writes every word it later reads.  Calls that may overlap on the device
@@ -368,7 +397,8 @@ nvq_status nvfp4_gather_rows(const uint8_t* codes, int64_t ld_codes, const uint8
 
 /*
  * moe_combine -- out[t, :] = bf16( sum over slots s = 0..topk-1, in slot order, in fp32, of
- * y[row_of[t * topk + s], :] ).  y bf16 [capacity][ldy]; out bf16 [tokens][ldo].
+ * y[row_of[t * topk + s], :] ), slots with row_of < 0 left out.  y bf16 [capacity][ldy]; out
+ * bf16 [tokens][ldo].
  */
 nvq_status moe_combine(const void* y, int64_t ldy, const int64_t* row_of, int64_t tokens,
                        int32_t topk, int64_t hidden, void* out, int64_t ldo, void* stream);

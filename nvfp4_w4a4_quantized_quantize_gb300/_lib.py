@@ -25,6 +25,8 @@ _SIGS = {
     "nvq_sf_bytes": ([_I64, _I64], _I64),
     "nvq_sf_offset": ([_I64, _I64, _I64], _I64),
     "nvfp4_quantize": ([_P, _I64, _I64, _I64, _P, _P, _I32, _P, _I64, _P, _I64, _I32, _P, _P, _I32, _P], C.c_int),
+    "nvfp4_amax": ([_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P], C.c_int),
+    "nvq_check_block_scale_division": ([_P, _P], C.c_int),
     "rac_select_quantize": ([_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _I32, _P, _I64, _P, _I64, _P, _P], C.c_int),
     "weight_qdq": ([_P, _I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P, _I32, _P], C.c_int),
     "w4a4_rac_grouped_gemm": ([_I32, _P, _P, _I64, _P, _I64, _P, _I64, _P, _I32, _P, _I64, _P, _I64, _P, _I64, _I64,
@@ -143,7 +145,19 @@ def fp4_mma_rate(mmas_per_sm: int = 65536, with_cp: bool = False, stream=None) -
     return float(v.value)
 
 
+def check_block_scale_division(result, stream=None):
+    """result: CUDA uint32/int32 tensor of 2: [mismatch count, lowest mismatching bf16 pattern]."""
+    _check("nvq_check_block_scale_division", LIB.nvq_check_block_scale_division(_ptr(result), _stream(stream)))
+
+
 # --------------------------------------------------------------------------- the C ABI calls
+def nvfp4_amax(x, tscale, grp_off=None, grp_rows=None, groups=1, rows=None, K=None, stream=None):
+    rows = x.shape[0] if rows is None else rows
+    K = x.shape[1] if K is None else K
+    _check("nvfp4_amax", LIB.nvfp4_amax(_ptr(x), rows, K, x.stride(0), _ptr(grp_off), _ptr(grp_rows), groups,
+                                        _ptr(tscale), _stream(stream)))
+
+
 def nvfp4_quantize(x, codes, sf, sf_cols_, tscale, scores=None, grp_off=None, grp_rows=None, groups=1,
                    zero_pad=False, rows=None, K=None, amax_given=False, stream=None):
     rows = x.shape[0] if rows is None else rows

@@ -48,7 +48,7 @@ extern "C" const char* nvq_last_error(void) { return g_last_error; }
 
 extern "C" nvq_status nvq_set_wait_limit(uint64_t cycles)
 {
-    NVQ_CHECK_ARG(cycles >= 1000, NVQ_ERR_ARG, "nvq_set_wait_limit: limit below 1000 cycles");
+    NVQ_CHECK_ARG(cycles >= 1, NVQ_ERR_ARG, "nvq_set_wait_limit: the limit must be at least 1 cycle");
     g_wait_limit = cycles;
     set_error("");
     return NVQ_OK;

@@ -168,6 +168,15 @@ __device__ __forceinline__ float2 e2m1x2_value(uint32_t byte)
     return __half22float2(*reinterpret_cast<__half2*>(&h));
 }
 
+// The per-block encode factor fl(S_enc / sb), saturated at the largest finite binary32 value.
+// The quotient overflows only when S_enc itself was clamped there (tensor amax below
+// 2688 / FLT_MAX, about 7.9e-36) and sb < 1; saturating keeps every product x * e_b finite, so
+// x = 0 still encodes as a signed zero, as S_enc's own clamp does for the tensor scale.
+__device__ __forceinline__ float encode_factor(float s_enc, float sbv)
+{
+    return fminf(__fdiv_rn(s_enc, sbv), 3.4028234663852886e38f);
+}
+
 // Quantization of one 16-element block held as 8 bf16x2 words.  Returns the scale byte,
 // writes the 8 code bytes into code_lo / code_hi (element 2i in the low nibble of byte i).
 struct BlockOut {
@@ -192,7 +201,7 @@ __device__ __forceinline__ BlockOut quantize16(const float* v, float s_enc, floa
     float t = __fmul_rn(__fdiv_rn(amax_b, 6.0f), s_enc);
     o.sb = e4m3(t);
     float sbv = e4m3_value(o.sb);
-    o.e_b = (o.sb == 0) ? 0.0f : __fdiv_rn(s_enc, sbv);
+    o.e_b = (o.sb == 0) ? 0.0f : encode_factor(s_enc, sbv);
     o.d_b = __fmul_rn(sbv, s_dec);
     uint32_t c[8];
     if (o.sb == 0) {
@@ -255,10 +264,24 @@ __device__ __forceinline__ uint64_t score_term(float r, const ScoreScale& s)
     return (uint64_t)q * (uint64_t)q;
 }
 
-// Bounded mbarrier / flag waits record this in the device status word.
-__device__ __forceinline__ void report_timeout(DeviceStatus* st, int where)
+// The first error a kernel records in the device status word wins; `where` identifies the
+// site (a wait or a check).
+__device__ __forceinline__ void report_status(DeviceStatus* st, nvq_status code, int where)
 {
-    if (atomicCAS(&st->status, 0, (int)NVQ_ERR_TIMEOUT) == 0) atomicExch(&st->where, where);
+    if (atomicCAS(&st->status, 0, (int)code) == 0) atomicExch(&st->where, where);
+}
+
+// Bounded mbarrier / flag waits record this in the device status word.
+__device__ __forceinline__ void report_timeout(DeviceStatus* st, int where) { report_status(st, NVQ_ERR_TIMEOUT, where); }
+
+// Bound of the wait, after another wait of the CTA ran out, for the asynchronous copies it
+// already issued to land before it exits (they complete within microseconds; this bound does
+// not shrink with the configurable limit, so even a tiny limit never lets a CTA exit while a
+// copy into its shared memory is in flight).
+constexpr unsigned long long kDrainWaitCycles = 1ull << 26;
+__host__ __device__ __forceinline__ unsigned long long drain_limit(unsigned long long limit)
+{
+    return limit > kDrainWaitCycles ? limit : kDrainWaitCycles;
 }
 
 }  // namespace nvq

@@ -21,8 +21,13 @@ namespace nvq {
 static constexpr int kUnit = 256;
 static constexpr int kWarpsPerCta = 2;  // 256 CTAs for the 512 units of 131072 pairs: every SM busy
 
+// An expert id outside [0, G) is a caller error: the pair is left out of the routing (its
+// row_of entry is -1, which combine skips) and the device status word records NVQ_ERR_ARG.
+static constexpr int kWhereBadExpertId = 41;
+
 // Per-unit histogram of experts: counts[unit][G].
-__global__ void dispatch_hist_kernel(const int32_t* __restrict__ ids, int64_t n, int G, int32_t* __restrict__ counts)
+__global__ void dispatch_hist_kernel(const int32_t* __restrict__ ids, int64_t n, int G, int32_t* __restrict__ counts,
+                                     DeviceStatus* __restrict__ st)
 {
     extern __shared__ int32_t hist[];  // [kWarpsPerCta][G]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -33,7 +38,11 @@ __global__ void dispatch_hist_kernel(const int32_t* __restrict__ ids, int64_t n,
     const int64_t p0 = unit * kUnit;
     if (p0 >= n) return;
     const int64_t p1 = min(p0 + kUnit, n);
-    for (int64_t p = p0 + lane; p < p1; p += 32) atomicAdd(&h[ids[p]], 1);
+    for (int64_t p = p0 + lane; p < p1; p += 32) {
+        const int e = ids[p];
+        if ((unsigned)e < (unsigned)G) atomicAdd(&h[e], 1);
+        else report_status(st, NVQ_ERR_ARG, kWhereBadExpertId);
+    }
     __syncwarp();
     for (int e = lane; e < G; e += 32) counts[unit * G + e] = h[e];
 }
@@ -151,7 +160,9 @@ __global__ void dispatch_scatter_kernel(const int32_t* __restrict__ ids, const f
 #pragma unroll
     for (int q = 0; q < kPer; ++q) {
         const int64_t p = p0 + q * 32 + lane;
-        const bool valid = p < p1;
+        const bool in_id = (unsigned)ev[q] < (unsigned)G;  // the histogram kernel reported the others
+        if (p < p1 && !in_id) row_of[p] = -1;
+        const bool valid = p < p1 && in_id;
         const unsigned act = __ballot_sync(0xffffffffu, valid);
         const int e = ev[q];
         int rank = 0;
@@ -250,6 +261,7 @@ __global__ void combine_kernel(const __nv_bfloat16* __restrict__ y, int64_t ldy,
         for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
         for (int s = 0; s < topk; ++s) {
             const int64_t r = row_of[t * topk + s];
+            if (r < 0) continue;  // a pair dispatch left out (expert id out of range)
             uint4 w = __ldg(reinterpret_cast<const uint4*>(y + r * ldy + c));
             acc[0] = __fadd_rn(acc[0], bf16lo(w.x)); acc[1] = __fadd_rn(acc[1], bf16hi(w.x));
             acc[2] = __fadd_rn(acc[2], bf16lo(w.y)); acc[3] = __fadd_rn(acc[3], bf16hi(w.y));
@@ -296,13 +308,16 @@ extern "C" nvq_status moe_dispatch(const int32_t* topk_ids, const float* topk_w,
                   (long long)moe_capacity(tokens, topk, groups));
     NVQ_CHECK_ARG(workspace_bytes >= moe_dispatch_workspace_size(tokens, topk, groups), NVQ_ERR_SHAPE,
                   "moe_dispatch: workspace too small");
+    DeviceStatus* dstat = device_status_ptr();
+    NVQ_CHECK_ARG(dstat, NVQ_ERR_CUDA, "moe_dispatch: device status word unavailable");
     set_error("");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t n = tokens * topk;
     const int units = (int)((n + kUnit - 1) / kUnit);
     const int ctas = (units + kWarpsPerCta - 1) / kWarpsPerCta;
     int32_t* counts = static_cast<int32_t*>(workspace);
-    dispatch_hist_kernel<<<ctas, 32 * kWarpsPerCta, kWarpsPerCta * groups * sizeof(int32_t), st>>>(topk_ids, n, groups, counts);
+    dispatch_hist_kernel<<<ctas, 32 * kWarpsPerCta, kWarpsPerCta * groups * sizeof(int32_t), st>>>(topk_ids, n, groups, counts,
+                                                                                                   dstat);
     NVQ_LAUNCH_CHECK("dispatch_hist_kernel");
     dispatch_scan_kernel<<<groups, units >= 1024 ? 1024 : ((units + 31) / 32) * 32, 0, st>>>(counts, units, groups, grp_rows);
     NVQ_LAUNCH_CHECK("dispatch_scan_kernel");
@@ -421,9 +436,10 @@ extern "C" nvq_status moe_dispatch_static_scratch(const int32_t* topk_ids, const
                   "moe_dispatch_static_scratch: null pointer argument");
     NVQ_CHECK_ARG(tokens >= 1 && topk >= 1 && topk <= 64 && tokens * topk <= (1ll << 26), NVQ_ERR_SHAPE,
                   "moe_dispatch_static_scratch: tokens*topk outside [1, 2^26] or topk outside [1, 64]");
-    // groups <= 768 keeps the scatter kernel's shared histogram (8 warps x groups x 8 bytes) within
-    // the 48 KB a launch gets without an attribute call
-    NVQ_CHECK_ARG(groups >= 1 && groups <= 768, NVQ_ERR_SHAPE, "moe_dispatch_static_scratch: groups outside [1, 768]");
+    // the same group limit as moe_dispatch: the scatter kernel's shared table of group bases
+    // (kWarpsPerCta x groups x 8 bytes, 16 KB at 1024 groups) stays within the 48 KB a launch
+    // gets without an attribute call
+    NVQ_CHECK_ARG(groups >= 1 && groups <= 1024, NVQ_ERR_SHAPE, "moe_dispatch_static_scratch: groups outside [1, 1024]");
     NVQ_CHECK_ARG(capacity >= moe_capacity(tokens, topk, groups), NVQ_ERR_SHAPE,
                   "moe_dispatch_static_scratch: capacity %lld < moe_capacity() = %lld", (long long)capacity,
                   (long long)moe_capacity(tokens, topk, groups));
@@ -435,6 +451,8 @@ extern "C" nvq_status moe_dispatch_static_scratch(const int32_t* topk_ids, const
     int32_t* counts = nullptr;
     const nvq_status s = dispatch_scratch_ptr(&counts);
     if (s != NVQ_OK) return s;
+    DeviceStatus* dstat = device_status_ptr();
+    NVQ_CHECK_ARG(dstat, NVQ_ERR_CUDA, "moe_dispatch_static_scratch: device status word unavailable");
     set_error("");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t n = tokens * topk;
@@ -442,7 +460,8 @@ extern "C" nvq_status moe_dispatch_static_scratch(const int32_t* topk_ids, const
     const int ctas = (units + kWarpsPerCta - 1) / kWarpsPerCta;
     // every counts word the later kernels read is written by the histogram kernel of this call:
     // nothing in the scratch has to start at zero
-    dispatch_hist_kernel<<<ctas, 32 * kWarpsPerCta, kWarpsPerCta * groups * sizeof(int32_t), st>>>(topk_ids, n, groups, counts);
+    dispatch_hist_kernel<<<ctas, 32 * kWarpsPerCta, kWarpsPerCta * groups * sizeof(int32_t), st>>>(topk_ids, n, groups, counts,
+                                                                                                   dstat);
     NVQ_LAUNCH_CHECK("dispatch_hist_kernel");
     dispatch_scan_kernel<<<groups, units >= 1024 ? 1024 : ((units + 31) / 32) * 32, 0, st>>>(counts, units, groups, grp_rows);
     NVQ_LAUNCH_CHECK("dispatch_scan_kernel");

@@ -128,22 +128,41 @@ __device__ __forceinline__ bool q_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of the phase (try_wait may suspend the thread in hardware for a while).
+__device__ __forceinline__ bool q_test_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(sa32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// A bound shorter than this polls with test_wait, so that it is honoured to within a poll
+// instead of the hardware's suspend window of try_wait.
+constexpr unsigned long long kShortWaitCycles = 1ull << 20;
+
 // Bounded wait: false after recording a timeout, or (unless draining) as soon as another warp
 // of the CTA gave up.
 __device__ __forceinline__ bool q_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, DeviceStatus* st,
                                        unsigned long long limit, int where, bool draining = false)
 {
-    if (q_try_wait(bar, parity)) return true;
+    const unsigned long long bound = draining ? drain_limit(limit) : limit;
+    const bool poll = bound < kShortWaitCycles;
+    if (poll ? q_test_wait(bar, parity) : q_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
-        for (int i = 0; i < 32; ++i)
-            if (q_try_wait(bar, parity)) return true;
+        // the bound is checked before each round of polls, so that a limit of a few cycles
+        // runs out at the first wait that is not already complete
         if (!draining && *abort_flag) return false;
-        if ((unsigned long long)(clock64() - t0) > limit) {
+        if ((unsigned long long)(clock64() - t0) > bound) {
             report_timeout(st, where);
             *abort_flag = 1;
             return false;
         }
+        for (int i = 0; i < 32; ++i)
+            if (poll ? q_test_wait(bar, parity) : q_try_wait(bar, parity)) return true;
     }
 }
 
@@ -173,8 +192,13 @@ __device__ __forceinline__ float amax_block(const uint4& w0, const uint4& w1)
     return fmaxf(__low2float(r), __high2float(r));
 }
 
-// fl(a / 6) for a non-negative bf16 value a: q1 = fl(a * fl(1/6)), one FMA residual correction.
-// Checked exhaustively against IEEE division for every finite non-negative bf16 value.
+// fl(a / 6) for a non-negative bf16 value a, without a division: the quotient estimate
+// q1 = fl(a * fl(1/6)) is corrected once with fused multiply-adds, as in Markstein's
+// FMA-based division (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Develop. 34(1), 1990): the remainder r = a - 6 q1 is exact
+// in one FMA, and q1 + r * fl(1/6) rounds to the correctly rounded quotient.  That this holds
+// for every finite non-negative bf16 input is checked exhaustively against the IEEE division
+// __fdiv_rn by nvq_check_block_scale_division.
 __device__ __forceinline__ float div6_bf16(float a)
 {
     constexpr float kInv6 = 1.0f / 6.0f;
@@ -355,7 +379,7 @@ __global__ void __launch_bounds__(kQThreads, 1) quant_score_kernel(const QuantAr
         consumer_sync();
         if (tid < 128) {
             const float sbv = e4m3_value((uint32_t)tid);
-            eb_tab[tid] = (tid == 0 || tid == 127) ? 0.0f : __fdiv_rn(t.s_enc, sbv);
+            eb_tab[tid] = (tid == 0 || tid == 127) ? 0.0f : encode_factor(t.s_enc, sbv);
             db_tab[tid] = (tid == 127) ? 0.0f : __fmul_rn(sbv, t.s_dec);
         }
         consumer_sync();
@@ -487,6 +511,21 @@ __global__ void __launch_bounds__(kQThreads, 1) quant_score_kernel(const QuantAr
     }
 }
 
+// ------------------------------------------------------------------------ self-check
+// Every finite non-negative bf16 bit pattern (0x0000 .. 0x7f7f) through div6_bf16 and through
+// the IEEE division; out[0] counts the inputs whose results differ, out[1] keeps the lowest such
+// pattern (0xffffffff when there is none).
+__global__ void __launch_bounds__(256) div6_check_kernel(unsigned int* __restrict__ out)
+{
+    const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b > 0x7f7fu) return;
+    const float a = __uint_as_float(b << 16);
+    if (__float_as_uint(div6_bf16(a)) != __float_as_uint(__fdiv_rn(a, 6.0f))) {
+        atomicAdd(&out[0], 1u);
+        atomicMin(&out[1], b);
+    }
+}
+
 // ------------------------------------------------------------------------ host side
 static int sm_count()
 {
@@ -506,6 +545,19 @@ static cudaError_t launch_quant(int grid, cudaStream_t st, const QuantArgs& qa)
     return cudaGetLastError();
 }
 
+// amax: ~8 CTAs per SM, whole rows per CTA, atomically folded into ts[g].amax (zeroed before).
+static nvq_status launch_amax(const __nv_bfloat16* x, int64_t rows, int64_t K, int64_t ldx, Groups gr,
+                              nvq_tensor_scale* ts, int sms, cudaStream_t st)
+{
+    const int64_t want = (int64_t)sms * 8;
+    int64_t rpc = (rows + want - 1) / want;
+    if (rpc < 1) rpc = 1;
+    const int grid = (int)((rows + rpc - 1) / rpc);
+    amax_kernel<<<grid, kAmaxThreads, 0, st>>>(x, ldx, (int)K, gr, rpc, ts);
+    NVQ_LAUNCH_CHECK("amax_kernel");
+    return NVQ_OK;
+}
+
 nvq_status quantize_impl(const void* x, int64_t rows, int64_t K, int64_t ldx, Groups gr, uint8_t* codes,
                          int64_t ld_codes, uint8_t* sf, int64_t sf_cols, int zero_pad, nvq_tensor_scale* ts,
                          uint64_t* scores, void* w_hat, int w_hat_dtype, cudaStream_t st, bool amax_given = false)
@@ -521,14 +573,10 @@ nvq_status quantize_impl(const void* x, int64_t rows, int64_t K, int64_t ldx, Gr
         if (e != cudaSuccess) return cuda_status(e, "cudaMemsetAsync(scores)");
     }
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-    // amax: ~8 CTAs per SM, whole rows per CTA (skipped when the producer of x computed it)
+    // amax (skipped when the producer of x computed it)
     if (!amax_given) {
-        const int64_t want = (int64_t)sms * 8;
-        int64_t rpc = (rows + want - 1) / want;
-        if (rpc < 1) rpc = 1;
-        const int grid = (int)((rows + rpc - 1) / rpc);
-        amax_kernel<<<grid, kAmaxThreads, 0, st>>>(xb, ldx, (int)K, gr, rpc, ts);
-        NVQ_LAUNCH_CHECK("amax_kernel");
+        const nvq_status s = launch_amax(xb, rows, K, ldx, gr, ts, sms, st);
+        if (s != NVQ_OK) return s;
     }
     QuantArgs qa;
     qa.x = xb;
@@ -606,4 +654,36 @@ extern "C" nvq_status weight_qdq(const void* w, int32_t groups, int64_t N, int64
     set_error("");
     return quantize_impl(w, (int64_t)groups * N, K, ldw, gr, codes, ld_codes, sf, sf_cols, 1, tscale, nullptr, w_hat,
                          w_hat_dtype, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" nvq_status nvfp4_amax(const void* x, int64_t rows, int64_t K, int64_t ldx, const int64_t* grp_off,
+                                 const int64_t* grp_rows, int32_t groups, nvq_tensor_scale* tscale, void* stream)
+{
+    NVQ_CHECK_ARG(x && tscale, NVQ_ERR_ARG, "nvfp4_amax: null pointer argument");
+    NVQ_CHECK_ARG(rows >= 1 && rows <= (1ll << 24), NVQ_ERR_SHAPE, "nvfp4_amax: rows=%lld outside [1, 2^24]", (long long)rows);
+    NVQ_CHECK_ARG(K >= 16 && K <= 8192 && K % 16 == 0, NVQ_ERR_SHAPE, "nvfp4_amax: K=%lld must be a multiple of 16 in [16, 8192]", (long long)K);
+    NVQ_CHECK_ARG(groups >= 1 && groups <= 4096, NVQ_ERR_SHAPE, "nvfp4_amax: groups=%d outside [1, 4096]", groups);
+    NVQ_CHECK_ARG(grp_off || groups == 1 || rows % groups == 0, NVQ_ERR_SHAPE, "nvfp4_amax: rows not divisible by groups");
+    NVQ_CHECK_ARG(ldx >= K && ldx % 8 == 0, NVQ_ERR_ALIGN, "nvfp4_amax: ldx=%lld must be >= K and a multiple of 8", (long long)ldx);
+    NVQ_CHECK_ARG(aligned(x, 16), NVQ_ERR_ALIGN, "nvfp4_amax: x must be 16-byte aligned");
+    set_error("");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = cudaMemsetAsync(tscale, 0, sizeof(nvq_tensor_scale) * groups, st);
+    if (e != cudaSuccess) return cuda_status(e, "cudaMemsetAsync(tscale)");
+    return launch_amax(static_cast<const __nv_bfloat16*>(x), rows, K, ldx, Groups{grp_off, grp_rows, groups, rows}, tscale,
+                       sm_count(), st);
+}
+
+extern "C" nvq_status nvq_check_block_scale_division(uint32_t* result, void* stream)
+{
+    NVQ_CHECK_ARG(result, NVQ_ERR_ARG, "nvq_check_block_scale_division: null result pointer");
+    NVQ_CHECK_ARG(aligned(result, 4), NVQ_ERR_ALIGN, "nvq_check_block_scale_division: result must be 4-byte aligned");
+    set_error("");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(result, 0, sizeof(uint32_t), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(result + 1, 0xff, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return cuda_status(e, "cudaMemsetAsync(result)");
+    div6_check_kernel<<<(0x7f80 + 255) / 256, 256, 0, st>>>(reinterpret_cast<unsigned int*>(result));
+    NVQ_LAUNCH_CHECK("div6_check_kernel");
+    return NVQ_OK;
 }

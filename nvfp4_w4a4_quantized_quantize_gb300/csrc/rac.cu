@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(512) act_tail_kernel(const __nv_bfloat16* __re
     const float s_enc0 = ts[g0].s_enc, s_dec0 = ts[g0].s_dec;
     for (int e = tid; e < 128; e += blockDim.x) {
         const float sbv = e4m3_value((uint32_t)e);
-        eb_tab[e] = (e == 0 || e == 127) ? 0.0f : __fdiv_rn(s_enc0, sbv);
+        eb_tab[e] = (e == 0 || e == 127) ? 0.0f : encode_factor(s_enc0, sbv);
         db_tab[e] = (e == 127) ? 0.0f : __fmul_rn(sbv, s_dec0);
     }
     const bool sel_smem = k <= 512;  // larger channel sets are read from global memory
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(512) act_tail_kernel(const __nv_bfloat16* __re
                 d_b = db_tab[sb[i]];
             } else {
                 const float sbv = e4m3_value(sb[i]);
-                e_b = sb[i] == 0 ? 0.0f : __fdiv_rn(s_enc, sbv);
+                e_b = sb[i] == 0 ? 0.0f : encode_factor(s_enc, sbv);
                 d_b = __fmul_rn(sbv, s_dec);
             }
             const uint32_t code = e2m1x2(__fmul_rn(xv[i], e_b), 0.0f) & 0xfu;  // e_b 0: +-0 keeps the sign
@@ -488,7 +488,7 @@ __global__ void __launch_bounds__(kRowThreads)
         const float sbv = e4m3_value(sb);
         float* dst = rt_smem + (size_t)r * stride + padded_ch(16 * b);
         if constexpr (kResidual) {
-            const float e_b = (sb == 0 || sb == 127) ? 0.0f : __fdiv_rn(ts[g].s_enc, sbv);
+            const float e_b = (sb == 0 || sb == 127) ? 0.0f : encode_factor(ts[g].s_enc, sbv);
             const float d_b = (sb == 127) ? 0.0f : __fmul_rn(sbv, ts[g].s_dec);
             const uint4* xp = reinterpret_cast<const uint4*>(x + row * ldx + 16 * b);
             const uint4 v0 = __ldg(xp), v1 = __ldg(xp + 1);

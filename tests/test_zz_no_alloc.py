@@ -52,7 +52,8 @@ def _assert_same(ref, got):
 
 
 def test_static_scratch_dispatch_matches_workspace_dispatch_twice(L):
-    # call 1: the prefill routing at 8192 tokens (Zipf, 128 experts, top-8): 256 KiB of scratch
+    # call 1: the prefill routing at 8192 tokens (Zipf, 128 experts, top-8): 256 units of 256
+    # (token, slot) pairs x 128 experts x 4 bytes = 128 KiB of scratch
     ids1, w1 = wl.routing_zipf(8192, 128, 8, 1.1, seed=31)
     ref1, got1 = _both(L, ids1, w1, 128)
     _assert_same(ref1, got1)
@@ -75,5 +76,28 @@ def test_static_scratch_dispatch_refuses_oversize(L):
         L.moe_dispatch_static_scratch(ids, None, E, out["grp_off"], out["grp_rows"], out["row_src"], out["row_of"],
                                       out["row_w"])
     assert ei.value.status == 2 and "static array" in str(ei.value)
+    torch.cuda.synchronize()
+    assert int(out["grp_off"][0]) == -7  # nothing was launched
+
+
+def test_static_scratch_dispatch_at_exactly_the_limit(L):
+    # 65536 tokens at top-8 over 128 experts: 2048 units x 128 x 4 bytes = 1 MiB, the whole array
+    T, topk, E = 65536, 8, 128
+    assert L.moe_dispatch_workspace_size(T, topk, E) == (1 << 20)
+    ids, w = wl.routing_zipf(T, E, topk, 1.1, seed=33)
+    ref, got = _both(L, ids, w, E)
+    _assert_same(ref, got)
+    assert np.array_equal(got["grp_rows"].cpu().numpy(), np.bincount(ids.ravel(), minlength=E))
+
+
+def test_static_scratch_dispatch_refuses_too_many_groups(L):
+    T, topk, E = 64, 2, 1025  # one group more than moe_dispatch accepts
+    dev = "cuda"
+    ids = torch.zeros(T, topk, dtype=torch.int32, device=dev)
+    out = _outputs(L, T, topk, E, L.moe_capacity(T, topk, E), dev)
+    with pytest.raises(L.NvqError) as ei:
+        L.moe_dispatch_static_scratch(ids, None, E, out["grp_off"], out["grp_rows"], out["row_src"], out["row_of"],
+                                      out["row_w"])
+    assert ei.value.status == 2 and "groups" in str(ei.value)
     torch.cuda.synchronize()
     assert int(out["grp_off"][0]) == -7  # nothing was launched
