@@ -34,7 +34,7 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".{os.getpid()}.tmp"
         subprocess.check_call(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
-                               "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"])
+                               "-fPIC", "-shared", _SRC, "-o", tmp, "-lm", "-lpthread"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -92,12 +92,23 @@ def lib():
             "oracle_fp8_encode": ([C.c_double], C.c_uint8),
             "oracle_fp8_quantize": ([P, I64, I64, I64, I32, P, I64, P, I64], None),
             "oracle_fp8_dequantize": ([P, I64, P, I64, I64, I64, I32, P, I64], None),
+            "oracle_set_threads": ([C.c_int], None),
+            "oracle_hardware_threads": ([], C.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(_lib, name)
             f.argtypes = args
             f.restype = res
     return _lib
+
+
+def set_threads(n: int) -> None:
+    """Host threads the GEMM's output pairs are spread over (the result does not depend on it)."""
+    lib().oracle_set_threads(int(n))
+
+
+def hardware_threads() -> int:
+    return int(lib().oracle_hardware_threads())
 
 
 def _p(a: np.ndarray):
