@@ -45,8 +45,10 @@ constexpr uint32_t kSBO = 8 * kRowBytes;    // stride between 8-row core-matrix 
 constexpr int kABytes = kBM * kRowBytes;    // 16384
 constexpr int kBBytes = kBN * kRowBytes;    // 32768
 constexpr int kMmaPerStage = 4;             // 32 bytes of every tile row per MMA
-constexpr int kThreads = 448;  // warp 0 TMA, warp 1 MMA, warps 2-5 scale staging, warps 6-13 epilogue
+constexpr int kThreads = 512;  // warps 0, 14, 15 TMA, warp 1 MMA, warps 2-5 scale staging, warps 6-13 epilogue
 constexpr int kFirstEpiWarp = 6;
+constexpr int kProducers = 3;       // one TMA box per stage each: A, weight rows half 0, half 1
+constexpr int kProdWarpB0 = 14, kProdWarpB1 = 15;
 constexpr int kEpiThreads = 256;
 constexpr int kMaxGroups = 512;
 constexpr uint32_t kTmemCols = 512;
@@ -392,8 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 {
     using GF = Geo<F>;
     constexpr int kStageBytes = GF::kStageBytes;
-    constexpr int kSFABytes = GF::kSFABytes, kSFBBytes = GF::kSFBBytes;
     constexpr int kSfAtoms = GF::kSfAtoms;
+    constexpr int kSFABytes = GF::kSFABytes, kSFBBytes = GF::kSFBBytes;
     constexpr uint32_t kSFColsPerStage = GF::kSFColsPerStage;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kStages], sf_bar[kStages], empty_bar[kStages], acc_full, acc_empty, drain_bar;
@@ -415,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&full_bar[i], 1);
+            mbar_init(&full_bar[i], kProducers);  // each producer's box
             mbar_init(&sf_bar[i], 4);  // the four scale-staging warps
             mbar_init(&empty_bar[i], 1);  // the MMA commit releases a stage
         }
@@ -465,44 +467,43 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int num_kt = (a.ktot + F::kElemsPerStage - 1) / F::kElemsPerStage;
     volatile int* abrt = &abort_flag;
 
-    if (warp == 0) {
-        // ---------------- producer: A and B code tiles by TMA (weights L2 evict-last: every
-        // 128-row block of the group re-reads them), scale atoms by bulk copies.
+    const int prod = warp == 0 ? 0 : (warp == kProdWarpB0 ? 1 : (warp == kProdWarpB1 ? 2 : -1));
+    if (prod >= 0) {
+        // ---------------- producers: the TMA engine sustains more per SM when its requests come
+        // from several warps, so each stage is loaded by three: warp 0 the A tile and its scale
+        // atoms, warps 14 and 15 one 128-row half of the weight tile each (L2 evict-last: every
+        // 128-row block of the group re-reads them) and its scale atoms.
         uint64_t pol_keep;
         asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
         int stage = 0;
         uint32_t phase = 0, issued = 0;
         for (int64_t t = blockIdx.x; t < total_tiles && !*abrt; t += gridDim.x) {
             const Tile T = tile_of(t, n_tiles, tab, G);
-            int64_t brow0, brow1;
-            if (a.epilogue == NVQ_EPI_SWIGLU) {
-                brow0 = (int64_t)T.g * a.N + (int64_t)T.nt * (kBN / 2);
-                brow1 = brow0 + a.N / 2;
-            } else {
-                brow0 = (int64_t)T.g * a.N + (int64_t)T.nt * kBN;
-                brow1 = brow0 + kBN / 2;
-            }
+            int64_t brow;
+            if (a.epilogue == NVQ_EPI_SWIGLU)
+                brow = (int64_t)T.g * a.N + (int64_t)T.nt * (kBN / 2) + (prod == 2 ? a.N / 2 : 0);
+            else
+                brow = (int64_t)T.g * a.N + (int64_t)T.nt * kBN + (prod == 2 ? kBN / 2 : 0);
             if (lane == 0) {
                 for (int kt = 0; kt < num_kt; ++kt) {
                     if (!mbar_wait(&empty_bar[stage], phase ^ 1, a, abrt, 1)) break;
                     const int kleft = a.ktot - kt * F::kElemsPerStage;
                     const int n_mma = kleft >= F::kElemsPerStage ? kMmaPerStage : (kleft + F::kMmaK - 1) / F::kMmaK;
-                    const int n_atoms = GF::atoms_for(n_mma);
+                    const uint32_t sf_bytes = 512u * GF::atoms_for(n_mma);
                     uint8_t* sA = smem + stage * kStageBytes;
-                    uint8_t* sB = sA + kABytes;
-                    uint8_t* sSFA = sB + kBBytes;
-                    uint8_t* sSFB = sSFA + kSFABytes;
-                    mbar_expect_tx(&full_bar[stage], kABytes + kBBytes + 3u * 512u * n_atoms);
-                    // the A tile and its scales; the two 128-row halves of the weight tile and theirs
-                    tma_load_2d(sA, &tmap_a, kt * kRowBytes, T.row0, &full_bar[stage]);
-                    const uint8_t* srcA = a.a_sf + ((int64_t)(T.row0 >> 7) * (a.a_sf_cols >> 2) + kt * kSfAtoms) * 512;
-                    bulk_load(sSFA, srcA, 512u * n_atoms, &full_bar[stage]);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int64_t brow = h ? brow1 : brow0;
-                        tma_load_2d_hint(sB + h * (kBBytes / 2), &tmap_b, kt * kRowBytes, (int)brow, &full_bar[stage], pol_keep);
-                        const uint8_t* srcB = a.b_sf + ((brow >> 7) * (a.b_sf_cols >> 2) + kt * kSfAtoms) * 512;
-                        bulk_load(sSFB + h * (kSFBBytes / 2), srcB, 512u * n_atoms, &full_bar[stage]);
+                    if (prod == 0) {
+                        mbar_expect_tx(&full_bar[stage], kABytes + sf_bytes);
+                        tma_load_2d(sA, &tmap_a, kt * kRowBytes, T.row0, &full_bar[stage]);
+                        bulk_load(sA + kABytes + kBBytes,
+                                  a.a_sf + ((int64_t)(T.row0 >> 7) * (a.a_sf_cols >> 2) + kt * kSfAtoms) * 512, sf_bytes,
+                                  &full_bar[stage]);
+                    } else {
+                        const int h = prod - 1;
+                        mbar_expect_tx(&full_bar[stage], kBBytes / 2 + sf_bytes);
+                        tma_load_2d_hint(sA + kABytes + h * (kBBytes / 2), &tmap_b, kt * kRowBytes, (int)brow, &full_bar[stage],
+                                         pol_keep);
+                        bulk_load(sA + kABytes + kBBytes + kSFABytes + h * (kSFBBytes / 2),
+                                  a.b_sf + ((brow >> 7) * (a.b_sf_cols >> 2) + kt * kSfAtoms) * 512, sf_bytes, &full_bar[stage]);
                     }
                     ++issued;
                     if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -511,8 +512,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             __syncwarp();
         }
         if (*abrt && lane == 0) {
-            // let the copies still in flight land before the CTA can exit: the last issue
-            // on each stage is the phase (phase ^ 1) for stages before `stage`, else `phase`
+            // let this producer's copies still in flight land before the CTA can exit: its last
+            // issue on each stage is the phase (phase ^ 1) for stages before `stage`, else `phase`
+            // (a phase another producer left incomplete only makes this wait use its bound)
             for (int s = 0; s < kStages; ++s)
                 if (issued > (uint32_t)s) mbar_wait(&full_bar[s], s < stage ? phase : phase ^ 1, a, abrt, 11, true);
         }
