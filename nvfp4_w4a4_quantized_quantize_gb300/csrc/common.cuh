@@ -271,6 +271,45 @@ __device__ __forceinline__ void report_status(DeviceStatus* st, nvq_status code,
     if (atomicCAS(&st->status, 0, (int)code) == 0) atomicExch(&st->where, where);
 }
 
+// ------------------------------------------------------------------ packed fp32 pairs
+// Two binary32 values in one 64-bit register (low word = first element), for the paired FP32
+// instructions of sm_100+ (one instruction, two independently rounded results).
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// bf16x2 word -> fp32 pair (exact).
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) { return f2pack(bf16lo(w), bf16hi(w)); }
+
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
 // Bounded mbarrier / flag waits record this in the device status word.
 __device__ __forceinline__ void report_timeout(DeviceStatus* st, int where) { report_status(st, NVQ_ERR_TIMEOUT, where); }
 

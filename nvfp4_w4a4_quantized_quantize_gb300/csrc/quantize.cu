@@ -216,6 +216,63 @@ __device__ __forceinline__ void score_acc(unsigned long long& acc, float r, floa
     acc += (unsigned long long)q * q;  // one wide multiply-add
 }
 
+// max(|a|, |b|) of two bf16x2 words per half (exact; the sign bits of the result are the
+// XOR of the inputs' and are cleared by the caller).
+__device__ __forceinline__ uint32_t max_abs_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Block amax of 16 bf16 values held as 8 bf16x2 words, as an fp32 value (exact).
+__device__ __forceinline__ float block_amax_words(const uint32_t* w)
+{
+    const uint32_t m = max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(w[0], w[1]), max_abs_bf16x2(w[2], w[3])),
+                                      max_abs_bf16x2(max_abs_bf16x2(w[4], w[5]), max_abs_bf16x2(w[6], w[7]))) &
+                       0x7fff7fffu;
+    return fmaxf(bf16lo(m), bf16hi(m));
+}
+
+// Eight fp32 values (four pairs, element 2i in the low word of pair i) -> eight E2M1 codes in
+// one word, element 2i in the low nibble of byte i (round to nearest even, saturate, sign kept).
+__device__ __forceinline__ uint32_t e2m1x8(const uint64_t* yp)
+{
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f2unpack(yp[i], y[2 * i], y[2 * i + 1]);
+    uint32_t w;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(w)
+        : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]), "f"(y[4]), "f"(y[5]), "f"(y[6]), "f"(y[7]));
+    return w;
+}
+
+// Byte j of a code word -> the two E2M1 values as an fp32 pair (exact).
+__device__ __forceinline__ uint64_t e2m1_byte_to_f2(uint32_t w, int j)
+{
+    uint32_t h;
+    switch (j) {
+    case 0: asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b0;\n\t}" : "=r"(h) : "r"(w)); break;
+    case 1: asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b1;\n\t}" : "=r"(h) : "r"(w)); break;
+    case 2: asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b2;\n\t}" : "=r"(h) : "r"(w)); break;
+    default: asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b3;\n\t}" : "=r"(h) : "r"(w)); break;
+    }
+    const float2 v = __half22float2(*reinterpret_cast<__half2*>(&h));
+    return f2pack(v.x, v.y);
+}
+
+// acc += q^2 for a signed q with |q| < 2^19: one 32 x 32 -> 64-bit multiply-add.
+__device__ __forceinline__ void score_acc_signed(unsigned long long& acc, int q)
+{
+    asm("mad.wide.s32 %0, %1, %1, %0;" : "+l"(acc) : "r"(q));
+}
+
 struct QuantArgs {
     const __nv_bfloat16* x;
     int64_t ldx;
@@ -410,47 +467,59 @@ __global__ void __launch_bounds__(kQThreads, 1) quant_score_kernel(const QuantAr
                         if (bc >= nb) continue;
                         const uint4* src = reinterpret_cast<const uint4*>(stage + rr * row_bytes + bc * 32);
                         const uint4 w0 = src[0], w1 = src[1];
-                        const float v[16] = {bf16lo(w0.x), bf16hi(w0.x), bf16lo(w0.y), bf16hi(w0.y),
-                                             bf16lo(w0.z), bf16hi(w0.z), bf16lo(w0.w), bf16hi(w0.w),
-                                             bf16lo(w1.x), bf16hi(w1.x), bf16lo(w1.y), bf16hi(w1.y),
-                                             bf16lo(w1.z), bf16hi(w1.z), bf16lo(w1.w), bf16hi(w1.w)};
-                        const uint32_t sb = e4m3(__fmul_rn(div6_bf16(amax_block(w0, w1)), t.s_enc));
+                        const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                        const uint32_t sb = e4m3(__fmul_rn(div6_bf16(block_amax_words(wv)), t.s_enc));
+                        // sb == 0: e_b = 0 turns every x into a signed zero (code 0x0 / 0x8) and
+                        // d_b = 0 makes the dequantized value 0, so no branch is needed
                         const float e_b = eb_tab[sb], d_b = db_tab[sb];
-                        uint32_t c[8];
-                        if (sb == 0) {
+                        const uint64_t e2 = f2pack(e_b, e_b);
+                        uint64_t xp[8], yp[8];
 #pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                c[i] = ((__float_as_uint(v[2 * i]) >> 28) & 0x8u) | ((__float_as_uint(v[2 * i + 1]) >> 24) & 0x80u);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) c[i] = e2m1x2(__fmul_rn(v[2 * i], e_b), __fmul_rn(v[2 * i + 1], e_b));
+                        for (int i = 0; i < 8; ++i) {
+                            xp[i] = bf16x2_to_f2(wv[i]);
+                            yp[i] = f2mul(xp[i], e2);
                         }
-                        const uint32_t lo = __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
-                        const uint32_t hi = __byte_perm(__byte_perm(c[4], c[5], 0x0040), __byte_perm(c[6], c[7], 0x0040), 0x5410);
+                        const uint32_t lo = e2m1x8(yp), hi = e2m1x8(yp + 4);
                         *reinterpret_cast<uint2*>(crow + bc * 8) = make_uint2(lo, hi);
                         qa.sf[sfrow + (bc >> 2) * 512 + (bc & 3)] = (uint8_t)sb;
                         if (kScores || kWhat) {
-                            float dq[16];
+                            const uint64_t d2 = f2pack(d_b, d_b);
+                            uint64_t dq[8];  // fl(V[q] * d_b), pairs
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const float2 vv = e2m1x2_value(c[i]);
-                                dq[2 * i] = __fmul_rn(vv.x, d_b);
-                                dq[2 * i + 1] = __fmul_rn(vv.y, d_b);
-                            }
+                            for (int i = 0; i < 8; ++i) dq[i] = f2mul(e2m1_byte_to_f2(i < 4 ? lo : hi, i & 3), d2);
                             if (kScores) {
                                 if (!ss.split) {
+                                    // rint(r * sc) by the magic-number addition: 1.5 * 2^23 is even, so
+                                    // the sum rounds to 1.5 * 2^23 + rint(r * sc) (ties to even) and its
+                                    // bit pattern minus that of 1.5 * 2^23 is the signed integer, whose
+                                    // square is rint(|r| * sc)^2
+                                    const uint64_t sc2 = f2pack(ss.sc_a, ss.sc_a);
+                                    const uint64_t m2 = f2pack(12582912.0f, 12582912.0f);
 #pragma unroll
-                                    for (int i = 0; i < 16; ++i) score_acc(part[p][i], __fsub_rn(v[i], dq[i]), ss.sc_a);
+                                    for (int i = 0; i < 8; ++i) {
+                                        float t0, t1;
+                                        f2unpack(f2fma(f2sub(xp[i], dq[i]), sc2, m2), t0, t1);
+                                        score_acc_signed(part[p][2 * i], __float_as_int(t0) - 0x4B400000);
+                                        score_acc_signed(part[p][2 * i + 1], __float_as_int(t1) - 0x4B400000);
+                                    }
                                 } else {
 #pragma unroll
-                                    for (int i = 0; i < 16; ++i) part[p][i] += score_term(__fsub_rn(v[i], dq[i]), ss);
+                                    for (int i = 0; i < 8; ++i) {
+                                        float x0, x1, q0, q1;
+                                        f2unpack(xp[i], x0, x1);
+                                        f2unpack(dq[i], q0, q1);
+                                        part[p][2 * i] += score_term(__fsub_rn(x0, q0), ss);
+                                        part[p][2 * i + 1] += score_term(__fsub_rn(x1, q1), ss);
+                                    }
                                 }
                             }
                             if (kWhat == 1) {
                                 uint32_t pk[8];
 #pragma unroll
                                 for (int i = 0; i < 8; ++i) {
-                                    __nv_bfloat162 h2 = __floats2bfloat162_rn(dq[2 * i], dq[2 * i + 1]);
+                                    float q0, q1;
+                                    f2unpack(dq[i], q0, q1);
+                                    __nv_bfloat162 h2 = __floats2bfloat162_rn(q0, q1);
                                     pk[i] = *reinterpret_cast<uint32_t*>(&h2);
                                 }
                                 uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(qa.w_hat) + grow * (int64_t)K + bc * 16);
@@ -459,7 +528,12 @@ __global__ void __launch_bounds__(kQThreads, 1) quant_score_kernel(const QuantAr
                             } else if (kWhat == 2) {
                                 float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(qa.w_hat) + grow * (int64_t)K + bc * 16);
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) dst[i] = make_float4(dq[4 * i], dq[4 * i + 1], dq[4 * i + 2], dq[4 * i + 3]);
+                                for (int i = 0; i < 4; ++i) {
+                                    float a0, a1, b0, b1;
+                                    f2unpack(dq[2 * i], a0, a1);
+                                    f2unpack(dq[2 * i + 1], b0, b1);
+                                    dst[i] = make_float4(a0, a1, b0, b1);
+                                }
                             }
                         }
                     }
