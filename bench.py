@@ -107,7 +107,7 @@ def job_throughput(units_per_rank_step: float, world: int, max_ms_per_step: floa
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi sampling (every 50 ms) over the timed region."""
+    """nvidia-smi sampling (every 20 ms) over the timed region."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -123,7 +123,7 @@ class ClockSampler:
         os.close(fd)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -205,10 +205,12 @@ def run_ours(args, world, rank, local):
     # the whole layer as one CUDA graph (no host synchronisation inside a forward), with the
     # per-kernel events recorded inside the graph
     # timing events recorded inside the graph must be external (event-record nodes)
+    # only the two grouped GEMMs carry timing events in the timed graph (each event is a graph
+    # node); the per-stage breakdown is taken from a separate graph after the timed region
     try:
         graph_events = {name: (torch.cuda.Event(enable_timing=True, external=True),
                                torch.cuda.Event(enable_timing=True, external=True))
-                        for name in ("quant_rac_tokens", "gemm_gate_up", "gemm_down")}
+                        for name in ("gemm_gate_up", "gemm_down")}
     except TypeError:  # torch without external events: per-kernel times come from an eager pass
         graph_events = None
     graph = None
@@ -257,7 +259,10 @@ def run_ours(args, world, rank, local):
             # graph events are re-recorded by every replay: read them before the next one
             ends[i].synchronize()
             for k2, (e0, e1) in ev_lists[i].items():
-                kernel_ms.setdefault(k2, []).append(e0.elapsed_time(e1))
+                try:
+                    kernel_ms.setdefault(k2, []).append(e0.elapsed_time(e1))
+                except (RuntimeError, ValueError):  # a stage this layer does not run
+                    pass
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
     barrier(world)
@@ -276,7 +281,7 @@ def run_ours(args, world, rank, local):
         return sum(v) / len(v) if v else None
 
     t_gu, t_dn = avg("gemm_gate_up"), avg("gemm_down")
-    t_q1 = avg("quant_rac_tokens")
+    stage_ms_rac = stage_times(lambda ev: layer.forward(x, ids_d, tw_d, out, events=ev), flush, max(5, min(args.steps, 50)))
     rows_total = T * topk
     flop_gu = 2.0 * rows_total * (2 * I) * (H + k)
     flop_dn = 2.0 * rows_total * H * (I + k)
@@ -312,8 +317,14 @@ def run_ours(args, world, rank, local):
     act = act_quant_bench(args, L, wl, dev, flush, peaks) if rank == 0 else None
     # ---- baseline rows: the same layer without RAC (k = 0), and the expert GEMMs in bf16
     base = baseline_rows(args, layer, x, ids_d, tw_d, w13_bits, w2_bits, cfg, dev, flush, ms_per_step,
-                         t_gu, t_dn) if rank == 0 else None
+                         t_gu, t_dn, stage_ms_rac) if rank == 0 else None
     trainer = trainer_rows(args, L, dev, flush, peaks) if rank == 0 else None
+    del layer
+    torch.cuda.empty_cache()
+    # ---- the other workloads of the measurement plan: the dense RAC GEMM and the decode step
+    dense = dense_rows(args, L, wl, dev, flush, peaks) if rank == 0 else None
+    decode = decode_rows(args, L, wl, dev, flush, peaks) if rank == 0 else None
+    probe = mma_probe_row(L) if rank == 0 else None
 
     result = {
         "metric": METRIC,
@@ -332,7 +343,8 @@ def run_ours(args, world, rank, local):
                    "intermediate": I, "rac_k": k, "parallelism": f"dp{world} (independent batches)",
                    "l2": "flushed (512 MiB write) before every timed step"},
         "gemm_tflops": round((flop_gu + flop_dn) / (ms_per_step * 1e-3) / 1e12, 2),
-        "kernel_ms": {"gemm_gate_up": t_gu, "gemm_down": t_dn, "quant_rac_tokens": t_q1},
+        "kernel_ms": {"gemm_gate_up": round(t_gu, 4), "gemm_down": round(t_dn, 4),
+                      "timing": "CUDA events around each GEMM inside the timed graph replays"},
         "roofline": {"kernel": "gemm_kernel (gate/up, SwiGLU epilogue)", "bound": "tensor",
                      "achieved": round(ach_gu, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                      "frac": round(ach_gu / fp4_peak, 4), "traffic": gemm_traffic_per_launch("gate_up"),
@@ -349,6 +361,12 @@ def run_ours(args, world, rank, local):
         result["baselines"] = base
     if trainer:
         result["trainer_side"] = trainer
+    if dense:
+        result["dense_rac_gemm"] = dense
+    if decode:
+        result["moe_decode"] = decode
+    if probe:
+        result["mma_probe"] = probe
     return result, (x_bits, ids, tw, w13_bits, w2_bits, cfg)
 
 
@@ -357,7 +375,162 @@ def _time_replays(fn, flush, steps, warmup):
     return time_graph_replays(fn, flush, steps, warmup)
 
 
-def baseline_rows(args, layer, x, ids_d, tw_d, w13_bits, w2_bits, cfg, dev, flush, ms_rac, t_gu, t_dn):
+def clocked(fn, flush, min_s: float = 0.35, warmup: int = 3):
+    """Median ms of CUDA-graph replays of fn (L2 flushed before each, outside the events), replayed
+    for at least min_s seconds so that the clock sampler running meanwhile takes several samples."""
+    import torch
+    t_est = _time_replays(fn, flush, 3, 1)
+    per_iter_s = (t_est + 0.12) * 1e-3  # + the 512 MiB flush write
+    steps = max(5, int(min_s / per_iter_s))
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    ms = _time_replays(fn, flush, steps, warmup)
+    return ms, sampler.stop()
+
+
+def stage_times(fwd, flush, steps: int):
+    """Mean per-stage ms of a layer forward captured in a CUDA graph with external timing events
+    (fwd(events) runs the forward with the events dict), L2 flushed before each replay."""
+    import torch
+    from nvfp4_w4a4_quantized_quantize_gb300.layers import MOE_STAGES
+    try:
+        ev = {n: (torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+              for n in MOE_STAGES}
+    except TypeError:
+        return {}
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        fwd(None)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            fwd(ev)
+    torch.cuda.current_stream().wait_stream(cap)
+    used = set()
+    acc = {}
+    for i in range(steps + 2):
+        flush.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        if i < 2:
+            continue
+        for n, (a, b) in ev.items():
+            try:
+                acc.setdefault(n, []).append(a.elapsed_time(b))
+                used.add(n)
+            except (RuntimeError, ValueError):  # a stage this layer does not run (never recorded)
+                pass
+    return {n: sum(v) / len(v) for n, v in acc.items() if n in used}
+
+
+def dense_rows(args, L, wl, dev, flush, peaks):
+    """The dense prefill-shaped RAC linear layer (M 4096, K 4096, N 14336, k 64): the whole forward
+    (quantize + select + residual and weight tails + GEMM) and the block-scaled GEMM alone, against
+    the NVFP4 roofline.  X from the workload generator; W ~ N(0, 0.02^2) drawn on the device."""
+    import torch
+    from nvfp4_w4a4_quantized_quantize_gb300.layers import RacLinear
+    cfg = wl.CFG_DENSE
+    x_bits = wl.activations(cfg.M, cfg.K, cfg.seed, cfg.dist, cfg.x_scale, cfg.n_outliers, cfg.outlier_gain)[0]
+    gen = torch.Generator(device=dev).manual_seed(cfg.seed + 1)
+    w = (torch.randn(cfg.N, cfg.K, device=dev, generator=gen) * cfg.w_std).bfloat16()
+    lin = RacLinear(w, cfg.k, cfg.M)
+    del w
+    x = _bf16(x_bits, dev)
+    out = torch.empty(cfg.M, cfg.N, dtype=torch.bfloat16, device=dev)
+    ms_fwd, clk_fwd = clocked(lambda: lin.forward(x, out), flush)
+    lin.forward(x, out)
+
+    def gemm():
+        L.w4a4_rac_grouped_gemm(lin.a.codes, lin.a.sf, lin.a.sf_cols, lin.a.tscale, lin.w.codes, lin.w.sf, lin.w.sf_cols,
+                                lin.w.tscale, lin.N, lin.K, lin.k, None, out, rows=cfg.M)
+    ms_gemm, clk_gemm = clocked(gemm, flush)
+    flop = 2.0 * cfg.M * cfg.N * (cfg.K + cfg.k)
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    tf = flop / (ms_gemm * 1e-3) / 1e12
+    del lin, x, out
+    torch.cuda.empty_cache()
+    return {"workload": cfg.name, "gemm_ms": round(ms_gemm, 4), "gemm_tflops": round(tf, 1),
+            "gemm_frac_of_fp4_peak": round(tf / fp4_peak, 4), "fp4_peak_tflops": round(fp4_peak, 1),
+            "layer_forward_ms": round(ms_fwd, 4),
+            "layer_tflops": round(flop / (ms_fwd * 1e-3) / 1e12, 1), "gemm_flop": flop,
+            "clocks_gemm": clk_gemm, "clocks_forward": clk_fwd,
+            "timing": "median of CUDA-graph replays, L2 flushed (512 MiB write) before each"}
+
+
+def decode_rows(args, L, wl, dev, flush, peaks):
+    """The decode-shaped MoE step (512 tokens, H 4096, 128 experts, top-8 uniform routing,
+    I 1536, k = 64 per GEMM): tokens/s, the grouped GEMMs against the HBM roofline (about 32 routed
+    rows per expert, so the GEMMs stream each expert's weights once), and the same layer at k = 0
+    and in FP8 W8A8 (the pages' decode comparison).  Tokens from the workload generator; expert
+    weights ~ N(0, 0.02^2) drawn on the device."""
+    import torch
+    from nvfp4_w4a4_quantized_quantize_gb300.layers import Fp8MoELayer, MoERacLayer
+    cfg = wl.CFG_MOE_DECODE
+    E, H, I, T, topk, k = cfg.E, cfg.H, cfg.I, cfg.T, cfg.topk, cfg.k
+    x_bits, ids, tw, _ = cfg.make_tokens()
+    gen = torch.Generator(device=dev).manual_seed(cfg.seed + 11)
+    w13 = (torch.randn(E, 2 * I, H, device=dev, generator=gen) * cfg.w_std).bfloat16()
+    w2 = (torch.randn(E, H, I, device=dev, generator=gen) * cfg.w_std).bfloat16()
+    x = _bf16(x_bits, dev)
+    ids_d, tw_d = torch.from_numpy(ids).to(dev), torch.from_numpy(tw).to(dev)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    steps = max(5, min(args.steps, 50))
+    res = {"workload": cfg.name}
+    layer = MoERacLayer(w13, w2, k, topk, T)
+    ms, clk = clocked(lambda: layer.forward(x, ids_d, tw_d, out), flush)
+    st = stage_times(lambda ev: layer.forward(x, ids_d, tw_d, out, events=ev), flush, steps)
+    # weight bytes the two GEMMs stream (codes + scales of the K + k columns of every expert)
+    wb13 = E * 2 * I * ((H + k) // 2 + L.sf_cols(H + k))
+    wb2 = E * H * ((I + k) // 2 + L.sf_cols(I + k))
+    t_gemm = st.get("gemm_gate_up", 0.0) + st.get("gemm_down", 0.0)
+    gbs = (wb13 + wb2) / (t_gemm * 1e-3) / 1e9 if t_gemm else None
+    res["w4a4_rac"] = {"ms_per_step": round(ms, 4), "tokens_per_s": round(T / (ms * 1e-3), 1), "clocks": clk,
+                       "stage_ms": {n: round(v, 4) for n, v in st.items()},
+                       "gemm_weight_bytes": int(wb13 + wb2),
+                       "gemm_weight_gbs": round(gbs, 1) if gbs else None,
+                       "gemm_frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4) if gbs else None}
+    del layer
+    layer0 = MoERacLayer(w13, w2, 0, topk, T)
+    ms0, clk0 = clocked(lambda: layer0.forward(x, ids_d, tw_d, out), flush)
+    del layer0
+    res["w4a4_no_rac"] = {"ms_per_step": round(ms0, 4), "tokens_per_s": round(T / (ms0 * 1e-3), 1), "clocks": clk0}
+    f8 = Fp8MoELayer(w13, w2, topk, T)
+    ms8, clk8 = clocked(lambda: f8.forward(x, ids_d, tw_d, out), flush)
+    del f8, w13, w2
+    torch.cuda.empty_cache()
+    res["fp8_w8a8"] = {"ms_per_step": round(ms8, 4), "tokens_per_s": round(T / (ms8 * 1e-3), 1), "clocks": clk8}
+    res["w4a4_over_fp8"] = round(ms8 / ms0, 3)
+    res["w4a4_rac_over_fp8"] = round(ms8 / ms, 3)
+    res["rac_cost"] = round((ms - ms0) / ms0, 4)
+    res["timing"] = "median of CUDA-graph replays, L2 flushed (512 MiB write) before each"
+    return res
+
+
+def mma_probe_row(L):
+    """The measured NVFP4 tensor-core rate (nvq_fp4_mma_rate: back-to-back M128 N256 K64 MMAs on
+    every SM, no memory traffic) with the SM clock sampled meanwhile: cycles per MMA = time x
+    median SM clock / MMAs."""
+    import torch
+    sampler = ClockSampler(torch.cuda.current_device())
+    L.fp4_mma_rate(4096)
+    mmas = 65536
+    sampler.start()
+    t0 = time.perf_counter()
+    rates = []
+    while time.perf_counter() - t0 < 0.4:
+        rates.append(L.fp4_mma_rate(mmas))
+    clk = sampler.stop()
+    tf = statistics.median(rates)
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    res = {"tflops": round(tf, 1), "launches": len(rates), "mmas_per_sm": mmas, "clocks": clk}
+    if clk.get("sm_mhz"):
+        flop_per_mma = 2.0 * 128 * 256 * 64
+        res["cycles_per_mma"] = round(flop_per_mma * sms / (tf * 1e12) * clk["sm_mhz"] * 1e6, 1)
+    return res
+
+
+def baseline_rows(args, layer, x, ids_d, tw_d, w13_bits, w2_bits, cfg, dev, flush, ms_rac, t_gu, t_dn, stage_ms_rac):
     """The comparison rows of the measurement plan: the same layer with k = 0 (W4A4 without RAC;
     RAC cost = (t_RAC - t_noRAC) / t_noRAC), and the two expert GEMMs with SwiGLU in bf16 through
     cuBLAS (a per-expert loop over this batch's routed rows, captured in a CUDA graph)."""
@@ -369,7 +542,13 @@ def baseline_rows(args, layer, x, ids_d, tw_d, w13_bits, w2_bits, cfg, dev, flus
     w2 = _bf16(w2_bits.reshape(E * H, I), dev).view(E, H, I)
     layer0 = MoERacLayer(w13, w2, 0, topk, T)
     out0 = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-    ms0 = _time_replays(lambda: layer0.forward(x, ids_d, tw_d, out0), flush, steps, 3)
+    ms0, clk0 = clocked(lambda: layer0.forward(x, ids_d, tw_d, out0), flush)
+    # the RAC layer with every launch in order on one stream (no side stream)
+    layer1 = MoERacLayer(w13, w2, cfg.k, topk, T, side_stream=False)
+    out1 = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    ms1, clk1 = clocked(lambda: layer1.forward(x, ids_d, tw_d, out1), flush)
+    del layer1, out1
+    stage0 = stage_times(lambda ev: layer0.forward(x, ids_d, tw_d, out0, events=ev), flush, steps)
     del layer0, out0
     # bf16 expert GEMMs on the routed rows of this batch (the rows gathered outside the timing)
     off = layer.grp_off.cpu().tolist()
@@ -413,9 +592,17 @@ def baseline_rows(args, layer, x, ids_d, tw_d, w13_bits, w2_bits, cfg, dev, flus
     flop_gu8 = 2.0 * rows * (2 * I) * H
     del f8, out8
     torch.cuda.empty_cache()
+    breakdown = {n: {"k32_ms": round(stage_ms_rac[n], 4), "k0_ms": round(stage0.get(n, 0.0), 4),
+                     "rac_ms": round(stage_ms_rac[n] - stage0.get(n, 0.0), 4)} for n in stage_ms_rac}
     return {
         "w4a4_no_rac_layer": {"ms_per_step": round(ms0, 4), "tokens_per_s": round(T / (ms0 * 1e-3), 1),
-                              "rac_cost": round((ms_rac - ms0) / ms0, 4)},
+                              "rac_cost": round((ms_rac - ms0) / ms0, 4), "clocks": clk0},
+        "w4a4_rac_layer_one_stream": {"ms_per_step": round(ms1, 4), "tokens_per_s": round(T / (ms1 * 1e-3), 1),
+                                      "clocks": clk1},
+        "rac_cost_breakdown": {"stages": breakdown,
+                               "note": "per-stage device time (CUDA events inside the graph, mean over replays) of the "
+                                       "layer at k = 32 per GEMM and at k = 0; the side-stream stages (tokens, weight "
+                                       "tails) overlap the main stream's, so the stages do not sum to the step"},
         "bf16_expert_gemms": {"ms": round(ms_bf, 4), "tflops": round(flop_k0 / (ms_bf * 1e-3) / 1e12, 1),
                               "impl": "cuBLAS per-expert loop (gate/up, SwiGLU, down) in a CUDA graph"},
         "w4a4_rac_expert_gemms": {"ms": round(t_gu + t_dn, 4),
@@ -443,6 +630,7 @@ def trainer_rows(args, L, dev, flush, peaks):
     gen = torch.Generator(device=dev).manual_seed(5)
     res = {}
     total_ms, elems = 0.0, 0
+    clks = []
     for (G, N, K) in ((128, 3072, 4096), (128, 4096, 1536)):
         w = (torch.randn(G, N, K, device=dev, generator=gen) * 0.02).bfloat16()
         op = Operand.empty(G * N, K, 0, G, device=dev)
@@ -450,7 +638,9 @@ def trainer_rows(args, L, dev, flush, peaks):
 
         def qdq():
             L.weight_qdq(w, G, N, K, op.codes, op.sf, op.sf_cols, op.tscale, w_hat=w_hat, w_hat_dtype=L.NVQ_BF16)
-        total_ms += _time_replays(qdq, flush, 5, 2)
+        ms_g, clk_g = clocked(qdq, flush, min_s=0.3)
+        total_ms += ms_g
+        clks.append(clk_g)
         elems += G * N * K
         del w, op, w_hat
         torch.cuda.empty_cache()
@@ -458,7 +648,8 @@ def trainer_rows(args, L, dev, flush, peaks):
     res["weight_qdq"] = {"workload": "W13 [128,3072,4096] + W2 [128,4096,1536], bf16 W-hat", "elements": elems,
                          "ms": round(total_ms, 4), "algorithmic_bytes": int(alg),
                          "gbs": round(alg / (total_ms * 1e-3) / 1e9, 1),
-                         "frac_of_measured_hbm": round(alg / (total_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+                         "frac_of_measured_hbm": round(alg / (total_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                         "clocks": clks}
     torch.manual_seed(6)
     M, K, N = 4096, 4096, 14336
     x = torch.randn(M, K, device=dev).bfloat16().requires_grad_(True)
@@ -521,7 +712,7 @@ def act_quant_bench(args, L, wl, dev, flush, peaks):
 
     # CUDA-graph replays (as the layer step), L2 flushed before each: the whole path, and each
     # half alone (the selection replays over the scores the last quantize left)
-    t_all = _time_replays(step, flush, args.steps, args.warmup)
+    t_all, clk = clocked(step, flush)
     t_q = _time_replays(quant, flush, args.steps, args.warmup)
     t_r = _time_replays(select, flush, args.steps, args.warmup)
     algo = M * K * (2 + 0.5 + 1 / 16) + M * k * (2 + 0.5 + 1 / 16) + k * 4
@@ -530,7 +721,7 @@ def act_quant_bench(args, L, wl, dev, flush, peaks):
     return {"workload": cfg.name, "algorithmic_bytes": int(algo), "ms": round(t_all, 4),
             "gbs": round(algo / (t_all * 1e-3) / 1e9, 1), "frac_of_measured_hbm": round(algo / (t_all * 1e-3) / 1e9 / hbm, 4),
             "nvfp4_quantize_ms": round(t_q, 4), "nvfp4_quantize_gbs": round(q_bytes / (t_q * 1e-3) / 1e9, 1),
-            "rac_select_quantize_ms": round(t_r, 4),
+            "rac_select_quantize_ms": round(t_r, 4), "clocks": clk,
             "timing": "median of CUDA-graph replays, L2 flushed (512 MiB write) before each"}
 
 

@@ -1,7 +1,9 @@
 // probe.cu -- measured NVFP4 tensor-core rate of this GPU: a loop of
 // tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X (M128 N256 K64) with no
-// memory traffic, one CTA per SM, optionally with the three scale-factor copies into TMEM that
-// the GEMM issues per MMA.  The result is a roofline reference for the block-scaled GEMM.
+// memory traffic, one CTA per SM, optionally with three scale-factor copies into TMEM per MMA.
+// The result is a roofline reference for the block-scaled GEMM.  The copy variant is a separate
+// instantiation: measured on GB300, a loop that merely contains a (never taken) branch around
+// tcgen05.cp issues the MMAs at 185 cycles each instead of 128.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -21,8 +23,8 @@ __device__ __forceinline__ uint64_t pdesc(uint32_t addr, uint32_t lbo, uint32_t 
            ((uint64_t)((sbo >> 4) & 0x3fffu) << 32) | (1ull << 46) | ((uint64_t)layout << 61);
 }
 
-__global__ void __launch_bounds__(kProbeThreads, 1) mma_rate_kernel(int mmas, int with_cp, DeviceStatus* st,
-                                                                    unsigned long long limit)
+template <bool kWithCp>
+__global__ void __launch_bounds__(kProbeThreads, 1) mma_rate_kernel(int mmas, DeviceStatus* st, unsigned long long limit)
 {
     extern __shared__ __align__(1024) uint8_t sm_raw[];
     __shared__ __align__(8) uint64_t done;
@@ -56,7 +58,7 @@ __global__ void __launch_bounds__(kProbeThreads, 1) mma_rate_kernel(int mmas, in
         asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(sfb), "l"(sd1) : "memory");
         asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(sfb + 4), "l"(sd2) : "memory");
         for (int i = 0; i < mmas; ++i) {
-            if (with_cp) {
+            if (kWithCp) {
                 asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(sfa), "l"(sd0) : "memory");
                 asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(sfb), "l"(sd1) : "memory");
                 asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(sfb + 4), "l"(sd2) : "memory");
@@ -109,15 +111,16 @@ extern "C" nvq_status nvq_fp4_mma_rate(int32_t mmas_per_sm, int32_t with_cp, flo
     DeviceStatus* ds = device_status_ptr();
     NVQ_CHECK_ARG(ds, NVQ_ERR_CUDA, "nvq_fp4_mma_rate: device status word unavailable");
     const int smem = 50688 + 1024;
-    cudaError_t e = cudaFuncSetAttribute(mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    auto kernel = with_cp ? mma_rate_kernel<true> : mma_rate_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(mma_rate_kernel)");
     // warm-up, then the timed launch
-    mma_rate_kernel<<<sms, kProbeThreads, smem, st>>>(64, with_cp, ds, wait_limit());
+    kernel<<<sms, kProbeThreads, smem, st>>>(64, ds, wait_limit());
     cudaEvent_t a, b;
     cudaEventCreate(&a);
     cudaEventCreate(&b);
     cudaEventRecord(a, st);
-    mma_rate_kernel<<<sms, kProbeThreads, smem, st>>>(mmas_per_sm, with_cp, ds, wait_limit());
+    kernel<<<sms, kProbeThreads, smem, st>>>(mmas_per_sm, ds, wait_limit());
     cudaEventRecord(b, st);
     e = cudaEventSynchronize(b);
     float ms = 0.0f;

@@ -106,6 +106,11 @@ class RacLinear:
         return out
 
 
+# Stages of MoERacLayer.forward that its `events` argument can time, in launch order.
+MOE_STAGES = ("dispatch", "quant_rac_tokens", "weight_tail_w13", "gather", "gemm_gate_up", "quant_h", "select_h",
+              "weight_tail_w2", "tail_h", "gemm_down", "combine")
+
+
 class MoERacLayer:
     """Routed SwiGLU expert layer with NVFP4 W4A4 + RAC in both expert GEMMs.
 
@@ -118,8 +123,11 @@ class MoERacLayer:
     """
 
     def __init__(self, w13: torch.Tensor, w2: torch.Tensor, k: int, topk: int, max_tokens: int,
-                 k2: Optional[int] = None):
-        """k: compensated channels at the gate/up site (of H), k2 at the down site (of I; default k)."""
+                 k2: Optional[int] = None, side_stream: bool = True):
+        """k: compensated channels at the gate/up site (of H), k2 at the down site (of I; default k).
+        side_stream: run the work that does not depend on dispatch (token quantization and
+        selection, the weight tails) on a second stream; False issues everything in order on the
+        caller's stream."""
         dev = w13.device
         self.E, twoI, self.H = w13.shape
         self.I = twoI // 2
@@ -150,7 +158,7 @@ class MoERacLayer:
         # side stream for the work that does not depend on dispatch (token quantization and
         # selection) or on the gather (the gate/up weight tail); events fork and join it, so
         # a CUDA graph captured around forward() holds the two branches in parallel
-        self.side = torch.cuda.Stream(device=dev)
+        self.side = torch.cuda.Stream(device=dev) if side_stream else None
         self.ev_fork = torch.cuda.Event()
         self.ev_tok = torch.cuda.Event()
         self.ev_wt = torch.cuda.Event()
@@ -170,12 +178,14 @@ class MoERacLayer:
 
     def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, out: torch.Tensor,
                 stream=None, events: Optional[dict] = None):
-        """events: optional dict that receives (start, end) CUDA events around the stages
-        'quant_rac_tokens', 'gemm_gate_up' and 'gemm_down' (for per-kernel timing)."""
+        """events: optional dict that receives (start, end) CUDA events around each stage (for
+        per-kernel timing): 'dispatch', 'quant_rac_tokens', 'weight_tail_w13', 'gather',
+        'gemm_gate_up', 'quant_h', 'select_h', 'weight_tail_w2', 'tail_h', 'gemm_down' and
+        'combine' (stages a site without RAC does not run are absent)."""
         T = x.shape[0]
         k, k2, E, H, I = self.k, self.k2, self.E, self.H, self.I
         st = torch.cuda.current_stream() if stream is None else stream
-        side = self.side
+        side = self.side if self.side is not None else st
 
         def mark(name, pos, on=None):
             if events is not None:
@@ -193,15 +203,21 @@ class MoERacLayer:
                                   self.a_tok.sf_cols, self.idx1, stream=side)
         mark("quant_rac_tokens", 1, side)
         self.ev_tok.record(side)
+        mark("dispatch", 0)
         L.moe_dispatch(topk_ids, topk_w, E, self.grp_off, self.grp_rows, self.row_src, self.row_of, self.row_w,
                        self.ws, stream=st)
+        mark("dispatch", 1)
         st.wait_event(self.ev_tok)
         # the gate/up weight tail (needs the selection only) beside the gather
         if k:
+            mark("weight_tail_w13", 0, side)
             _weight_tail(self.w13, self.w13_cm, E, 2 * I, k, self.idx1, stream=side)
+            mark("weight_tail_w13", 1, side)
         self.ev_wt.record(side)
+        mark("gather", 0)
         L.nvfp4_gather_rows(self.a_tok.codes, self.a_tok.sf, self.a_tok.sf_cols, T, self.row_src, self.topk, H + k,
                             self.a_routed.codes, self.a_routed.sf, stream=st)
+        mark("gather", 1)
         st.wait_event(self.ev_wt)  # join
         mark("gemm_gate_up", 0)
         L.w4a4_rac_grouped_gemm(self.a_routed.codes, self.a_routed.sf, self.a_routed.sf_cols, self.a_tok.tscale,
@@ -211,18 +227,26 @@ class MoERacLayer:
         mark("gemm_gate_up", 1)
         # down input: per-expert tensor scale (amax of h measured by the gate/up epilogue) and
         # channel set
+        mark("quant_h", 0)
         L.nvfp4_quantize(self.h, self.a2.codes, self.a2.sf, self.a2.sf_cols, self.a2.tscale,
                          scores=self.scores2 if k2 else None, grp_off=self.grp_off, grp_rows=self.grp_rows,
                          groups=E, zero_pad=(k2 == 0), amax_given=True, stream=st)
+        mark("quant_h", 1)
         if k2:
             # selection, then the down weight tail (needs idx2 only) beside the residual tail of h
+            mark("select_h", 0)
             L.rac_select(self.scores2, I, k2, self.idx2, groups=E, stream=st)
+            mark("select_h", 1)
             self.ev_sel2.record(st)
             side.wait_event(self.ev_sel2)
+            mark("weight_tail_w2", 0, side)
             _weight_tail(self.w2, self.w2_cm, E, H, k2, self.idx2, idx_per_group=True, stream=side)
+            mark("weight_tail_w2", 1, side)
             self.ev_wt2.record(side)
+            mark("tail_h", 0)
             L.rac_residual_tail(self.h, self.a2.tscale, self.idx2, k2, self.a2.codes, self.a2.sf, self.a2.sf_cols,
                                 grp_off=self.grp_off, grp_rows=self.grp_rows, groups=E, stream=st)
+            mark("tail_h", 1)
             st.wait_event(self.ev_wt2)
         mark("gemm_down", 0)
         L.w4a4_rac_grouped_gemm(self.a2.codes, self.a2.sf, self.a2.sf_cols, self.a2.tscale, self.w2.codes,
@@ -231,7 +255,9 @@ class MoERacLayer:
                                 a_scale_per_group=True, idx_per_group=True, epilogue=L.NVQ_EPI_ROW_SCALE,
                                 row_w=self.row_w, stream=st)
         mark("gemm_down", 1)
+        mark("combine", 0)
         L.moe_combine(self.y, self.row_of, T, self.topk, H, out, stream=st)
+        mark("combine", 1)
         return out
 
 
