@@ -38,7 +38,9 @@ namespace nvq {
 
 constexpr int kBM = 128, kBN = 256;
 constexpr int kRowBytes = 128;              // bytes of a K-tile row in shared memory = swizzle span
-constexpr int kStages = 4;                  // 4 x 54 KB for FP4 (a 128-element K-tile in 8 x 27 KB was
+// Epilogue staging for the coalesced bf16 stores (one 32-row x 128-byte buffer per epilogue warp).
+constexpr int kStagingBytes = 8 * 32 * 128;
+constexpr int kStagesMax = 4;               // 4 x 54 KB for FP4 (a 128-element K-tile in 8 x 27 KB was
                                             // slower: twice the per-stage hand-offs)
 constexpr uint32_t kSwizzleLayout = 2u;     // tcgen05 smem layout: 128-byte swizzle
 constexpr uint32_t kSBO = 8 * kRowBytes;    // stride between 8-row core-matrix groups
@@ -104,7 +106,7 @@ struct Geo {
     static constexpr int kSFABytes = 512 * kSfAtoms;
     static constexpr int kSFBBytes = 1024 * kSfAtoms;                     // 2 row blocks
     static constexpr int kStageBytes = (kABytes + kBBytes + kSFABytes + kSFBBytes + 1023) / 1024 * 1024;
-    static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+    static constexpr int kSmemBytes(int stages, bool staged) { return stages * kStageBytes + (staged ? kStagingBytes : 0) + 1024; }
     static constexpr uint32_t kSFColsPerStage = 12 * kSfAtoms;            // SFA 4 + SFB 8 per atom
     // scale atom of MMA j of a stage (FP4: one per MMA; FP8: one for all four)
     static constexpr int atom_of(int j) { return (j * F::kMmaK) / (4 * F::kSfVec); }
@@ -388,9 +390,12 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
         : "memory");
 }
 
-template <class F>
+// kStages: depth of the operand ring; kStaged: the bf16 store and routing-weight epilogues write
+// through a per-warp shared-memory buffer (needs the room of one stage: the ring is 3 deep then).
+template <class F, int kStages, bool kStaged>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                                                           const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a)
+                                                           const __grid_constant__ CUtensorMap tmap_b,
+                                                           const __grid_constant__ CUtensorMap tmap_b256, const GemmArgs a)
 {
     using GF = Geo<F>;
     constexpr int kStageBytes = GF::kStageBytes;
@@ -469,10 +474,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
     const int prod = warp == 0 ? 0 : (warp == kProdWarpB0 ? 1 : (warp == kProdWarpB1 ? 2 : -1));
     if (prod >= 0) {
-        // ---------------- producers: the TMA engine sustains more per SM when its requests come
-        // from several warps, so each stage is loaded by three: warp 0 the A tile and its scale
-        // atoms, warps 14 and 15 one 128-row half of the weight tile each (L2 evict-last: every
-        // 128-row block of the group re-reads them) and its scale atoms.
+        // ---------------- producers: the TMA engine sustains more per SM with fewer, larger
+        // requests and with requests from several warps, so each stage is loaded by three:
+        // warp 0 the A tile and its scale atoms; when the weight tile's 256 rows are contiguous
+        // (every epilogue but SwiGLU) warp 14 loads them as one box and warp 15 their scale
+        // atoms, otherwise warps 14 and 15 one 128-row half each with its scale atoms.  Weight
+        // loads are L2 evict-last: every 128-row block of the group re-reads them.
         uint64_t pol_keep;
         asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
         int stage = 0;
@@ -497,13 +504,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         bulk_load(sA + kABytes + kBBytes,
                                   a.a_sf + ((int64_t)(T.row0 >> 7) * (a.a_sf_cols >> 2) + kt * kSfAtoms) * 512, sf_bytes,
                                   &full_bar[stage]);
-                    } else {
+                    } else if (a.epilogue == NVQ_EPI_SWIGLU) {
                         const int h = prod - 1;
                         mbar_expect_tx(&full_bar[stage], kBBytes / 2 + sf_bytes);
                         tma_load_2d_hint(sA + kABytes + h * (kBBytes / 2), &tmap_b, kt * kRowBytes, (int)brow, &full_bar[stage],
                                          pol_keep);
                         bulk_load(sA + kABytes + kBBytes + kSFABytes + h * (kSFBBytes / 2),
                                   a.b_sf + ((brow >> 7) * (a.b_sf_cols >> 2) + kt * kSfAtoms) * 512, sf_bytes, &full_bar[stage]);
+                    } else if (prod == 1) {  // brow: the tile's first weight row
+                        mbar_expect_tx(&full_bar[stage], kBBytes);
+                        tma_load_2d_hint(sA + kABytes, &tmap_b256, kt * kRowBytes, (int)brow, &full_bar[stage], pol_keep);
+                    } else {  // brow: the tile's second 128-row block
+                        mbar_expect_tx(&full_bar[stage], 2 * sf_bytes);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            bulk_load(sA + kABytes + kBBytes + kSFABytes + h * (kSFBBytes / 2),
+                                      a.b_sf + (((brow >> 7) - 1 + h) * (a.b_sf_cols >> 2) + kt * kSfAtoms) * 512, sf_bytes,
+                                      &full_bar[stage]);
                     }
                     ++issued;
                     if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -688,7 +705,33 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 }
                 tc_fence_before();
                 mbar_arrive(&acc_empty);
-                if (valid) store_row<64>(a.out + grow * a.ldo + (int64_t)T.nt * kBN + half * (kBN / 2), pk, wide);
+                if constexpr (kStaged) {
+                    // this warp's 32 rows go through its shared-memory buffer 64 columns (128 bytes
+                    // a row) at a time, 16-byte units XOR-swizzled by row (conflict-free both ways),
+                    // and leave as whole 128-byte row pieces, four rows per store instruction,
+                    // instead of 32 scattered 32-byte pieces
+                    uint8_t* buf = smem + kStages * kStageBytes + (warp - kFirstEpiWarp) * 4096;
+                    const int64_t col0 = (int64_t)T.nt * kBN + half * (kBN / 2);
+                    const int64_t rbase = (int64_t)T.row0 + quarter * 32;
+                    const int rvalid = T.rows - quarter * 32;  // rows of this warp's 32 inside the tile
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        __syncwarp();
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            *reinterpret_cast<uint4*>(buf + lane * 128 + ((u ^ (lane & 7)) << 4)) =
+                                make_uint4(pk[32 * c + 4 * u], pk[32 * c + 4 * u + 1], pk[32 * c + 4 * u + 2], pk[32 * c + 4 * u + 3]);
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int r = 4 * j + (lane >> 3), u = lane & 7;
+                            const uint4 d = *reinterpret_cast<const uint4*>(buf + r * 128 + ((u ^ (r & 7)) << 4));
+                            if (r < rvalid) *reinterpret_cast<uint4*>(a.out + (rbase + r) * a.ldo + col0 + 64 * c + 8 * u) = d;
+                        }
+                    }
+                } else if (valid) {
+                    store_row<64>(a.out + grow * a.ldo + (int64_t)T.nt * kBN + half * (kBN / 2), pk, wide);
+                }
                 if (a.out_ts) warp_amax_to(valid ? amax_packed<64>(pk) : 0.0f, &a.out_ts[T.g].amax);
             }
             acc_phase ^= 1;
@@ -738,22 +781,34 @@ nvq_status weight_tail_impl(uint8_t* codes, int64_t ld_codes, uint8_t* sf, int64
                             int G, const nvq_tensor_scale* ts, const int32_t* idx, int idx_per_group, cudaStream_t st);
 
 // Persistent launch: one CTA per SM, no more CTAs than tiles.
-template <class F>
-nvq_status launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& ga, int32_t groups, int64_t N,
-                       cudaStream_t st)
+template <class F, int kStages, bool kStaged>
+nvq_status launch_gemm_cfg(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mb256, const GemmArgs& ga,
+                           int32_t groups, int64_t N, cudaStream_t st)
 {
-    constexpr int kSmem = Geo<F>::kSmemBytes;
+    constexpr int kSmem = Geo<F>::kSmemBytes(kStages, kStaged);
+    static_assert(kSmem + 8 * 1024 <= 227 * 1024, "shared memory of the GEMM");
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<F, kStages, kStaged>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(gemm_kernel)");
     // an upper bound of the tiles: every group adds at most one partial 128-row tile
     const int64_t max_tiles = (int64_t)(ga.total_mtiles_max + groups) * (N / kBN);
     const int ctas = (int)(max_tiles < sms ? max_tiles : sms);
-    gemm_kernel<F><<<ctas, kThreads, kSmem, st>>>(ma, mb, ga);
+    gemm_kernel<F, kStages, kStaged><<<ctas, kThreads, kSmem, st>>>(ma, mb, mb256, ga);
     NVQ_LAUNCH_CHECK("gemm_kernel");
     return NVQ_OK;
+}
+
+// The routing-weight epilogue (the down projection: a full 128 x 256 bf16 tile per output,
+// written to memory once and read back by the combine) stores through shared memory with a
+// 3-deep operand ring; the other epilogues keep the 4-deep ring.
+template <class F>
+nvq_status launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mb256, const GemmArgs& ga, int32_t groups,
+                       int64_t N, cudaStream_t st)
+{
+    if (ga.epilogue == NVQ_EPI_ROW_SCALE) return launch_gemm_cfg<F, 3, true>(ma, mb, mb256, ga, groups, N, st);
+    return launch_gemm_cfg<F, kStagesMax, false>(ma, mb, mb256, ga, groups, N, st);
 }
 
 // Arguments shared by both entries.
@@ -835,10 +890,12 @@ extern "C" nvq_status w4a4_rac_grouped_gemm(int32_t groups, const int64_t* grp_o
         if (s != NVQ_OK) return s;
     }
 
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mb256;
     s = make_map(&ma, a_codes, ktot / 2, rows, lda);
     if (s != NVQ_OK) return s;
     s = make_map(&mb, b_codes, ktot / 2, (int64_t)groups * N, ldb);
+    if (s != NVQ_OK) return s;
+    s = make_map(&mb256, b_codes, ktot / 2, (int64_t)groups * N, ldb, 256);
     if (s != NVQ_OK) return s;
 
     GemmArgs ga = gemm_args(groups, grp_off, grp_rows, rows, a_sf, a_sf_cols, b_sf, b_sf_cols, N, ktot, epilogue, row_w,
@@ -852,7 +909,7 @@ extern "C" nvq_status w4a4_rac_grouped_gemm(int32_t groups, const int64_t* grp_o
         const cudaError_t me = cudaMemsetAsync(out_tscale, 0, sizeof(nvq_tensor_scale) * groups, st);
         if (me != cudaSuccess) return cuda_status(me, "cudaMemsetAsync(out_tscale)");
     }
-    return launch_gemm<Fp4>(ma, mb, ga, groups, N, st);
+    return launch_gemm<Fp4>(ma, mb, mb256, ga, groups, N, st);
 }
 
 extern "C" nvq_status fp8_blockscaled_grouped_gemm(int32_t groups, const int64_t* grp_off, const int64_t* grp_rows,
@@ -875,12 +932,14 @@ extern "C" nvq_status fp8_blockscaled_grouped_gemm(int32_t groups, const int64_t
                   "%s: operands must be 16-byte aligned", fn);
     set_error("");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mb256;
     s = make_map(&ma, a_codes, K, rows, lda);
     if (s != NVQ_OK) return s;
     s = make_map(&mb, b_codes, K, (int64_t)groups * N, ldb);
     if (s != NVQ_OK) return s;
+    s = make_map(&mb256, b_codes, K, (int64_t)groups * N, ldb, 256);
+    if (s != NVQ_OK) return s;
     GemmArgs ga = gemm_args(groups, grp_off, grp_rows, rows, a_sf, a_sf_cols, b_sf, b_sf_cols, N, K, epilogue, row_w, out, ldo);
     NVQ_CHECK_ARG(ga.status, NVQ_ERR_CUDA, "%s: device status word unavailable", fn);
-    return launch_gemm<Fp8>(ma, mb, ga, groups, N, st);
+    return launch_gemm<Fp8>(ma, mb, mb256, ga, groups, N, st);
 }
