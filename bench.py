@@ -853,7 +853,8 @@ def sweep_k(args):
 
 
 def profile_case(name: str):
-    """Small cases for ncu captures (no timing, no JSON line): 'moe_small' runs two MoE layer
+    """Cases for ncu captures (no timing, no JSON line): 'moe_prefill' runs three eager forwards of
+    the bench's full-size MoE layer (for the one-pass launch list only); 'moe_small' runs two MoE layer
     forwards at E=32, T=4096, H=2048, I=768, top-8, k=32 (about 1 GB on the device);
     'act_256mb' quantizes and selects twice on a 32768 x 4096 bf16 activation (256 MB, larger
     than L2), k=64; 'act_8192x4096' runs the activation workload of the bench line three times
@@ -866,7 +867,20 @@ def profile_case(name: str):
     from nvfp4_w4a4_quantized_quantize_gb300 import workloads as wl
     from nvfp4_w4a4_quantized_quantize_gb300.layers import MoERacLayer, Operand
     dev = "cuda"
-    if name == "moe_small":
+    if name == "moe_prefill":
+        # the bench's layer step at full size, three eager forwards (for the launch list)
+        cfg = wl.CFG_MOE_PREFILL
+        x_bits, ids, tw, _ = cfg.make_tokens()
+        w13_bits, w2_bits = cfg.make_weights()
+        E, H, I, T = cfg.E, cfg.H, cfg.I, cfg.T
+        layer = MoERacLayer(_bf16(w13_bits.reshape(E * 2 * I, H), dev).view(E, 2 * I, H),
+                            _bf16(w2_bits.reshape(E * H, I), dev).view(E, H, I), cfg.k, cfg.topk, T)
+        x = _bf16(x_bits, dev)
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        ids_d, tw_d = torch.from_numpy(ids).to(dev), torch.from_numpy(tw).to(dev)
+        for _ in range(3):
+            layer.forward(x, ids_d, tw_d, out)
+    elif name == "moe_small":
         E, T, H, I, k, topk = 32, 4096, 2048, 768, 32, 8
         cfg = wl.MoELayer("moe_small", T=T, H=H, E=E, topk=topk, I=I, k=k, seed=7, routing="zipf", n_outliers=20)
         x_bits, ids, tw, _ = cfg.make_tokens()
@@ -949,7 +963,8 @@ def main():
     ap.add_argument("--sweep-k", action="store_true",
                     help="residual channel ratio sweep (0 to 100 %% of K) at the activation, dense and MoE "
                          "workloads: error and time per ratio, one JSON line, then exit")
-    ap.add_argument("--profile-case", choices=["moe_small", "fp8_moe_small", "act_256mb", "act_8192x4096", "row_tails_kK"],
+    ap.add_argument("--profile-case", choices=["moe_prefill", "moe_small", "fp8_moe_small", "act_256mb", "act_8192x4096",
+                                               "row_tails_kK"],
                     help="run a small case twice for an ncu capture and exit (no timing)")
     args = ap.parse_args()
     if args.profile_case:
