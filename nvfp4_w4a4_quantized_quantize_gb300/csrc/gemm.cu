@@ -9,9 +9,11 @@
 //   tile 128 x 256 x 256 (M x N x K-tile of FP4 elements = 128 bytes per row) per CTA; tiles run
 //   N-fastest inside each 128-row block, so the CTAs working at the same time read one A block
 //   and one group's weights, which L2 serves to all of them;
-//   warp 0     TMA producer: A and B code tiles by cp.async.bulk.tensor (128-byte swizzle,
-//              out-of-range columns zero-filled), scale atoms by cp.async.bulk (the blocked
-//              scale layout makes every 128-row x 64-column scale tile one contiguous 512 B);
+//   warps 0, 14, 15  TMA producers (A; the two 128-row halves of B, or all of B and the B
+//              scales): code tiles by cp.async.bulk.tensor (128-byte swizzle, out-of-range
+//              columns zero-filled), scale atoms by cp.async.bulk (the blocked scale layout
+//              makes every 128-row x 64-column scale tile one contiguous 512 B); three issuing
+//              warps fill shared memory faster than one;
 //   warp 1     TMEM allocator and MMA issuer: per K-tile, once the stage's scales are in
 //              TMEM, tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (K = 64 each, UE4M3
 //              scales, FP32 accumulation in TMEM), tcgen05.commit to free the stage;
@@ -21,7 +23,8 @@
 //              Register stores keep the scales off the tensor pipe's copy path, which at
 //              12 small copies per K-tile cost about 40% of the MMA rate;
 //   warps 6-13 epilogue: tcgen05.ld of the accumulator, alpha scaling, bf16 store, with the
-//              SwiGLU or routing-weight variants.
+//              SwiGLU or routing-weight variants; the routing-weight tile goes out through a
+//              swizzled shared-memory buffer per warp as TMA tile stores.
 // The same kernel, instantiated for E4M3 operands (kind::mxf8f6f4, scale_vec::1X, one UE8M0
 // scale per 32 elements, K = 32 per MMA, 128 elements per 128-byte K-tile row, no tensor
 // scale), is the FP8 W8A8 block-scaled baseline the paper compares against (§2.2 "FP8",
@@ -31,6 +34,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
+
+#include <cstring>
 
 #include "common.cuh"
 
@@ -134,6 +139,7 @@ struct GemmArgs {
     DeviceStatus* status;
     unsigned long long wait_limit;
     nvq_tensor_scale* out_ts;  // NULL, or per-group max |out| (bf16 epilogues) into .amax
+    int32_t out_tma;           // staged epilogue: full 32-row pieces leave by TMA store (tmap_out)
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -390,12 +396,22 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
         : "memory");
 }
 
+// Shared memory -> global tile store (bulk async group of the issuing thread).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(smem_u32(src))
+                 : "memory");
+}
+
 // kStages: depth of the operand ring; kStaged: the bf16 store and routing-weight epilogues write
 // through a per-warp shared-memory buffer (needs the room of one stage: the ring is 3 deep then).
 template <class F, int kStages, bool kStaged>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                            const __grid_constant__ CUtensorMap tmap_b,
-                                                           const __grid_constant__ CUtensorMap tmap_b256, const GemmArgs a)
+                                                           const __grid_constant__ CUtensorMap tmap_b256,
+                                                           const __grid_constant__ CUtensorMap tmap_out, const GemmArgs a)
 {
     using GF = Geo<F>;
     constexpr int kStageBytes = GF::kStageBytes;
@@ -707,26 +723,38 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 mbar_arrive(&acc_empty);
                 if constexpr (kStaged) {
                     // this warp's 32 rows go through its shared-memory buffer 64 columns (128 bytes
-                    // a row) at a time, 16-byte units XOR-swizzled by row (conflict-free both ways),
-                    // and leave as whole 128-byte row pieces, four rows per store instruction,
-                    // instead of 32 scattered 32-byte pieces
+                    // a row) at a time, 16-byte units XOR-swizzled by row (the 128-byte swizzle of
+                    // a TMA box, conflict-free both ways).  A piece of 32 rows inside the tile
+                    // leaves as one TMA tile store (32 x 64 bf16); a ragged piece leaves as whole
+                    // 128-byte row pieces, four rows per store instruction, up to the last row.
                     uint8_t* buf = smem + kStages * kStageBytes + (warp - kFirstEpiWarp) * 4096;
                     const int64_t col0 = (int64_t)T.nt * kBN + half * (kBN / 2);
                     const int64_t rbase = (int64_t)T.row0 + quarter * 32;
                     const int rvalid = T.rows - quarter * 32;  // rows of this warp's 32 inside the tile
+                    const bool by_tma = a.out_tma && rvalid >= 32;
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
+                        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // buffer read out
                         __syncwarp();
 #pragma unroll
                         for (int u = 0; u < 8; ++u)
                             *reinterpret_cast<uint4*>(buf + lane * 128 + ((u ^ (lane & 7)) << 4)) =
                                 make_uint4(pk[32 * c + 4 * u], pk[32 * c + 4 * u + 1], pk[32 * c + 4 * u + 2], pk[32 * c + 4 * u + 3]);
-                        __syncwarp();
+                        if (by_tma) {
+                            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the TMA unit
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(&tmap_out, buf, (int)(col0 + 64 * c), (int)rbase);
+                                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                            }
+                        } else {
+                            __syncwarp();
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int r = 4 * j + (lane >> 3), u = lane & 7;
-                            const uint4 d = *reinterpret_cast<const uint4*>(buf + r * 128 + ((u ^ (r & 7)) << 4));
-                            if (r < rvalid) *reinterpret_cast<uint4*>(a.out + (rbase + r) * a.ldo + col0 + 64 * c + 8 * u) = d;
+                            for (int j = 0; j < 8; ++j) {
+                                const int r = 4 * j + (lane >> 3), u = lane & 7;
+                                const uint4 d = *reinterpret_cast<const uint4*>(buf + r * 128 + ((u ^ (r & 7)) << 4));
+                                if (r < rvalid) *reinterpret_cast<uint4*>(a.out + (rbase + r) * a.ldo + col0 + 64 * c + 8 * u) = d;
+                            }
                         }
                     }
                 } else if (valid) {
@@ -736,6 +764,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             }
             acc_phase ^= 1;
         }
+        // the TMA stores this thread issued have finished (reading shared memory and writing)
+        if (kStaged && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
 
     tc_fence_before();
@@ -777,13 +807,30 @@ static nvq_status make_map(CUtensorMap* m, const void* base, int64_t inner_bytes
     return NVQ_OK;
 }
 
+// 2D bf16 tensor map over the output rows for the staged epilogue's TMA stores: box 64 columns
+// (128 bytes, 128-byte swizzle, as the staging buffer is laid out) x 32 rows.
+static nvq_status make_out_map(CUtensorMap* m, const void* out, int64_t width, int64_t rows, int64_t ldo)
+{
+    auto enc = get_encode();
+    NVQ_CHECK_ARG(enc, NVQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ldo * 2)};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(out), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    NVQ_CHECK_ARG(r == CUDA_SUCCESS, NVQ_ERR_CUDA, "cuTensorMapEncodeTiled (output) failed (%d)", (int)r);
+    return NVQ_OK;
+}
+
 nvq_status weight_tail_impl(uint8_t* codes, int64_t ld_codes, uint8_t* sf, int64_t sf_cols, int64_t N, int K, int k,
                             int G, const nvq_tensor_scale* ts, const int32_t* idx, int idx_per_group, cudaStream_t st);
 
 // Persistent launch: one CTA per SM, no more CTAs than tiles.
 template <class F, int kStages, bool kStaged>
-nvq_status launch_gemm_cfg(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mb256, const GemmArgs& ga,
-                           int32_t groups, int64_t N, cudaStream_t st)
+nvq_status launch_gemm_cfg(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mb256, const CUtensorMap& mo,
+                           const GemmArgs& ga, int32_t groups, int64_t N, cudaStream_t st)
 {
     constexpr int kSmem = Geo<F>::kSmemBytes(kStages, kStaged);
     static_assert(kSmem + 8 * 1024 <= 227 * 1024, "shared memory of the GEMM");
@@ -795,20 +842,28 @@ nvq_status launch_gemm_cfg(const CUtensorMap& ma, const CUtensorMap& mb, const C
     // an upper bound of the tiles: every group adds at most one partial 128-row tile
     const int64_t max_tiles = (int64_t)(ga.total_mtiles_max + groups) * (N / kBN);
     const int ctas = (int)(max_tiles < sms ? max_tiles : sms);
-    gemm_kernel<F, kStages, kStaged><<<ctas, kThreads, kSmem, st>>>(ma, mb, mb256, ga);
+    gemm_kernel<F, kStages, kStaged><<<ctas, kThreads, kSmem, st>>>(ma, mb, mb256, mo, ga);
     NVQ_LAUNCH_CHECK("gemm_kernel");
     return NVQ_OK;
 }
 
 // The routing-weight epilogue (the down projection: a full 128 x 256 bf16 tile per output,
-// written to memory once and read back by the combine) stores through shared memory with a
-// 3-deep operand ring; the other epilogues keep the 4-deep ring.
+// written to memory once and read back by the combine) stores through shared memory, by TMA,
+// with a 3-deep operand ring; the other epilogues keep the 4-deep ring and plain stores.
 template <class F>
-nvq_status launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mb256, const GemmArgs& ga, int32_t groups,
+nvq_status launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mb256, GemmArgs ga, int32_t groups,
                        int64_t N, cudaStream_t st)
 {
-    if (ga.epilogue == NVQ_EPI_ROW_SCALE) return launch_gemm_cfg<F, 3, true>(ma, mb, mb256, ga, groups, N, st);
-    return launch_gemm_cfg<F, kStagesMax, false>(ma, mb, mb256, ga, groups, N, st);
+    CUtensorMap mo;
+    memset(&mo, 0, sizeof(mo));
+    ga.out_tma = 0;
+    if (ga.epilogue == NVQ_EPI_ROW_SCALE) {
+        nvq_status s = make_out_map(&mo, ga.out, N, ga.gr.total_rows, ga.ldo);
+        if (s != NVQ_OK) return s;
+        ga.out_tma = 1;
+        return launch_gemm_cfg<F, 3, true>(ma, mb, mb256, mo, ga, groups, N, st);
+    }
+    return launch_gemm_cfg<F, kStagesMax, false>(ma, mb, mb256, mo, ga, groups, N, st);
 }
 
 // Arguments shared by both entries.
@@ -852,6 +907,7 @@ static GemmArgs gemm_args(int32_t groups, const int64_t* grp_off, const int64_t*
     ga.status = device_status_ptr();
     ga.wait_limit = wait_limit();
     ga.out_ts = nullptr;
+    ga.out_tma = 0;
     return ga;
 }
 
