@@ -203,28 +203,38 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
     }
     __syncthreads();
     if (out_codes != nullptr) {
-        // four rows per warp at a time: all their loads are in flight before the stores
-        const int nvec = (int)(byte_end / 16);  // 16-byte vectors of codes
-        const bool tail8 = (byte_end % 16) != 0;
-        for (int r4 = warp * 4; r4 < 128; r4 += 32) {
-            for (int v0 = (int)(byte0 / 16); v0 < nvec; v0 += 32) {
-                const int v = v0 + lane;
-                uint4 val[4];
+        // the block's 128 rows x nv 16-byte vectors as one flat range, consecutive threads on
+        // consecutive vectors of a row: every lane busy, eight loads in flight per thread before
+        // their stores
+        const int v_begin = (int)(byte0 / 16);
+        const int nv = (int)(byte_end / 16) - v_begin;  // 16-byte vectors per row
+        const int total = 128 * nv;
+        for (int i0 = tid; i0 < total; i0 += 8 * 256) {
+            uint4 val[8];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int sr = src[r4 + i];
-                    const uint4* sp = reinterpret_cast<const uint4*>(codes + (int64_t)(sr >= 0 ? sr : 0) * ld_codes);
-                    val[i] = (sr >= 0 && v < nvec) ? __ldg(sp + v) : make_uint4(0, 0, 0, 0);
+            for (int j = 0; j < 8; ++j) {
+                const int i = i0 + j * 256;
+                val[j] = make_uint4(0, 0, 0, 0);
+                if (i < total) {
+                    const int r = i / nv, v = v_begin + (i - r * nv);
+                    const int sr = src[r];
+                    if (sr >= 0) val[j] = __ldg(reinterpret_cast<const uint4*>(codes + (int64_t)sr * ld_codes) + v);
                 }
+            }
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    if (v < nvec) reinterpret_cast<uint4*>(out_codes + (r0 + r4 + i) * ld_out)[v] = val[i];
+            for (int j = 0; j < 8; ++j) {
+                const int i = i0 + j * 256;
+                if (i < total) {
+                    const int r = i / nv, v = v_begin + (i - r * nv);
+                    reinterpret_cast<uint4*>(out_codes + (r0 + r) * ld_out)[v] = val[j];
+                }
             }
-            if (tail8 && lane < 4) {
-                const int sr = src[r4 + lane];
-                const uint2* sp = reinterpret_cast<const uint2*>(codes + (int64_t)(sr >= 0 ? sr : 0) * ld_codes);
-                reinterpret_cast<uint2*>(out_codes + (r0 + r4 + lane) * ld_out)[nvec * 2] = sr >= 0 ? sp[nvec * 2] : make_uint2(0, 0);
-            }
+        }
+        if ((byte_end % 16) != 0 && tid < 128) {  // the 8-byte piece at the end of each row
+            const int64_t off = byte_end - 8;
+            const int sr = src[tid];
+            *reinterpret_cast<uint2*>(out_codes + (r0 + tid) * ld_out + off) =
+                sr >= 0 ? *reinterpret_cast<const uint2*>(codes + (int64_t)sr * ld_codes + off) : make_uint2(0, 0);
         }
     }
     // scales: four words per thread at a time, loads before stores
