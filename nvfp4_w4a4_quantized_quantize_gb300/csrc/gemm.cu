@@ -680,8 +680,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     } else {
         // ---------------- epilogue: warps 6..13; TMEM lane quarter = warp % 4, column half =
         // (warp - 6) / 4.  The accumulator is read in 32-column pieces, packed to bf16 as it
-        // comes, and released after the last piece; the global stores overlap the next tile's
-        // MMAs.
+        // comes, and released once the last piece is in registers; the last piece's arithmetic
+        // and the global stores overlap the next tile's MMAs.
         const int quarter = warp & 3;
         const int half = (warp - kFirstEpiWarp) >> 2;
         const int r_in_tile = quarter * 32 + lane;
@@ -724,6 +724,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 for (int c = 0; c < 2; ++c) {
                     float g[32], u[32];
                     tmem_ld32x2(tacc + half * 64 + 32 * c, tacc + kBN / 2 + half * 64 + 32 * c, g, u);
+                    if (c == 1) {  // released once the last piece is in registers
+                        tc_fence_before();
+                        mbar_arrive(&acc_empty);
+                    }
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const float g0 = __fmul_rn(alpha, g[2 * i]), u0 = __fmul_rn(alpha, u[2 * i]);
@@ -731,8 +735,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         pk[16 * c + i] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u0, __fdividef(g1, 1.0f + __expf(-g1)) * u1);
                     }
                 }
-                tc_fence_before();
-                mbar_arrive(&acc_empty);
                 if (valid) store_row<32>(a.out + grow * a.ldo + (int64_t)T.nt * (kBN / 2) + half * 64, pk, wide);
                 if (a.out_ts) warp_amax_to(valid ? amax_packed<32>(pk) : 0.0f, &a.out_ts[T.g].amax);
             } else {
@@ -742,6 +744,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 for (int c = 0; c < 2; ++c) {
                     float v0[32], v1[32];
                     tmem_ld32x2(tacc + half * (kBN / 2) + 64 * c, tacc + half * (kBN / 2) + 64 * c + 32, v0, v1);
+                    if (c == 1) {  // released once the last piece is in registers
+                        tc_fence_before();
+                        mbar_arrive(&acc_empty);
+                    }
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         float y0 = __fmul_rn(alpha, v0[2 * i]), y1 = __fmul_rn(alpha, v0[2 * i + 1]);
@@ -753,8 +759,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         pk[32 * c + 16 + i] = pack_bf16x2(z0, z1);
                     }
                 }
-                tc_fence_before();
-                mbar_arrive(&acc_empty);
                 if constexpr (kStaged) {
                     const int rvalid = T.rows - quarter * 32;  // rows of this warp's 32 inside the tile
 #pragma unroll
