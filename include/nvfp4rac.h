@@ -90,8 +90,17 @@ const char* nvq_last_error(void);
 
 /* Reads and clears the device status word of the current device (synchronises the stream).
  * *status receives the first error a kernel recorded since the last read: NVQ_OK, or
- * NVQ_ERR_TIMEOUT (a bounded wait ran out), or NVQ_ERR_ARG (moe_dispatch met an expert id
- * outside [0, groups)); *where identifies the wait or check. */
+ * NVQ_ERR_TIMEOUT (a bounded wait ran out), or NVQ_ERR_ARG (a caller-supplied index outside its
+ * range); *where identifies the wait or check.  The index checks, made before any access
+ * through the index:
+ *   41  moe_dispatch: an expert id outside [0, groups) (the pair is left out of the routing);
+ *   42  activation tails (rac_select_quantize, rac_residual_tail): a channel of idx outside
+ *       [0, K) (channel 0 is read instead);
+ *   43  weight tails (rac_weight_tail, w4a4_rac_grouped_gemm with idx): the same;
+ *   44  rac_reconstruct: the same (the tail value is added to column 0 instead);
+ *   45  nvfp4_gather_rows / fp8_gather_rows: row_src[i] / topk >= src_rows (row i is written as
+ *       a padding row).
+ * The output of a call that recorded NVQ_ERR_ARG is meaningless; no access leaves its operands. */
 nvq_status nvq_device_status(void* stream, int32_t* status, int32_t* where);
 
 /* Sets the bound of every device-side wait, in GPU clock cycles (default 2^32, about 2 s; any

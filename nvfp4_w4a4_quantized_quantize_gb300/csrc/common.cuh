@@ -12,6 +12,7 @@
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "../../include/nvfp4rac.h"
@@ -37,6 +38,17 @@ int tail_path();                      // nvq_tail_path set by nvq_set_tail_path
             return code;                        \
         }                                       \
     } while (0)
+
+// NVTX range around one API call, named after the entry point: Nsight Systems and Nsight
+// Compute (--nvtx) show each call's kernels under it.  With no tool attached a push or pop is a
+// test of one function pointer.
+struct TraceRange {
+    explicit TraceRange(const char* name) { nvtxRangePushA(name); }
+    ~TraceRange() { nvtxRangePop(); }
+    TraceRange(const TraceRange&) = delete;
+    TraceRange& operator=(const TraceRange&) = delete;
+};
+#define NVQ_TRACE(name) ::nvq::TraceRange nvq_trace_range_(name)
 
 #define NVQ_LAUNCH_CHECK(what)                                             \
     do {                                                                   \
@@ -312,6 +324,22 @@ __device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c)
 
 // Bounded mbarrier / flag waits record this in the device status word.
 __device__ __forceinline__ void report_timeout(DeviceStatus* st, int where) { report_status(st, NVQ_ERR_TIMEOUT, where); }
+
+// A channel index read from a caller's selection list (idx): inside [0, K) it is returned as
+// is; outside, the device status records NVQ_ERR_ARG at `where` and channel 0 is used instead,
+// so that no load leaves the operand (the call's output is then meaningless, and the status
+// says so).  One unsigned compare per index.
+constexpr int kWhereBadChannelAct = 42;     // act_tail_kernel / row_tail_kernel<true>
+constexpr int kWhereBadChannelWeight = 43;  // weight tails
+constexpr int kWhereBadChannelRecon = 44;   // rac_reconstruct
+__device__ __forceinline__ int checked_channel(int j, int K, DeviceStatus* st, int where)
+{
+    if ((unsigned)j >= (unsigned)K) {
+        report_status(st, NVQ_ERR_ARG, where);
+        return 0;
+    }
+    return j;
+}
 
 // Bound of the wait, after another wait of the CTA ran out, for the asynchronous copies it
 // already issued to land before it exits (they complete within microseconds; this bound does

@@ -144,6 +144,7 @@ extern "C" int64_t nvq_fp8_sf_cols(int64_t K) { return ((K / 32) + 3) / 4 * 4; }
 extern "C" nvq_status fp8_quantize(const void* x, int64_t rows, int64_t K, int64_t ldx, int32_t tile_rows, uint8_t* codes,
                                    int64_t ld_codes, uint8_t* sf, int64_t sf_cols, void* stream)
 {
+    NVQ_TRACE("fp8_quantize");
     static const char* fn = "fp8_quantize";
     NVQ_CHECK_ARG(x && codes && sf, NVQ_ERR_ARG, "%s: null pointer argument", fn);
     NVQ_CHECK_ARG(tile_rows == 1 || tile_rows == 128, NVQ_ERR_ARG, "%s: tile_rows must be 1 or 128", fn);

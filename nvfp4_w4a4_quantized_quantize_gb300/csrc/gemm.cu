@@ -935,6 +935,7 @@ extern "C" nvq_status w4a4_rac_grouped_gemm(int32_t groups, const int64_t* grp_o
                                             const float* row_w, void* out, int64_t ldo, nvq_tensor_scale* out_tscale,
                                             void* stream)
 {
+    NVQ_TRACE("w4a4_rac_grouped_gemm");
     static const char* fn = "w4a4_rac_grouped_gemm";
     NVQ_CHECK_ARG(a_codes && a_sf && a_tscale && b_codes && b_sf && b_tscale && out, NVQ_ERR_ARG, "%s: null pointer argument", fn);
     nvq_status s = check_gemm_common(fn, groups, grp_off, rows, N, epilogue, row_w, ldo, out);
@@ -986,6 +987,7 @@ extern "C" nvq_status fp8_blockscaled_grouped_gemm(int32_t groups, const int64_t
                                                    int32_t epilogue, const float* row_w, void* out, int64_t ldo,
                                                    void* stream)
 {
+    NVQ_TRACE("fp8_blockscaled_grouped_gemm");
     static const char* fn = "fp8_blockscaled_grouped_gemm";
     NVQ_CHECK_ARG(a_codes && a_sf && b_codes && b_sf && out, NVQ_ERR_ARG, "%s: null pointer argument", fn);
     nvq_status s = check_gemm_common(fn, groups, grp_off, rows, N, epilogue, row_w, ldo, out);

@@ -24,6 +24,7 @@ static constexpr int kWarpsPerCta = 2;  // 256 CTAs for the 512 units of 131072 
 // An expert id outside [0, G) is a caller error: the pair is left out of the routing (its
 // row_of entry is -1, which combine skips) and the device status word records NVQ_ERR_ARG.
 static constexpr int kWhereBadExpertId = 41;
+static constexpr int kWhereBadSourceRow = 45;  // gather: row_src[i] / topk >= src_rows
 
 // Per-unit histogram of experts: counts[unit][G].
 __global__ void dispatch_hist_kernel(const int32_t* __restrict__ ids, int64_t n, int G, int32_t* __restrict__ counts,
@@ -192,14 +193,19 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
                                                           const int32_t* __restrict__ row_src, int topk, int64_t byte0,
                                                           int64_t byte_end, int atom0, int atom_end,
                                                           uint8_t* __restrict__ out_codes, int64_t ld_out,
-                                                          uint8_t* __restrict__ out_sf)
+                                                          uint8_t* __restrict__ out_sf, int64_t src_rows, DeviceStatus* dst)
 {
     __shared__ int src[128];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x;
     const int64_t r0 = (int64_t)blockIdx.x * 128;
     if (tid < 128) {
         const int32_t s = row_src[r0 + tid];
-        src[tid] = s >= 0 ? s / topk : -1;
+        int v = s >= 0 ? s / topk : -1;
+        if (v >= src_rows) {  // a row map not made for this source: recorded, and the row is left as padding
+            report_status(dst, NVQ_ERR_ARG, kWhereBadSourceRow);
+            v = -1;
+        }
+        src[tid] = v;
     }
     __syncthreads();
     if (out_codes != nullptr) {
@@ -308,6 +314,7 @@ extern "C" nvq_status moe_dispatch(const int32_t* topk_ids, const float* topk_w,
                                    int64_t* row_of, float* row_w, int64_t capacity, void* workspace,
                                    size_t workspace_bytes, void* stream)
 {
+    NVQ_TRACE("moe_dispatch");
     NVQ_CHECK_ARG(topk_ids && grp_off && grp_rows && row_src && row_of && workspace, NVQ_ERR_ARG,
                   "moe_dispatch: null pointer argument");
     NVQ_CHECK_ARG(tokens >= 1 && topk >= 1 && topk <= 64 && tokens * topk <= (1ll << 26), NVQ_ERR_SHAPE,
@@ -344,6 +351,7 @@ extern "C" nvq_status nvfp4_gather_rows(const uint8_t* codes, int64_t ld_codes, 
                                         int64_t ktot, int64_t col0, uint8_t* out_codes, int64_t ld_out, uint8_t* out_sf,
                                         void* stream)
 {
+    NVQ_TRACE("nvfp4_gather_rows");
     NVQ_CHECK_ARG(codes && sf && row_src && out_sf, NVQ_ERR_ARG, "nvfp4_gather_rows: null pointer argument");
     NVQ_CHECK_ARG(ktot >= 16 && ktot % 16 == 0 && sf_cols >= ktot / 16 && sf_cols % 4 == 0, NVQ_ERR_SHAPE,
                   "nvfp4_gather_rows: bad ktot / sf_cols");
@@ -356,9 +364,11 @@ extern "C" nvq_status nvfp4_gather_rows(const uint8_t* codes, int64_t ld_codes, 
                   NVQ_ERR_ALIGN, "nvfp4_gather_rows: codes need 16-byte aligned rows");
     set_error("");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    DeviceStatus* dst = device_status_ptr();
+    NVQ_CHECK_ARG(dst, NVQ_ERR_CUDA, "nvfp4_gather_rows: device status word unavailable");
     gather_rows_kernel<<<(unsigned)(capacity / 128), 256, 0, st>>>(codes, ld_codes, sf, sf_cols, row_src, topk, col0 / 2,
                                                                    ktot / 2, (int)(col0 / 64), (int)((ktot + 63) / 64),
-                                                                   out_codes, ld_out, out_sf);
+                                                                   out_codes, ld_out, out_sf, src_rows, dst);
     NVQ_LAUNCH_CHECK("gather_rows_kernel");
     return NVQ_OK;
 }
@@ -367,6 +377,7 @@ extern "C" nvq_status fp8_gather_rows(const uint8_t* codes, int64_t ld_codes, co
                                       int64_t src_rows, const int32_t* row_src, int32_t topk, int64_t capacity, int64_t K,
                                       uint8_t* out_codes, int64_t ld_out, uint8_t* out_sf, void* stream)
 {
+    NVQ_TRACE("fp8_gather_rows");
     NVQ_CHECK_ARG(codes && sf && row_src && out_codes && out_sf, NVQ_ERR_ARG, "fp8_gather_rows: null pointer argument");
     NVQ_CHECK_ARG(K >= 32 && K % 32 == 0 && sf_cols >= nvq_fp8_sf_cols(K) && sf_cols % 4 == 0, NVQ_ERR_SHAPE,
                   "fp8_gather_rows: K must be a positive multiple of 32 and sf_cols >= nvq_fp8_sf_cols(K)");
@@ -377,8 +388,11 @@ extern "C" nvq_status fp8_gather_rows(const uint8_t* codes, int64_t ld_codes, co
                   NVQ_ERR_ALIGN, "fp8_gather_rows: codes need 16-byte aligned rows");
     set_error("");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    DeviceStatus* dst = device_status_ptr();
+    NVQ_CHECK_ARG(dst, NVQ_ERR_CUDA, "fp8_gather_rows: device status word unavailable");
     gather_rows_kernel<<<(unsigned)(capacity / 128), 256, 0, st>>>(codes, ld_codes, sf, sf_cols, row_src, topk, 0, K, 0,
-                                                                   (int)((K + 127) / 128), out_codes, ld_out, out_sf);
+                                                                   (int)((K + 127) / 128), out_codes, ld_out, out_sf,
+                                                                   src_rows, dst);
     NVQ_LAUNCH_CHECK("gather_rows_kernel");
     return NVQ_OK;
 }
@@ -386,6 +400,7 @@ extern "C" nvq_status fp8_gather_rows(const uint8_t* codes, int64_t ld_codes, co
 extern "C" nvq_status moe_combine(const void* y, int64_t ldy, const int64_t* row_of, int64_t tokens, int32_t topk,
                                   int64_t hidden, void* out, int64_t ldo, void* stream)
 {
+    NVQ_TRACE("moe_combine");
     NVQ_CHECK_ARG(y && row_of && out, NVQ_ERR_ARG, "moe_combine: null pointer argument");
     NVQ_CHECK_ARG(tokens >= 1 && tokens <= (1ll << 31) - 1 && topk >= 1 && hidden >= 8 && hidden % 8 == 0, NVQ_ERR_SHAPE,
                   "moe_combine: hidden must be a positive multiple of 8");
@@ -442,6 +457,7 @@ extern "C" nvq_status moe_dispatch_static_scratch(const int32_t* topk_ids, const
                                                   int32_t* row_src, int64_t* row_of, float* row_w, int64_t capacity,
                                                   void* stream)
 {
+    NVQ_TRACE("moe_dispatch_static_scratch");
     NVQ_CHECK_ARG(topk_ids && grp_off && grp_rows && row_src && row_of, NVQ_ERR_ARG,
                   "moe_dispatch_static_scratch: null pointer argument");
     NVQ_CHECK_ARG(tokens >= 1 && topk >= 1 && topk <= 64 && tokens * topk <= (1ll << 26), NVQ_ERR_SHAPE,

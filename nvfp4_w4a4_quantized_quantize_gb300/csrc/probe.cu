@@ -103,6 +103,7 @@ using namespace nvq;
  * issues.  Synchronous: returns the achieved TFLOP/s in *tflops. */
 extern "C" nvq_status nvq_fp4_mma_rate(int32_t mmas_per_sm, int32_t with_cp, float* tflops, void* stream)
 {
+    NVQ_TRACE("nvq_fp4_mma_rate");
     NVQ_CHECK_ARG(tflops && mmas_per_sm >= 16 && mmas_per_sm <= (1 << 20), NVQ_ERR_ARG, "nvq_fp4_mma_rate: bad arguments");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int dev = 0, sms = 148;

@@ -693,6 +693,7 @@ extern "C" nvq_status nvfp4_quantize(const void* x, int64_t rows, int64_t K, int
                                      uint8_t* sf, int64_t sf_cols, int32_t zero_pad, nvq_tensor_scale* tscale,
                                      uint64_t* scores, int32_t amax_given, void* stream)
 {
+    NVQ_TRACE("nvfp4_quantize");
     NVQ_CHECK_ARG(x && codes && sf && tscale, NVQ_ERR_ARG, "nvfp4_quantize: null pointer argument");
     NVQ_CHECK_ARG(rows >= 1 && rows <= (1ll << 24), NVQ_ERR_SHAPE, "nvfp4_quantize: rows=%lld outside [1, 2^24]", (long long)rows);
     NVQ_CHECK_ARG(K >= 16 && K <= 8192 && K % 16 == 0, NVQ_ERR_SHAPE, "nvfp4_quantize: K=%lld must be a multiple of 16 in [16, 8192]", (long long)K);
@@ -713,6 +714,7 @@ extern "C" nvq_status weight_qdq(const void* w, int32_t groups, int64_t N, int64
                                  int64_t ld_codes, uint8_t* sf, int64_t sf_cols, nvq_tensor_scale* tscale, void* w_hat,
                                  int32_t w_hat_dtype, void* stream)
 {
+    NVQ_TRACE("weight_qdq");
     NVQ_CHECK_ARG(w && codes && sf && tscale, NVQ_ERR_ARG, "weight_qdq: null pointer argument");
     NVQ_CHECK_ARG(w_hat_dtype == NVQ_BF16 || w_hat_dtype == NVQ_F32, NVQ_ERR_ARG, "weight_qdq: w_hat_dtype must be NVQ_BF16 or NVQ_F32");
     NVQ_CHECK_ARG(groups >= 1 && groups <= 4096, NVQ_ERR_SHAPE, "weight_qdq: groups=%d outside [1, 4096]", groups);
@@ -733,6 +735,7 @@ extern "C" nvq_status weight_qdq(const void* w, int32_t groups, int64_t N, int64
 extern "C" nvq_status nvfp4_amax(const void* x, int64_t rows, int64_t K, int64_t ldx, const int64_t* grp_off,
                                  const int64_t* grp_rows, int32_t groups, nvq_tensor_scale* tscale, void* stream)
 {
+    NVQ_TRACE("nvfp4_amax");
     NVQ_CHECK_ARG(x && tscale, NVQ_ERR_ARG, "nvfp4_amax: null pointer argument");
     NVQ_CHECK_ARG(rows >= 1 && rows <= (1ll << 24), NVQ_ERR_SHAPE, "nvfp4_amax: rows=%lld outside [1, 2^24]", (long long)rows);
     NVQ_CHECK_ARG(K >= 16 && K <= 8192 && K % 16 == 0, NVQ_ERR_SHAPE, "nvfp4_amax: K=%lld must be a multiple of 16 in [16, 8192]", (long long)K);
@@ -750,6 +753,7 @@ extern "C" nvq_status nvfp4_amax(const void* x, int64_t rows, int64_t K, int64_t
 
 extern "C" nvq_status nvq_check_block_scale_division(uint32_t* result, void* stream)
 {
+    NVQ_TRACE("nvq_check_block_scale_division");
     NVQ_CHECK_ARG(result, NVQ_ERR_ARG, "nvq_check_block_scale_division: null result pointer");
     NVQ_CHECK_ARG(aligned(result, 4), NVQ_ERR_ALIGN, "nvq_check_block_scale_division: result must be 4-byte aligned");
     set_error("");

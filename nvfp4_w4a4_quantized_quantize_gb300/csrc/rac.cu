@@ -196,7 +196,8 @@ __device__ __forceinline__ float ld_bf16_last_use(const __nv_bfloat16* p, uint64
 __global__ void __launch_bounds__(512) act_tail_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, int K, int k,
                                                        Groups gr, const nvq_tensor_scale* __restrict__ ts,
                                                        const int32_t* __restrict__ idx, uint8_t* __restrict__ codes,
-                                                       int64_t ld_codes, uint8_t* __restrict__ sf, int64_t sf_cols, int bsplit)
+                                                       int64_t ld_codes, uint8_t* __restrict__ sf, int64_t sf_cols, int bsplit,
+                                                       DeviceStatus* dst)
 {
     __shared__ float eb_tab[128], db_tab[128];
     __shared__ int s_sel[512];
@@ -218,7 +219,7 @@ __global__ void __launch_bounds__(512) act_tail_kernel(const __nv_bfloat16* __re
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     if (sel_smem)
-        for (int c = tid; c < k; c += blockDim.x) s_sel[c] = idx[(int64_t)g0 * k + c];
+        for (int c = tid; c < k; c += blockDim.x) s_sel[c] = checked_channel(idx[(int64_t)g0 * k + c], K, dst, kWhereBadChannelAct);
     __syncthreads();
 
     const int64_t row = tile_row + t;
@@ -244,7 +245,7 @@ __global__ void __launch_bounds__(512) act_tail_kernel(const __nv_bfloat16* __re
         uint32_t sb[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const int j = (own && sel_smem) ? s_sel[b * 16 + i] : sel_g[b * 16 + i];
+            const int j = (own && sel_smem) ? s_sel[b * 16 + i] : checked_channel(sel_g[b * 16 + i], K, dst, kWhereBadChannelAct);
             xv[i] = ld_bf16_last_use(xr + j, pol);
             sb[i] = sf[sf_offset(row, j >> 4, sf_cols)];
         }
@@ -289,7 +290,8 @@ __global__ void __launch_bounds__(512) act_tail_kernel(const __nv_bfloat16* __re
 __global__ void __launch_bounds__(256) weight_tail_kernel(uint8_t* __restrict__ codes, int64_t ld_codes,
                                                            uint8_t* __restrict__ sf, int64_t sf_cols, int64_t N, int K,
                                                            int k, int G, const nvq_tensor_scale* __restrict__ ts,
-                                                           const int32_t* __restrict__ idx, int idx_per_group)
+                                                           const int32_t* __restrict__ idx, int idx_per_group,
+                                                           DeviceStatus* dst)
 {
     const int nbt = k / 16;
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -304,7 +306,7 @@ __global__ void __launch_bounds__(256) weight_tail_kernel(uint8_t* __restrict__ 
     float wv[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        const int j = sel[b * 16 + i];
+        const int j = checked_channel(sel[b * 16 + i], K, dst, kWhereBadChannelWeight);
         const uint32_t c = (cr[j >> 1] >> ((j & 1) * 4)) & 0xfu;
         const uint32_t sb = sf[sf_offset(row, j >> 4, sf_cols)];
         wv[i] = __fmul_rn(e2m1_value(c), __fmul_rn(e4m3_value(sb), s_dec));
@@ -330,7 +332,7 @@ constexpr int kWtMaxSplit = 4;
 __global__ void __launch_bounds__(kWtRows * kWtMaxSplit) weight_tail_cm_kernel(
     uint8_t* __restrict__ codes, int64_t ld_codes, uint8_t* __restrict__ sf, int64_t sf_cols, int64_t N, int K, int k,
     const nvq_tensor_scale* __restrict__ ts, const int32_t* __restrict__ idx, int idx_per_group,
-    const uint8_t* __restrict__ cm_codes, const uint8_t* __restrict__ cm_sf)
+    const uint8_t* __restrict__ cm_codes, const uint8_t* __restrict__ cm_sf, DeviceStatus* dst)
 {
     extern __shared__ __align__(16) uint8_t wt_smem[];
     const int kc = k < kWtChunk ? k : kWtChunk;   // channels staged at a time
@@ -352,7 +354,7 @@ __global__ void __launch_bounds__(kWtRows * kWtMaxSplit) weight_tail_cm_kernel(
     // stage: per channel 2 x 16 code bytes + 4 x 16 scale bytes
     for (int w = threadIdx.x; w < cnt * 6; w += nthr) {
         const int c = w / 6, q = w % 6;
-        const int j = sel[c0 + c];
+        const int j = checked_channel(sel[c0 + c], K, dst, kWhereBadChannelWeight);
         uint4 v;
         if (q < 2)
             v = __ldg(reinterpret_cast<const uint4*>(cm_codes + ((int64_t)g * K + j) * (N / 2) + n0 / 2) + q);
@@ -457,7 +459,7 @@ __global__ void __launch_bounds__(kRowThreads)
     row_tail_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, uint8_t* __restrict__ codes, int64_t ld_codes,
                     uint8_t* __restrict__ sf, int64_t sf_cols, int K, int k, Groups gr,
                     const nvq_tensor_scale* __restrict__ ts, const int32_t* __restrict__ idx, int idx_per_group,
-                    int idx_vec)
+                    int idx_vec, DeviceStatus* dst)
 {
     extern __shared__ __align__(16) float rt_smem[];
     const int R = row_tile_rows(K);
@@ -531,6 +533,8 @@ __global__ void __launch_bounds__(kRowThreads)
 #pragma unroll
             for (int i = 0; i < 16; ++i) j[i] = __ldg(sel + i);
         }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) j[i] = checked_channel(j[i], K, dst, kResidual ? kWhereBadChannelAct : kWhereBadChannelWeight);
         const float* src = rt_smem + (size_t)r * stride;
         float v[16];
 #pragma unroll
@@ -562,8 +566,11 @@ nvq_status launch_row_tail(const void* x, int64_t ldx, uint8_t* codes, int64_t l
     const int R = row_tile_rows(K);
     const int64_t tiles = (gr.total_rows + R - 1) / R;
     const int idx_vec = aligned(idx, 16) ? 1 : 0;  // per-group offsets g * k * 4 bytes keep 16-byte alignment
+    DeviceStatus* dst = device_status_ptr();
+    NVQ_CHECK_ARG(dst, NVQ_ERR_CUDA, "row tail: device status word unavailable");
     row_tail_kernel<kResidual><<<(unsigned)tiles, kRowThreads, row_tail_smem(K), st>>>(
-        static_cast<const __nv_bfloat16*>(x), ldx, codes, ld_codes, sf, sf_cols, K, k, gr, ts, idx, idx_per_group, idx_vec);
+        static_cast<const __nv_bfloat16*>(x), ldx, codes, ld_codes, sf, sf_cols, K, k, gr, ts, idx, idx_per_group, idx_vec,
+        dst);
     NVQ_LAUNCH_CHECK(kResidual ? "row_tail_kernel<residual>" : "row_tail_kernel<weight>");
     return NVQ_OK;
 }
@@ -574,8 +581,10 @@ nvq_status weight_tail_impl(uint8_t* codes, int64_t ld_codes, uint8_t* sf, int64
     if (k == 0) return NVQ_OK;
     const int64_t total = (int64_t)G * N * (k / 16);
     const int threads = 256;
+    DeviceStatus* dst = device_status_ptr();
+    NVQ_CHECK_ARG(dst, NVQ_ERR_CUDA, "weight tail: device status word unavailable");
     weight_tail_kernel<<<(unsigned)((total + threads - 1) / threads), threads, 0, st>>>(
-        codes, ld_codes, sf, sf_cols, N, K, k, G, ts, idx, idx_per_group);
+        codes, ld_codes, sf, sf_cols, N, K, k, G, ts, idx, idx_per_group, dst);
     NVQ_LAUNCH_CHECK("weight_tail_kernel");
     return NVQ_OK;
 }
@@ -625,8 +634,11 @@ static nvq_status launch_act_tail(const void* x, int64_t rows, int64_t K, int64_
     const int nbt = k > 0 ? k / 16 : 1;
     while (bsplit < nbt && bsplit < 8 && tiles * bsplit < (int64_t)sms * 8) bsplit *= 2;
     if (bsplit > nbt) bsplit = nbt;
+    DeviceStatus* dst = device_status_ptr();
+    NVQ_CHECK_ARG(dst, NVQ_ERR_CUDA, "act tail: device status word unavailable");
     act_tail_kernel<<<(unsigned)tiles, kTailRows * bsplit, 0, st>>>(static_cast<const __nv_bfloat16*>(x), ldx, (int)K,
-                                                                   k, gr, tscale, idx, codes, ld_codes, sf, sf_cols, bsplit);
+                                                                   k, gr, tscale, idx, codes, ld_codes, sf, sf_cols, bsplit,
+                                                                   dst);
     NVQ_LAUNCH_CHECK("act_tail_kernel");
     return NVQ_OK;
 }
@@ -636,6 +648,7 @@ extern "C" nvq_status rac_select_quantize(const void* x, int64_t rows, int64_t K
                                           const uint64_t* scores, int32_t k, uint8_t* codes, int64_t ld_codes,
                                           uint8_t* sf, int64_t sf_cols, int32_t* idx, void* stream)
 {
+    NVQ_TRACE("rac_select_quantize");
     nvq_status s = check_rac_args("rac_select_quantize", x, rows, K, ldx, grp_off, groups, tscale, k, codes, ld_codes, sf, sf_cols);
     if (s != NVQ_OK) return s;
     NVQ_CHECK_ARG(k == 0 || (scores && idx), NVQ_ERR_ARG, "rac_select_quantize: scores and idx are required when k > 0");
@@ -648,6 +661,7 @@ extern "C" nvq_status rac_select_quantize(const void* x, int64_t rows, int64_t K
 
 extern "C" nvq_status rac_select(const uint64_t* scores, int64_t K, int32_t groups, int32_t k, int32_t* idx, void* stream)
 {
+    NVQ_TRACE("rac_select");
     NVQ_CHECK_ARG(scores && idx, NVQ_ERR_ARG, "rac_select: null pointer argument");
     NVQ_CHECK_ARG(K >= 16 && K <= 8192 && K % 16 == 0, NVQ_ERR_SHAPE, "rac_select: K must be a multiple of 16 in [16, 8192]");
     NVQ_CHECK_ARG(k >= 16 && k <= K && k % 16 == 0, NVQ_ERR_SHAPE, "rac_select: k=%d must be a multiple of 16 in [16, K]", k);
@@ -661,6 +675,7 @@ extern "C" nvq_status rac_residual_tail(const void* x, int64_t rows, int64_t K, 
                                         const int32_t* idx, int32_t k, uint8_t* codes, int64_t ld_codes, uint8_t* sf,
                                         int64_t sf_cols, void* stream)
 {
+    NVQ_TRACE("rac_residual_tail");
     nvq_status s = check_rac_args("rac_residual_tail", x, rows, K, ldx, grp_off, groups, tscale, k, codes, ld_codes, sf, sf_cols);
     if (s != NVQ_OK) return s;
     NVQ_CHECK_ARG(k == 0 || idx, NVQ_ERR_ARG, "rac_residual_tail: idx is required when k > 0");
@@ -673,6 +688,7 @@ extern "C" nvq_status nvfp4_channel_major(int32_t groups, int64_t N, int64_t K, 
                                           const uint8_t* b_sf, int64_t b_sf_cols, uint8_t* cm_codes, uint8_t* cm_sf,
                                           void* stream)
 {
+    NVQ_TRACE("nvfp4_channel_major");
     NVQ_CHECK_ARG(b_codes && b_sf && cm_codes && cm_sf, NVQ_ERR_ARG, "nvfp4_channel_major: null pointer argument");
     NVQ_CHECK_ARG(groups >= 1 && groups <= 4096 && N >= 64 && N % 64 == 0 && (int64_t)groups * N <= (1ll << 24),
                   NVQ_ERR_SHAPE, "nvfp4_channel_major: N must be a positive multiple of 64 and groups*N <= 2^24");
@@ -696,6 +712,7 @@ extern "C" nvq_status rac_weight_tail(int32_t groups, int64_t N, int64_t K, int3
                                       int64_t b_sf_cols, const nvq_tensor_scale* b_tscale, const uint8_t* cm_codes,
                                       const uint8_t* cm_sf, void* stream)
 {
+    NVQ_TRACE("rac_weight_tail");
     NVQ_CHECK_ARG(idx && b_codes && b_sf && b_tscale, NVQ_ERR_ARG, "rac_weight_tail: null pointer argument");
     NVQ_CHECK_ARG(!cm_codes == !cm_sf, NVQ_ERR_ARG, "rac_weight_tail: give both channel-major arrays or neither");
     NVQ_CHECK_ARG(!cm_codes || N % 64 == 0, NVQ_ERR_SHAPE, "rac_weight_tail: the channel-major path needs N % 64 == 0");
@@ -717,8 +734,10 @@ extern "C" nvq_status rac_weight_tail(int32_t groups, int64_t N, int64_t K, int3
     const size_t smem = (size_t)(k < kWtChunk ? k : kWtChunk) * 96;
     const dim3 grid((unsigned)(N / kWtRows), (unsigned)groups, (unsigned)((k + kWtChunk - 1) / kWtChunk));
     const int split = k / 16 < kWtMaxSplit ? k / 16 : kWtMaxSplit;  // threads per row
+    DeviceStatus* dst = device_status_ptr();
+    NVQ_CHECK_ARG(dst, NVQ_ERR_CUDA, "rac_weight_tail: device status word unavailable");
     weight_tail_cm_kernel<<<grid, kWtRows * split, smem, st>>>(b_codes, ldb, b_sf, b_sf_cols, N, (int)K, k, b_tscale, idx,
-                                                      idx_per_group, cm_codes, cm_sf);
+                                                      idx_per_group, cm_codes, cm_sf, dst);
     NVQ_LAUNCH_CHECK("weight_tail_cm_kernel");
     return NVQ_OK;
 }

@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(kReconThreads)
 __global__ void __launch_bounds__(kReconThreads)
     add_tail_kernel(const uint8_t* __restrict__ codes, int64_t ld_codes, const uint8_t* __restrict__ sf,
                     int64_t sf_cols, const nvq_tensor_scale* __restrict__ ts, Groups gr, int64_t rows, int64_t K,
-                    int k, const int32_t* __restrict__ idx, float* __restrict__ out, int64_t ldo)
+                    int k, const int32_t* __restrict__ idx, float* __restrict__ out, int64_t ldo, DeviceStatus* dst)
 {
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= rows * k) return;
@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(kReconThreads)
     const uint32_t byte = codes[r * ld_codes + col / 2];
     const float2 a = e2m1x2_value(byte);
     const float v = __fmul_rn((p & 1) ? a.y : a.x, d_b);
-    float* o = out + r * ldo + idx[(int64_t)g * k + p];
+    float* o = out + r * ldo + checked_channel(idx[(int64_t)g * k + p], (int)K, dst, kWhereBadChannelRecon);
     *o = __fadd_rn(*o, v);
 }
 
@@ -80,6 +80,7 @@ extern "C" nvq_status rac_reconstruct(const uint8_t* codes, int64_t ld_codes, co
                                       const int32_t* idx, const int64_t* grp_off, const int64_t* grp_rows,
                                       int32_t groups, float* out, int64_t ldo, void* stream)
 {
+    NVQ_TRACE("rac_reconstruct");
     static const char* fn = "rac_reconstruct";
     NVQ_CHECK_ARG(codes && sf && tscale && out && (k == 0 || idx), NVQ_ERR_ARG, "%s: null pointer", fn);
     NVQ_CHECK_ARG(rows >= 0 && K >= 16 && K % 16 == 0 && groups >= 1, NVQ_ERR_SHAPE,
@@ -100,8 +101,10 @@ extern "C" nvq_status rac_reconstruct(const uint8_t* codes, int64_t ld_codes, co
     NVQ_LAUNCH_CHECK("rac_reconstruct: dequant_main_kernel");
     if (k > 0) {
         const int64_t n2 = rows * k;
+        DeviceStatus* dst = device_status_ptr();
+        NVQ_CHECK_ARG(dst, NVQ_ERR_CUDA, "%s: device status word unavailable", fn);
         add_tail_kernel<<<(unsigned)((n2 + kReconThreads - 1) / kReconThreads), kReconThreads, 0, s>>>(
-            codes, ld_codes, sf, sf_cols, tscale, gr, rows, K, k, idx, out, ldo);
+            codes, ld_codes, sf, sf_cols, tscale, gr, rows, K, k, idx, out, ldo, dst);
         NVQ_LAUNCH_CHECK("rac_reconstruct: add_tail_kernel");
     }
     return NVQ_OK;

@@ -49,3 +49,22 @@ def test_product_path_has_no_oracle_import():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 txt = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in txt and "from oracle" not in txt and "nvfp4_oracle" not in txt, f
+
+
+def test_every_launching_entry_opens_an_nvtx_range_named_after_it():
+    """Tracing: each entry point that launches kernels opens NVQ_TRACE("<its name>") as its
+    first statement, so a profiler's timeline groups every call's kernels under the call."""
+    csrc = os.path.join(ROOT, "nvfp4_w4a4_quantized_quantize_gb300", "csrc")
+    settings = {"nvq_set_wait_limit", "nvq_set_tail_path", "nvq_device_status"}  # launch nothing
+    seen = []
+    for f in sorted(os.listdir(csrc)):
+        if not f.endswith(".cu"):
+            continue
+        src = open(os.path.join(csrc, f)).read()
+        for m in re.finditer(r'extern "C" nvq_status (\w+)\([^{]*\)\s*\{\s*\n(\s*[^\n]*)', src):
+            name, first = m.group(1), m.group(2).strip()
+            if name in settings:
+                continue
+            seen.append(name)
+            assert first == f'NVQ_TRACE("{name}");', (f, name, first)
+    assert len(seen) >= 19 and "w4a4_rac_grouped_gemm" in seen and "nvfp4_quantize" in seen
