@@ -266,23 +266,48 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
     }
 }
 
-// CTA per token; each thread sums 8 columns over the slots in slot order.
+// CTA per token; each thread sums 8 columns over the slots in slot order.  The token's slot rows
+// are read once into shared memory; for up to kCombineSlots slots every thread then has all its
+// loads in flight before the first add (a runtime-bounded loop would wait on each slot's load
+// in turn).  Larger topk takes the same sum slot by slot.
+constexpr int kCombineSlots = 8;
+
+__device__ __forceinline__ void add_bf16x8(float* acc, const uint4& w)
+{
+    acc[0] = __fadd_rn(acc[0], bf16lo(w.x)); acc[1] = __fadd_rn(acc[1], bf16hi(w.x));
+    acc[2] = __fadd_rn(acc[2], bf16lo(w.y)); acc[3] = __fadd_rn(acc[3], bf16hi(w.y));
+    acc[4] = __fadd_rn(acc[4], bf16lo(w.z)); acc[5] = __fadd_rn(acc[5], bf16hi(w.z));
+    acc[6] = __fadd_rn(acc[6], bf16lo(w.w)); acc[7] = __fadd_rn(acc[7], bf16hi(w.w));
+}
+
 __global__ void combine_kernel(const __nv_bfloat16* __restrict__ y, int64_t ldy, const int64_t* __restrict__ row_of,
                                int topk, int64_t hidden, __nv_bfloat16* __restrict__ out, int64_t ldo)
 {
+    __shared__ int64_t s_row[kCombineSlots];
     const int64_t t = blockIdx.x;
+    const bool few = topk <= kCombineSlots;
+    if (few && threadIdx.x < topk) s_row[threadIdx.x] = row_of[t * topk + threadIdx.x];
+    __syncthreads();
     for (int64_t c = (int64_t)threadIdx.x * 8; c < hidden; c += (int64_t)blockDim.x * 8) {
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-        for (int s = 0; s < topk; ++s) {
-            const int64_t r = row_of[t * topk + s];
-            if (r < 0) continue;  // a pair dispatch left out (expert id out of range)
-            uint4 w = __ldg(reinterpret_cast<const uint4*>(y + r * ldy + c));
-            acc[0] = __fadd_rn(acc[0], bf16lo(w.x)); acc[1] = __fadd_rn(acc[1], bf16hi(w.x));
-            acc[2] = __fadd_rn(acc[2], bf16lo(w.y)); acc[3] = __fadd_rn(acc[3], bf16hi(w.y));
-            acc[4] = __fadd_rn(acc[4], bf16lo(w.z)); acc[5] = __fadd_rn(acc[5], bf16hi(w.z));
-            acc[6] = __fadd_rn(acc[6], bf16lo(w.w)); acc[7] = __fadd_rn(acc[7], bf16hi(w.w));
+        if (few) {
+            uint4 w[kCombineSlots];
+#pragma unroll
+            for (int s = 0; s < kCombineSlots; ++s) {
+                const int64_t r = s < topk ? s_row[s] : -1;
+                w[s] = r >= 0 ? __ldg(reinterpret_cast<const uint4*>(y + r * ldy + c)) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int s = 0; s < kCombineSlots; ++s)
+                if (s < topk && s_row[s] >= 0) add_bf16x8(acc, w[s]);  // slot order; a pair left out adds nothing
+        } else {
+            for (int s = 0; s < topk; ++s) {
+                const int64_t r = row_of[t * topk + s];
+                if (r < 0) continue;  // a pair dispatch left out (expert id out of range)
+                add_bf16x8(acc, __ldg(reinterpret_cast<const uint4*>(y + r * ldy + c)));
+            }
         }
         uint32_t pk[4];
 #pragma unroll

@@ -193,3 +193,28 @@ def test_host_pipeline_matches_direct_forward(L, use_graph):
     ms = pipe.run(x_h, torch.from_numpy(ids).pin_memory(), torch.from_numpy(tw).pin_memory(), out_h, 5)
     assert ms > 0 and L.device_status() == (0, 0)
     assert torch.equal(out_h.view(torch.int16), ref.cpu().view(torch.int16))
+
+
+@pytest.mark.parametrize("topk,hidden", [(1, 264), (3, 2048), (8, 2048), (9, 520), (12, 64)])
+def test_combine_slot_order_sum(L, topk, hidden):
+    """moe_combine against the oracle's slot-order fp32 sum, for topk up to the kernel's
+    all-loads-in-flight bound (8) and past it, with widths that leave threads idle.  Two pairs
+    are left out (row_of = -1, as moe_dispatch marks an out-of-range expert id); the oracle sees
+    those slots pointing at an all-zero row of y, which adds nothing."""
+    T = 37
+    n = T * topk
+    rows = n + 6
+    y_bits, _ = wl.activations(rows, hidden, seed=topk * 7 + hidden, n_outliers=2, outlier_gain=8.0)
+    zero_row = rows - 1
+    y_bits[zero_row] = 0
+    rng = np.random.default_rng(topk)
+    pos = rng.permutation(rows - 1)[:n].astype(np.int64)
+    out_pairs = [2, (5 * topk + 1) % n]
+    pos_gpu, pos_ref = pos.copy(), pos.copy()
+    pos_gpu[out_pairs] = -1
+    pos_ref[out_pairs] = zero_row
+    out = torch.empty(T, hidden, dtype=torch.bfloat16, device="cuda")
+    L.moe_combine(bf16_tensor(y_bits), torch.from_numpy(pos_gpu).cuda(), T, topk, hidden, out)
+    torch.cuda.synchronize()
+    assert L.device_status() == (0, 0)
+    assert np.array_equal(bf16_bits(out), oracle.moe_combine(y_bits, pos_ref, topk))
