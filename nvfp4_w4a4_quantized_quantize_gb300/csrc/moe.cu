@@ -182,7 +182,8 @@ __global__ void dispatch_scatter_kernel(const int32_t* __restrict__ ids, const f
     }
 }
 
-// CTA per 128-row block of the routed layout.  Codes: bytes [byte0, byte_end) of every row,
+// CTA (or gridDim.y CTAs, splitting its bytes, when there are few blocks) per 128-row block of
+// the routed layout.  Codes: bytes [byte0, byte_end) of every row,
 // 16-byte vectors (an 8-byte piece at the end when byte_end % 16 == 8).  Scales: the 512-byte
 // atoms [atom0, atom_end) of the row block (4 scale columns each), the block's output words
 // written in the blocked layout's own order (coalesced); each reads its word from the source
@@ -215,13 +216,16 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
         const int v_begin = (int)(byte0 / 16);
         const int nv = (int)(byte_end / 16) - v_begin;  // 16-byte vectors per row
         const int total = 128 * nv;
-        for (int i0 = tid; i0 < total; i0 += 8 * 256) {
+        // this CTA's share of the block (gridDim.y CTAs per block when blocks are few)
+        const int chunk = (total + (int)gridDim.y - 1) / (int)gridDim.y;
+        const int lo = (int)blockIdx.y * chunk, hi = min(total, lo + chunk);
+        for (int i0 = lo + tid; i0 < hi; i0 += 8 * 256) {
             uint4 val[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int i = i0 + j * 256;
                 val[j] = make_uint4(0, 0, 0, 0);
-                if (i < total) {
+                if (i < hi) {
                     const int r = i / nv, v = v_begin + (i - r * nv);
                     const int sr = src[r];
                     if (sr >= 0) val[j] = __ldg(reinterpret_cast<const uint4*>(codes + (int64_t)sr * ld_codes) + v);
@@ -230,13 +234,13 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int i = i0 + j * 256;
-                if (i < total) {
+                if (i < hi) {
                     const int r = i / nv, v = v_begin + (i - r * nv);
                     reinterpret_cast<uint4*>(out_codes + (r0 + r) * ld_out)[v] = val[j];
                 }
             }
         }
-        if ((byte_end % 16) != 0 && tid < 128) {  // the 8-byte piece at the end of each row
+        if ((byte_end % 16) != 0 && blockIdx.y == 0 && tid < 128) {  // the 8-byte piece at the end of each row
             const int64_t off = byte_end - 8;
             const int sr = src[tid];
             *reinterpret_cast<uint2*>(out_codes + (r0 + tid) * ld_out + off) =
@@ -245,9 +249,11 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restr
     }
     // scales: four words per thread at a time, loads before stores
     const int natoms = (int)(sf_cols / 4);
-    const int nwords = atom_end * 128;
+    const int wchunk = (atom_end * 128 - atom0 * 128 + (int)gridDim.y - 1) / (int)gridDim.y;
+    const int wlo = atom0 * 128 + (int)blockIdx.y * wchunk;
+    const int nwords = min(atom_end * 128, wlo + wchunk);  // this CTA's words end here
     uint32_t* outw = reinterpret_cast<uint32_t*>(out_sf + blockIdx.x * (int64_t)natoms * 512);
-    for (int w0 = atom0 * 128 + tid; w0 < nwords; w0 += 4 * 256) {
+    for (int w0 = wlo + tid; w0 < nwords; w0 += 4 * 256) {
         uint32_t val[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -317,6 +323,20 @@ __global__ void combine_kernel(const __nv_bfloat16* __restrict__ y, int64_t ldy,
         }
         *reinterpret_cast<uint4*>(out + t * ldo + c) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
+}
+
+// One CTA per 128-row block, or up to 8 per block (splitting its bytes) until there are about
+// four CTAs per SM: the decode shapes have few blocks (capacity 20352 rows: 159 blocks).
+static dim3 gather_grid(int64_t capacity)
+{
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t blocks = capacity / 128;
+    int64_t split = (4 * (int64_t)sms + blocks - 1) / blocks;
+    if (split < 1) split = 1;
+    if (split > 8) split = 8;
+    return dim3((unsigned)blocks, (unsigned)split);
 }
 
 }  // namespace nvq
@@ -391,7 +411,7 @@ extern "C" nvq_status nvfp4_gather_rows(const uint8_t* codes, int64_t ld_codes, 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     DeviceStatus* dst = device_status_ptr();
     NVQ_CHECK_ARG(dst, NVQ_ERR_CUDA, "nvfp4_gather_rows: device status word unavailable");
-    gather_rows_kernel<<<(unsigned)(capacity / 128), 256, 0, st>>>(codes, ld_codes, sf, sf_cols, row_src, topk, col0 / 2,
+    gather_rows_kernel<<<gather_grid(capacity), 256, 0, st>>>(codes, ld_codes, sf, sf_cols, row_src, topk, col0 / 2,
                                                                    ktot / 2, (int)(col0 / 64), (int)((ktot + 63) / 64),
                                                                    out_codes, ld_out, out_sf, src_rows, dst);
     NVQ_LAUNCH_CHECK("gather_rows_kernel");
@@ -415,7 +435,7 @@ extern "C" nvq_status fp8_gather_rows(const uint8_t* codes, int64_t ld_codes, co
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     DeviceStatus* dst = device_status_ptr();
     NVQ_CHECK_ARG(dst, NVQ_ERR_CUDA, "fp8_gather_rows: device status word unavailable");
-    gather_rows_kernel<<<(unsigned)(capacity / 128), 256, 0, st>>>(codes, ld_codes, sf, sf_cols, row_src, topk, 0, K, 0,
+    gather_rows_kernel<<<gather_grid(capacity), 256, 0, st>>>(codes, ld_codes, sf, sf_cols, row_src, topk, 0, K, 0,
                                                                    (int)((K + 127) / 128), out_codes, ld_out, out_sf,
                                                                    src_rows, dst);
     NVQ_LAUNCH_CHECK("gather_rows_kernel");
