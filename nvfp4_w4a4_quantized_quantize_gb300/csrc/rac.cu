@@ -329,12 +329,36 @@ constexpr int kWtRows = 64;
 constexpr int kWtChunk = 256;  // selected channels staged per pass (24 KB of shared memory)
 constexpr int kWtMaxSplit = 4;
 
+// quantize16 with the encode factor fl(S_enc / sb) read from a per-group table (eb_tab[sb],
+// 0 for sb = 0) instead of divided per block: the same scale byte and codes.
+__device__ __forceinline__ void quantize16_tab(const float* v, float s_enc, const float* eb_tab, uint32_t& sb,
+                                               uint32_t& code_lo, uint32_t& code_hi)
+{
+    const float amax_b = block_amax(v);
+    sb = e4m3(__fmul_rn(__fdiv_rn(amax_b, 6.0f), s_enc));
+    const float e_b = eb_tab[sb];
+    uint32_t c[8];
+    if (sb == 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            c[i] = ((__float_as_uint(v[2 * i]) >> 28) & 0x8u) | ((__float_as_uint(v[2 * i + 1]) >> 24) & 0x80u);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = e2m1x2(__fmul_rn(v[2 * i], e_b), __fmul_rn(v[2 * i + 1], e_b));
+    }
+    code_lo = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+    code_hi = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
+}
+
 __global__ void __launch_bounds__(kWtRows * kWtMaxSplit) weight_tail_cm_kernel(
     uint8_t* __restrict__ codes, int64_t ld_codes, uint8_t* __restrict__ sf, int64_t sf_cols, int64_t N, int K, int k,
     const nvq_tensor_scale* __restrict__ ts, const int32_t* __restrict__ idx, int idx_per_group,
     const uint8_t* __restrict__ cm_codes, const uint8_t* __restrict__ cm_sf, DeviceStatus* dst)
 {
     extern __shared__ __align__(16) uint8_t wt_smem[];
+    // per-group tables: E2M1 values, dequantization scale fl(sb * S_dec) and encode factor
+    // fl(S_enc / sb) of every E4M3 scale byte (the same operations as the direct forms)
+    __shared__ float v_tab[16], db_tab[128], eb_tab[128];
     const int kc = k < kWtChunk ? k : kWtChunk;   // channels staged at a time
     uint8_t* s_codes = wt_smem;                    // [kc][32]: rows n0 .. n0+63, two per byte
     uint8_t* s_sf = wt_smem + (size_t)kc * 32;     // [kc][64]
@@ -351,6 +375,12 @@ __global__ void __launch_bounds__(kWtRows * kWtMaxSplit) weight_tail_cm_kernel(
     const int64_t row = (int64_t)g * N + n0 + t;
     uint8_t* crow = codes + row * ld_codes + K / 2;
     const int cnt = k - c0 < kc ? k - c0 : kc;  // channels of this chunk (a multiple of 16)
+    for (int e = threadIdx.x; e < 128; e += nthr) {
+        const float sbv = e4m3_value((uint32_t)e);
+        db_tab[e] = __fmul_rn(sbv, s_dec);
+        eb_tab[e] = e == 0 ? 0.0f : encode_factor(s_enc, sbv);
+        if (e < 16) v_tab[e] = e2m1_value((uint32_t)e);
+    }
     // stage: per channel 2 x 16 code bytes + 4 x 16 scale bytes
     for (int w = threadIdx.x; w < cnt * 6; w += nthr) {
         const int c = w / 6, q = w % 6;
@@ -371,12 +401,13 @@ __global__ void __launch_bounds__(kWtRows * kWtMaxSplit) weight_tail_cm_kernel(
         for (int i = 0; i < 16; ++i) {
             const int c = b * 16 + i - c0;
             const uint32_t code = (s_codes[c * 32 + (t >> 1)] >> ((t & 1) * 4)) & 0xfu;
-            const uint32_t sb = s_sf[c * 64 + t];
-            wv[i] = __fmul_rn(e2m1_value(code), __fmul_rn(e4m3_value(sb), s_dec));
+            const uint32_t sb = s_sf[c * 64 + t] & 0x7fu;
+            wv[i] = __fmul_rn(v_tab[code], db_tab[sb]);  // fl(V[q] * fl(sb * S_dec))
         }
-        const BlockOut o = quantize16(wv, s_enc, s_dec);
-        *reinterpret_cast<uint2*>(crow + 8 * b) = make_uint2(o.code_lo, o.code_hi);
-        sf[sf_offset(row, nsb + b, sf_cols)] = (uint8_t)o.sb;
+        uint32_t osb, lo, hi;
+        quantize16_tab(wv, s_enc, eb_tab, osb, lo, hi);
+        *reinterpret_cast<uint2*>(crow + 8 * b) = make_uint2(lo, hi);
+        sf[sf_offset(row, nsb + b, sf_cols)] = (uint8_t)osb;
     }
     // scale padding of the row: by the thread that holds the row's last tail block
     if (c0 + kWtChunk < k || part != (b_end - 1 - c0 / 16) % split) return;
