@@ -341,6 +341,16 @@ __device__ __forceinline__ int checked_channel(int j, int K, DeviceStatus* st, i
     return j;
 }
 
+// The same check for unrolled gather loops, without a branch: an index outside [0, K) becomes
+// channel 0 and sets `bad`, which the caller reports once after the loop (a branch and an
+// atomic per index would hold every load of the loop behind its own check).
+__device__ __forceinline__ int clamp_channel(int j, int K, bool& bad)
+{
+    const bool out = (unsigned)j >= (unsigned)K;
+    bad |= out;
+    return out ? 0 : j;
+}
+
 // Bound of the wait, after another wait of the CTA ran out, for the asynchronous copies it
 // already issued to land before it exits (they complete within microseconds; this bound does
 // not shrink with the configurable limit, so even a tiny limit never lets a CTA exit while a

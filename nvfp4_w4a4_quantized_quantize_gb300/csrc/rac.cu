@@ -240,12 +240,13 @@ __global__ void __launch_bounds__(512) act_tail_kernel(const __nv_bfloat16* __re
     const int nsb = K / 16;
     const bool word_sf = (nsb % 4) == 0 && bsplit == 1;
     uint32_t sfw = 0;
+    bool bad = false;
     for (int b = part; b < k / 16; b += bsplit) {
         float xv[16];
         uint32_t sb[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const int j = (own && sel_smem) ? s_sel[b * 16 + i] : checked_channel(sel_g[b * 16 + i], K, dst, kWhereBadChannelAct);
+            const int j = (own && sel_smem) ? s_sel[b * 16 + i] : clamp_channel(sel_g[b * 16 + i], K, bad);
             xv[i] = ld_bf16_last_use(xr + j, pol);
             sb[i] = sf[sf_offset(row, j >> 4, sf_cols)];
         }
@@ -276,6 +277,7 @@ __global__ void __launch_bounds__(512) act_tail_kernel(const __nv_bfloat16* __re
             sf[sf_offset(row, nsb + b, sf_cols)] = (uint8_t)o.sb;
         }
     }
+    if (bad) report_status(dst, NVQ_ERR_ARG, kWhereBadChannelAct);
     const int64_t c0 = (K + k) / 16;
     if (word_sf && (c0 & 3)) {
         *reinterpret_cast<uint32_t*>(sf + sf_offset(row, c0 & ~3ll, sf_cols)) = sfw;  // rest of the group: padding
@@ -303,14 +305,16 @@ __global__ void __launch_bounds__(256) weight_tail_kernel(uint8_t* __restrict__ 
     const float s_enc = ts[g].s_enc, s_dec = ts[g].s_dec;
     const int32_t* sel = idx + (idx_per_group ? (int64_t)g * k : 0);
     const uint8_t* cr = codes + row * ld_codes;
+    bool bad = false;
     float wv[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        const int j = checked_channel(sel[b * 16 + i], K, dst, kWhereBadChannelWeight);
+        const int j = clamp_channel(sel[b * 16 + i], K, bad);
         const uint32_t c = (cr[j >> 1] >> ((j & 1) * 4)) & 0xfu;
         const uint32_t sb = sf[sf_offset(row, j >> 4, sf_cols)];
         wv[i] = __fmul_rn(e2m1_value(c), __fmul_rn(e4m3_value(sb), s_dec));
     }
+    if (bad) report_status(dst, NVQ_ERR_ARG, kWhereBadChannelWeight);
     BlockOut o = quantize16(wv, s_enc, s_dec);
     *reinterpret_cast<uint2*>(codes + row * ld_codes + (K + 16 * b) / 2) = make_uint2(o.code_lo, o.code_hi);
     sf[sf_offset(row, K / 16 + b, sf_cols)] = (uint8_t)o.sb;
@@ -564,8 +568,10 @@ __global__ void __launch_bounds__(kRowThreads)
 #pragma unroll
             for (int i = 0; i < 16; ++i) j[i] = __ldg(sel + i);
         }
+        bool bad = false;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) j[i] = checked_channel(j[i], K, dst, kResidual ? kWhereBadChannelAct : kWhereBadChannelWeight);
+        for (int i = 0; i < 16; ++i) j[i] = clamp_channel(j[i], K, bad);
+        if (bad) report_status(dst, NVQ_ERR_ARG, kResidual ? kWhereBadChannelAct : kWhereBadChannelWeight);
         const float* src = rt_smem + (size_t)r * stride;
         float v[16];
 #pragma unroll
