@@ -229,13 +229,6 @@ __device__ __forceinline__ BlockOut quantize16(const float* v, float s_enc, floa
     return o;
 }
 
-// Code of element i (0..15) from the packed block codes.
-__device__ __forceinline__ uint32_t block_code(const BlockOut& o, int i)
-{
-    uint32_t w = (i < 8) ? o.code_lo : o.code_hi;
-    return (w >> (4 * (i & 7))) & 0xfu;
-}
-
 // Residual r = fl(x - fl(V[q] * d_b)).
 __device__ __forceinline__ float residual(float x, uint32_t code, float d_b)
 {

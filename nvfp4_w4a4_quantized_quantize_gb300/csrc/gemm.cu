@@ -337,19 +337,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v)
-{
-    uint32_t pk[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-        pk[i] = *reinterpret_cast<uint32_t*>(&h);
-    }
-    uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) d[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-}
-
 // ------------------------------------------------------------------ tile scheduling
 struct Tile {
     int g;

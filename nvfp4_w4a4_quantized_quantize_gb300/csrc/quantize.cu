@@ -179,19 +179,6 @@ __device__ __forceinline__ void q_bulk_row(void* dst, const void* src, uint32_t 
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kQCompute) : "memory"); }
 
-// max |x| of a 16-element bf16 block (exact): a bf16x2 maximum tree over the sign-cleared words.
-__device__ __forceinline__ float amax_block(const uint4& w0, const uint4& w1)
-{
-    const uint32_t m = 0x7fff7fffu;
-    uint32_t u[8] = {w0.x & m, w0.y & m, w0.z & m, w0.w & m, w1.x & m, w1.y & m, w1.z & m, w1.w & m};
-    __nv_bfloat162 h[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) h[i] = *reinterpret_cast<__nv_bfloat162*>(&u[i]);
-    const __nv_bfloat162 r = __hmax2(__hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3])),
-                                     __hmax2(__hmax2(h[4], h[5]), __hmax2(h[6], h[7])));
-    return fmaxf(__low2float(r), __high2float(r));
-}
-
 // fl(a / 6) for a non-negative bf16 value a, without a division: the quotient estimate
 // q1 = fl(a * fl(1/6)) is corrected once with fused multiply-adds, as in Markstein's
 // FMA-based division (P. Markstein, "Computation of elementary functions on the IBM RISC
@@ -205,15 +192,6 @@ __device__ __forceinline__ float div6_bf16(float a)
     const float q1 = __fmul_rn(a, kInv6);
     const float r = __fmaf_rn(-q1, 6.0f, a);
     return __fmaf_rn(r, kInv6, q1);
-}
-
-// acc += rint(|r| * sc)^2 (sc = 2^(20-E), a normal power of two): one FMA puts the rounded
-// integer in the low mantissa bits, one multiply-add accumulates its square in 64 bits.
-__device__ __forceinline__ void score_acc(unsigned long long& acc, float r, float sc)
-{
-    const float y = __fmaf_rn(fabsf(r), sc, 8388608.0f);
-    const uint32_t q = __float_as_uint(y) & 0x7fffffu;
-    acc += (unsigned long long)q * q;  // one wide multiply-add
 }
 
 // max(|a|, |b|) of two bf16x2 words per half (exact; the sign bits of the result are the
