@@ -301,6 +301,13 @@ __device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b)
     return r;
 }
 
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 __device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b)
 {
     uint64_t r;

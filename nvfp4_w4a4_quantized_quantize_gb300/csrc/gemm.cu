@@ -337,6 +337,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// 2^x and 1/x on the special-function unit (approximate; |x| large gives inf / 0 as IEEE).
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 // ------------------------------------------------------------------ tile scheduling
 struct Tile {
     int g;
@@ -706,6 +721,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 mbar_arrive(&acc_empty);
             } else if (a.epilogue == NVQ_EPI_SWIGLU) {
                 // gate columns [half*64, +64), up columns [128 + half*64, +64) -> h columns [half*64, +64)
+                const uint64_t alpha2 = f2pack(alpha, alpha);
+                const uint64_t nlog2e2 = f2pack(-1.4426950408889634f, -1.4426950408889634f);  // -log2(e)
+                const uint64_t one2 = f2pack(1.0f, 1.0f);
                 uint32_t pk[32];
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
@@ -715,11 +733,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         tc_fence_before();
                         mbar_arrive(&acc_empty);
                     }
+                    // silu(g) u = g u / (1 + 2^(-g log2 e)), element pairs on the paired fp32
+                    // instructions (the epilogue is bound by instruction issue at two warps per
+                    // scheduler), the power of two and the reciprocal on the special-function unit
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float g0 = __fmul_rn(alpha, g[2 * i]), u0 = __fmul_rn(alpha, u[2 * i]);
-                        const float g1 = __fmul_rn(alpha, g[2 * i + 1]), u1 = __fmul_rn(alpha, u[2 * i + 1]);
-                        pk[16 * c + i] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u0, __fdividef(g1, 1.0f + __expf(-g1)) * u1);
+                        const uint64_t gp = f2mul(alpha2, f2pack(g[2 * i], g[2 * i + 1]));
+                        const uint64_t up = f2mul(alpha2, f2pack(u[2 * i], u[2 * i + 1]));
+                        float t0, t1;
+                        f2unpack(f2mul(gp, nlog2e2), t0, t1);
+                        float d0, d1;
+                        f2unpack(f2add(f2pack(ex2_approx(t0), ex2_approx(t1)), one2), d0, d1);
+                        float h0, h1;
+                        f2unpack(f2mul(f2mul(gp, f2pack(rcp_approx(d0), rcp_approx(d1))), up), h0, h1);
+                        pk[16 * c + i] = pack_bf16x2(h0, h1);
                     }
                 }
                 if (valid) store_row<32>(a.out + grow * a.ldo + (int64_t)T.nt * (kBN / 2) + half * 64, pk, wide);
