@@ -753,6 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 if (a.out_ts) warp_amax_to(valid ? amax_packed<32>(pk) : 0.0f, &a.out_ts[T.g].amax);
             } else {
                 const float sc = (a.epilogue == NVQ_EPI_ROW_SCALE) ? w : 1.0f;
+                const uint64_t alpha2 = f2pack(alpha, alpha), sc2 = f2pack(sc, sc);
                 uint32_t pk[64];
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
@@ -763,12 +764,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         mbar_arrive(&acc_empty);
                     }
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float y0 = __fmul_rn(alpha, v0[2 * i]), y1 = __fmul_rn(alpha, v0[2 * i + 1]);
-                        float z0 = __fmul_rn(alpha, v1[2 * i]), z1 = __fmul_rn(alpha, v1[2 * i + 1]);
+                    for (int i = 0; i < 16; ++i) {  // fl(fl(alpha acc) w), element pairs per instruction
+                        uint64_t yp = f2mul(alpha2, f2pack(v0[2 * i], v0[2 * i + 1]));
+                        uint64_t zp = f2mul(alpha2, f2pack(v1[2 * i], v1[2 * i + 1]));
                         if (a.epilogue == NVQ_EPI_ROW_SCALE) {
-                            y0 = __fmul_rn(y0, sc); y1 = __fmul_rn(y1, sc); z0 = __fmul_rn(z0, sc); z1 = __fmul_rn(z1, sc);
+                            yp = f2mul(yp, sc2);
+                            zp = f2mul(zp, sc2);
                         }
+                        float y0, y1, z0, z1;
+                        f2unpack(yp, y0, y1);
+                        f2unpack(zp, z0, z1);
                         pk[32 * c + i] = pack_bf16x2(y0, y1);
                         pk[32 * c + 16 + i] = pack_bf16x2(z0, z1);
                     }
