@@ -87,3 +87,12 @@ def test_binding_refuses_host_tensors():
     sf = torch.zeros(512, dtype=torch.uint8)
     with pytest.raises(ValueError, match="CUDA tensor"):
         Lmod.fp8_quantize(x, codes, sf, 4)
+
+
+@pytest.mark.parametrize("mmas,out", [(8, True), (1 << 21, True), (1024, False)])
+def test_mma_rate_probe_argument_errors(mmas, out):
+    """nvq_fp4_mma_rate refuses a loop shorter than 16 or longer than 2^20 MMAs per SM and a NULL
+    result pointer before it touches the GPU."""
+    v = C.c_float(0.0)
+    assert LIB.nvq_fp4_mma_rate(mmas, 0, C.byref(v) if out else None, None) == ARG
+    assert _err().startswith("nvq_fp4_mma_rate")
