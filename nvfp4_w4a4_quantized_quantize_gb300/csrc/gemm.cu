@@ -253,6 +253,40 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float* va,
     }
 }
 
+// Six 16-column accumulator loads (addresses t[0..5]), one wait: 96 values.
+__device__ __forceinline__ void tmem_ld16x6(const uint32_t* t, float* v)
+{
+    uint32_t r[96];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%96];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%97];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47}, [%98];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%99];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79}, [%100];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%101];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95])
+        : "r"(t[0]), "r"(t[1]), "r"(t[2]), "r"(t[3]), "r"(t[4]), "r"(t[5])
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 96; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Two 16-column accumulator loads, one wait: 32 values.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float* v)
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(ta), "r"(tb)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // 4 / 8 / 16 / 32 consecutive TMEM columns of this warp's 32 lanes from registers.
 __device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t* v)
 {
@@ -700,7 +734,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             if (!mbar_wait(&acc_full, acc_phase, a, abrt, 4)) break;
             tc_fence_after();
             const uint32_t tacc = tmem + kAccCol + lane_addr;
-            if (a.epilogue == NVQ_EPI_STORE_F32) {
+            // the staged instantiation runs only the routing-weight epilogue (launch_gemm): the
+            // fp32 and SwiGLU branches are compiled out of it, which keeps its registers
+            if (!kStaged && a.epilogue == NVQ_EPI_STORE_F32) {
                 float* orow = reinterpret_cast<float*>(a.out) + grow * a.ldo + (int64_t)T.nt * kBN + half * (kBN / 2);
 #pragma unroll 1
                 for (int c = 0; c < kBN / 2; c += 64) {
@@ -719,25 +755,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 }
                 tc_fence_before();
                 mbar_arrive(&acc_empty);
-            } else if (a.epilogue == NVQ_EPI_SWIGLU) {
+            } else if (!kStaged && a.epilogue == NVQ_EPI_SWIGLU) {
                 // gate columns [half*64, +64), up columns [128 + half*64, +64) -> h columns [half*64, +64)
                 const uint64_t alpha2 = f2pack(alpha, alpha);
                 const uint64_t nlog2e2 = f2pack(-1.4426950408889634f, -1.4426950408889634f);  // -log2(e)
                 const uint64_t one2 = f2pack(1.0f, 1.0f);
+                // the accumulator in 16-column pieces (gate and up halves of each): three pieces
+                // are read before any arithmetic, the first one's SwiGLU runs, the last piece is
+                // read and the accumulator released, so only a quarter of the arithmetic comes
+                // before the release
+                // silu(g) u = g u / (1 + 2^(-g log2 e)), element pairs on the paired fp32
+                // instructions (the epilogue is bound by instruction issue at two warps per
+                // scheduler), the power of two and the reciprocal on the special-function unit
                 uint32_t pk[32];
+                auto swiglu8 = [&](const float* g, const float* u, uint32_t* out) {
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    float g[32], u[32];
-                    tmem_ld32x2(tacc + half * 64 + 32 * c, tacc + kBN / 2 + half * 64 + 32 * c, g, u);
-                    if (c == 1) {  // released once the last piece is in registers
-                        tc_fence_before();
-                        mbar_arrive(&acc_empty);
-                    }
-                    // silu(g) u = g u / (1 + 2^(-g log2 e)), element pairs on the paired fp32
-                    // instructions (the epilogue is bound by instruction issue at two warps per
-                    // scheduler), the power of two and the reciprocal on the special-function unit
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
+                    for (int i = 0; i < 8; ++i) {
                         const uint64_t gp = f2mul(alpha2, f2pack(g[2 * i], g[2 * i + 1]));
                         const uint64_t up = f2mul(alpha2, f2pack(u[2 * i], u[2 * i + 1]));
                         float t0, t1;
@@ -746,8 +779,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         f2unpack(f2add(f2pack(ex2_approx(t0), ex2_approx(t1)), one2), d0, d1);
                         float h0, h1;
                         f2unpack(f2mul(f2mul(gp, f2pack(rcp_approx(d0), rcp_approx(d1))), up), h0, h1);
-                        pk[16 * c + i] = pack_bf16x2(h0, h1);
+                        out[i] = pack_bf16x2(h0, h1);
                     }
+                };
+                {
+                    float v[96];  // pieces 0..2: gate 16, up 16 each
+                    const uint32_t tg = tacc + half * 64, tu = tacc + kBN / 2 + half * 64;
+                    const uint32_t t6[6] = {tg, tu, tg + 16, tu + 16, tg + 32, tu + 32};
+                    tmem_ld16x6(t6, v);
+                    swiglu8(v, v + 16, pk);
+                    float w[32];  // piece 3
+                    tmem_ld16x2(tg + 48, tu + 48, w);
+                    tc_fence_before();
+                    mbar_arrive(&acc_empty);  // released: the rest overlaps the next tile's MMAs
+                    swiglu8(v + 32, v + 48, pk + 8);
+                    swiglu8(v + 64, v + 80, pk + 16);
+                    swiglu8(w, w + 16, pk + 24);
                 }
                 if (valid) store_row<32>(a.out + grow * a.ldo + (int64_t)T.nt * (kBN / 2) + half * 64, pk, wide);
                 if (a.out_ts) warp_amax_to(valid ? amax_packed<32>(pk) : 0.0f, &a.out_ts[T.g].amax);
